@@ -1,0 +1,436 @@
+"""Benchmark of the block-hybrid attention step on one B300 (or N replicas).
+
+Default workload: the continuous-batching step of one linearized layer —
+64 requests with 16 heads (d=128, f=64, L=32) and prefixes of 32*U{8..128}
+tokens held as fixed-size states; one hb_block_attend for all 64 requests
+plus an hb_commit_block for the 16 requests that finish their block. A step
+cycles through 6 independent layer instances (own W, gate, states and
+activations), as the 6 linearized layers of the model would, so that a
+layer's 80+ MB working set has left the 126 MB L2 by the time it comes back.
+
+Metric: active-block tokens/s (B*L per step) and the attend kernel's HBM
+GB/s against the measured peak. ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same step instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own 64 requests (weak scaling); rank 0
+prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-attn active-block tokens/s and HBM GB/s vs ~8 TB/s, 1 B300"
+UNIT = "tokens/s"
+N_LAYERS = 6
+B, H, D, FH, L, N_COMMIT = 64, 16, 128, 64, 32, 16
+F = 2 * FH
+
+# Algorithmic bytes of one hb_block_attend launch at this shape: per request
+# the state S (F*d fp32) and Z (F fp32), q/k/v (3*L*H*d bf16) and o (L*H*d
+# bf16); W (H*d*f bf16) once per launch.
+ATTEND_BYTES_PER_REQUEST = H * (F * D * 4 + F * 4) + 4 * L * H * D * 2
+ATTEND_BYTES_W = H * D * FH * 2
+# hb_commit_block: read and write S and Z, read k/v; W once.
+COMMIT_BYTES_PER_REQUEST = H * 2 * (F * D * 4 + F * 4) + 2 * L * H * D * 2
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world: int):
+    """Max of the per-rank step times and sum of the units over ranks."""
+    if world == 1:
+        return local_ms, local_units
+    import torch.distributed as dist
+
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    u = torch.tensor([local_units], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t, u = t.cuda(), u.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
+def _traffic(kernel: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if
+    the summary was taken on the kernel source as it is now."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    from linear_attention_diffusion_feature_b300 import build
+
+    if rec.get("source_sha") != build.source_digest():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def make_layers(device):
+    """6 independent layer instances of the continuous-batching workload, with
+    states built by hb_prefill_state from each layer's own prefixes."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    layers = []
+    cfg = hb.Config(H, D, FH, L, dtype=hb.DTYPE_BF16, merge=hb.MERGE_SHARED_NORM)
+    for layer in range(N_LAYERS):
+        w = inputs.continuous_batching(seed=2 + 100 * layer, device=device, B=B, n_commit=N_COMMIT)
+        t = w.tensors
+        S = torch.empty((B, H, F, D), dtype=torch.float32, device=device)
+        Z = torch.empty((B, H, F), dtype=torch.float32, device=device)
+        sl = torch.arange(B, dtype=torch.int32, device=device)
+        hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                            w.meta["max_prefix"], t["W"], S, Z)
+        ci = t["commit_idx"]
+        layers.append(dict(
+            W=t["W"], gate=t["gate"], q=t["q"], k=t["k"], v=t["v"], S=S, Z=Z, slots=sl,
+            o=torch.empty_like(t["q"]), commit_slots=sl[ci].contiguous(),
+            commit_k=t["k"][ci].contiguous(), commit_v=t["v"][ci].contiguous(),
+            mean_prefix=float(w.meta["total_prefix"]) / B))
+        del t["prefix_k"], t["prefix_v"]
+    torch.cuda.synchronize()
+    assert hb.hb_get_device_status() == 0
+    return cfg, layers
+
+
+def run_ours(args, world, rank, local):
+    import linear_attention_diffusion_feature_b300 as hb
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg, layers = make_layers(device)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        ly = layers[i % N_LAYERS]
+        if ev is not None:
+            ev[0].record(stream)
+        hb.hb_block_attend(cfg, ly["slots"], ly["q"], ly["k"], ly["v"], ly["S"], ly["Z"],
+                           ly["W"], ly["gate"], o=ly["o"])
+        if ev is not None:
+            ev[1].record(stream)
+        hb.hb_commit_block(cfg, ly["commit_slots"], ly["commit_k"], ly["commit_v"], ly["W"],
+                           ly["S"], ly["Z"])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    _barrier(world)
+
+    # timed region: K steps, events around every attend launch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        _barrier(world)
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+    total_ms = start.elapsed_time(end)
+    attend_ms = [a.elapsed_time(b) for a, b in evs]
+    status = hb.hb_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {hb.hb_status_string(status)}")
+    ms_per_step, units = aggregate(total_ms / args.steps, B * L, world)
+    value = units / (ms_per_step / 1e3)
+
+    attend_avg_ms = sum(attend_ms) / len(attend_ms)
+    attend_bytes = B * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W
+    achieved = attend_bytes / (attend_avg_ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+
+    e2e = run_e2e(args, cfg, layers, device)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": "continuous-batching step of one linearized layer: 64 requests, "
+                        "16 heads, d=128, f=64 (F=128), L=32, prefixes 32*U{8..128} tokens as "
+                        "fp32 states; attend all 64 + commit 16",
+            "batch": B, "block_len": L, "heads": H, "head_dim": D, "feat_half": FH,
+            "commit_per_step": N_COMMIT, "merge": "shared_norm",
+            "mean_prefix_tokens": layers[0]["mean_prefix"],
+            "l2": f"steps cycle through {N_LAYERS} independent layer instances "
+                  f"({N_LAYERS} x ~{(B * ATTEND_BYTES_PER_REQUEST) / 1e6:.0f} MB > 126 MB L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "kernel": "hb_block_attend", "bound": "hbm", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": attend_bytes,
+            "launch_ms": attend_avg_ms,
+            "traffic": _traffic("hb_block_attend"),
+        },
+        "components": {
+            "attend_ms": attend_avg_ms,
+            "commit_ms_est": ms_per_step - attend_avg_ms,
+            "attend_tokens_per_s": B * L / (attend_avg_ms / 1e3),
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, cfg, layers, device):
+    """Same step through the binding with pinned host buffers: every step
+    copies that step's activations host->device and reads o back."""
+    import linear_attention_diffusion_feature_b300 as hb
+
+    ly0 = layers[0]
+    host = {name: ly0[name].cpu().pin_memory() for name in ("q", "k", "v", "commit_k", "commit_v")}
+    host_o = torch.empty_like(host["q"]).pin_memory()
+    dev = {name: torch.empty_like(ly0[name]) for name in host}
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_o.numel() * host_o.element_size()
+
+    def step(i):
+        ly = layers[i % N_LAYERS]
+        for name in host:
+            dev[name].copy_(host[name], non_blocking=True)
+        hb.hb_block_attend(cfg, ly["slots"], dev["q"], dev["k"], dev["v"], ly["S"], ly["Z"],
+                           ly["W"], ly["gate"], o=ly["o"])
+        hb.hb_commit_block(cfg, ly["commit_slots"], dev["commit_k"], dev["commit_v"], ly["W"],
+                           ly["S"], ly["Z"])
+        host_o.copy_(ly["o"], non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    return {"value": B * L / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+# ----------------------------------------------------------- CPU oracle arm
+
+def _oracle_sample(n_req: int, seed: int = 2):
+    """A bounded sample of the step for the oracle: ``n_req`` requests of the
+    same workload recipe, their states from the oracle's own prefill (outside
+    the timed region), and a quarter of them committing."""
+    import numpy as np
+
+    import oracle.block_hybrid as ob
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    w = inputs.continuous_batching(seed=seed, device="cpu", B=n_req,
+                                   n_commit=max(1, n_req // 4))
+    t = {k: (v.to(torch.float64).numpy() if v.is_floating_point() else v.numpy())
+         for k, v in w.tensors.items()}
+    cu = t["cu_prefix"]
+    states = [ob.prefill(t["prefix_k"][cu[b]:cu[b + 1]], t["prefix_v"][cu[b]:cu[b + 1]], t["W"])
+              for b in range(n_req)]
+    commit = set(np.asarray(t["commit_idx"]).tolist())
+    return ob, t, states, commit
+
+
+def _oracle_step(ob, t, states, commit):
+    for b, (S, Z) in enumerate(states):
+        ob.attend(t["q"][b], t["k"][b], t["v"][b], S, Z, t["W"], t["gate"], ob.MERGE_SHARED_NORM)
+        if b in commit:
+            ob.commit(S, Z, t["k"][b], t["v"][b], t["W"])
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:  # noqa: BLE001
+        return 1
+
+
+def cpu_baseline(max_seconds: float = 15.0, n_req: int = 8):
+    ob, t, states, commit = _oracle_sample(n_req)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_step(ob, t, states, commit)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= max_seconds or reps >= 1000:
+            break
+    tokens = reps * n_req * L
+    return {"value": tokens / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{reps} repetitions of the step restricted to {n_req} requests "
+                      f"({len(commit)} committing), fp64 numpy oracle, {el:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    n_req = 8
+    ob, t, states, commit = _oracle_sample(n_req)
+    for _ in range(args.warmup):
+        _oracle_step(ob, t, states, commit)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(ob, t, states, commit)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = n_req * L / (ms / 1e3)
+    cores = _blas_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "continuous-batching step (oracle sample)", "batch": n_req,
+                   "block_len": L, "heads": H, "head_dim": D, "feat_half": FH},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {n_req} requests' attend + {len(commit)} commits"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=6)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

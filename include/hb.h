@@ -1,0 +1,240 @@
+/*
+ * hb.h — C ABI of the block-hybrid attention library (libhb.so), sm_103a.
+ *
+ * Block-hybrid attention, as described for arXiv 2608.06628 ("Retrofitting
+ * Linear Attention into Diffusion Language Models"; gist.science technical
+ * summary, "Methodology: Block-Hybrid Attention / Architecture Design";
+ * pith.science review, "What carries the argument"): inside a linearized
+ * layer, every query of the active denoising block gets exact bidirectional
+ * softmax attention over the block and a linear-attention read of a
+ * fixed-size per-head state (S, Z) that summarises every committed token
+ * through the Hedgehog feature map phi(x) = [softmax(xW), softmax(-xW)].
+ * A per-head scalar gate merges the two branches.
+ *
+ * Notation: B requests in a call, L tokens in the active block, H heads,
+ * d head dimension, f width of one softmax half, F = 2f.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.      Every pointer except `cfg` is a DEVICE pointer on the current
+ *              CUDA device, owned by the caller, 16-byte aligned. The library
+ *              allocates nothing; the only device memory it owns is a
+ *              file-scope status word per device.
+ * Layouts.     Row-major, outermost index first. Activations (q, k, v, o, x)
+ *              are [tokens, H, d] of the activation dtype (`cfg->dtype`).
+ *              W is [H, d, f] of the activation dtype. The state pool is
+ *              S_pool [num_slots, H, F, d] and Z_pool [num_slots, H, F], fp32.
+ *              Within a half of phi, index c < f is softmax(xW)_c and index
+ *              f + c is softmax(-xW)_c.
+ * Streams.     Every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *              the legacy default stream). No call synchronises except
+ *              hb_get_device_status.
+ * Errors.      Arguments are validated on the host before anything is
+ *              launched; a rejected call returns a non-zero hb_status and has
+ *              no effect. batch == 0 (or n_tokens == 0) is a valid no-op.
+ *              A launch failure returns HB_ERR_CUDA. Faults that only the
+ *              device can see (a slot index outside [0, num_slots), a
+ *              bounded wait that ran out) never trap: the affected block of
+ *              work is skipped, a bit is set in the device status word, and
+ *              hb_get_device_status reports it.
+ * Shapes.      1 <= H <= 1024; d in {16, 32, ..., 128}; f in {8, 16, ..., 64};
+ *              1 <= L <= 64.
+ * Determinism. No atomics touch S, Z or outputs; repeated calls on the same
+ *              inputs give bitwise-identical results.
+ * Threads.     The library keeps no per-call host state; calls from several
+ *              host threads are safe.
+ */
+#ifndef HB_H_
+#define HB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* hb_stream_t; /* same object as cudaStream_t */
+
+typedef enum hb_status {
+  HB_OK = 0,
+  HB_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum     */
+  HB_ERR_UNSUPPORTED_SHAPE = 2, /* H, d, f or L outside the supported set    */
+  HB_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned          */
+  HB_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed      */
+  HB_ERR_DEVICE_BOUNDS = 5,     /* device saw a slot index out of range      */
+  HB_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out        */
+  HB_ERR_WORKSPACE = 7          /* workspace too small for the request       */
+} hb_status;
+
+typedef enum hb_dtype {
+  HB_DTYPE_BF16 = 0, /* activations and W in bfloat16, fp32 arithmetic      */
+  HB_DTYPE_FP32 = 1  /* everything fp32 (accuracy mode)                      */
+} hb_dtype;
+
+/*
+ * Merge of the two branches for query i of head h (s_ij = scale * q_i.k_j,
+ * sums over the L block tokens j; num_i = phi(q_i)^T S, den_i = phi(q_i)^T Z):
+ *
+ * HB_MERGE_SHARED_NORM — the pages' form (gist.science technical summary,
+ *   merging bullet: one shared normaliser and a learned scalar gate;
+ *   pith.science review, comment on the Section 3.1 out(q) equation: the
+ *   gate w = sigmoid(alpha_h) scales only the softmax numerator and
+ *   denominator):
+ *       o_i = (w sum_j e^{s_ij} v_j + num_i) / (w sum_j e^{s_ij} + den_i)
+ *   evaluated in a rescaled form that cannot overflow.
+ * HB_MERGE_CONVEX — a convex blend of the two normalised branches:
+ *       o_i = sigmoid(g_h) softmax_j(s_ij) v + (1 - sigmoid(g_h)) num_i / den_i
+ *   and, while nothing is committed (den_i == 0), o_i = softmax_j(s_ij) v.
+ */
+typedef enum hb_merge {
+  HB_MERGE_SHARED_NORM = 0,
+  HB_MERGE_CONVEX = 1
+} hb_merge;
+
+typedef struct hb_config {
+  int32_t num_heads; /* H                                   */
+  int32_t head_dim;  /* d                                   */
+  int32_t feat_half; /* f (F = 2f)                          */
+  int32_t block_len; /* L                                   */
+  int32_t dtype;     /* hb_dtype                            */
+  int32_t merge;     /* hb_merge                            */
+  float scale;       /* block softmax scale; 0 => 1/sqrt(d) */
+} hb_config;
+
+/*
+ * hb_feature_map — phi(x) = [softmax(x W_h), softmax(-x W_h)] for every token
+ * and head (gist.science technical summary, cross-block bullet; pith.science
+ * review, "What carries the argument").
+ *   x   [n_tokens, H, d]  activation dtype
+ *   W   [H, d, f]         activation dtype
+ *   phi [n_tokens, H, 2f] fp32, written
+ * Each half of every output row sums to 1.
+ */
+hb_status hb_feature_map(const hb_config* cfg, int64_t n_tokens, const void* x,
+                         const void* W, float* phi, hb_stream_t stream);
+
+/*
+ * hb_block_attend — one denoising step of a block-hybrid layer for `batch`
+ * requests (gist.science technical summary, within-block, cross-block,
+ * state-compression and merging bullets; pith.science review, "What carries
+ * the argument": the cross-block read costs O(Fd) per query whatever the
+ * prefix length).
+ *   slot_idx     [batch] int32: request b reads state slot slot_idx[b]
+ *   q, k, v      [batch, L, H, d] activation dtype: the active block
+ *   S_pool       [num_slots, H, F, d] fp32, read only
+ *   Z_pool       [num_slots, H, F] fp32, read only
+ *   W            [H, d, f] activation dtype (one W per head for q and k)
+ *   gate_logits  [H] fp32: alpha_h (SHARED_NORM) or g_h (CONVEX)
+ *   o            [batch, L, H, d] activation dtype, written
+ * A request whose slot is out of range gets no output written and sets
+ * HB_ERR_DEVICE_BOUNDS in the status word.
+ */
+hb_status hb_block_attend(const hb_config* cfg, int32_t batch,
+                          const int32_t* slot_idx, const void* q,
+                          const void* k, const void* v, const float* S_pool,
+                          const float* Z_pool, int32_t num_slots,
+                          const void* W, const float* gate_logits, void* o,
+                          hb_stream_t stream);
+
+/*
+ * hb_commit_block — fold a finished block into the state (gist.science
+ * technical summary, state-compression bullet: the states change only when a
+ * block is committed; pith.science review, "What carries the argument":
+ * S_n = S_{n-1} + sum_t phi(k_t) v_t^T, Z_n = Z_{n-1} + sum_t phi(k_t)).
+ *   slot_idx [batch] int32, distinct slots (two requests writing one slot race)
+ *   k, v     [batch, L, H, d] activation dtype: the committed block
+ *   W        [H, d, f]
+ *   S_pool, Z_pool updated in place for the listed slots only.
+ */
+hb_status hb_commit_block(const hb_config* cfg, int32_t batch,
+                          const int32_t* slot_idx, const void* k,
+                          const void* v, const void* W, float* S_pool,
+                          float* Z_pool, int32_t num_slots, hb_stream_t stream);
+
+/*
+ * hb_prefill_state — ingest prompts as committed context: the same sums as
+ * hb_commit_block over every prompt token (the prompt precedes the first
+ * generated block, so it is committed context; the sums are order-free, so
+ * the chunking does not change the result).
+ *   k, v        [total_tokens, H, d] activation dtype, requests packed
+ *               back to back (NULL allowed when total_tokens == 0)
+ *   cu_seqlens  [batch + 1] int64, device: request b owns token rows
+ *               [cu_seqlens[b], cu_seqlens[b+1]); a request whose rows fall
+ *               outside [0, total_tokens) is skipped and flagged as
+ *               HB_ERR_DEVICE_BOUNDS
+ *   max_seqlen  host upper bound on any request's length (sizes the grid).
+ *               A request longer than max_seqlen, or with a negative length,
+ *               is skipped (its slot is left untouched) and flagged as
+ *               HB_ERR_DEVICE_BOUNDS
+ *   accumulate  0: S, Z of each slot are overwritten with the prompt's sums;
+ *               1: the sums are added to what the slot holds
+ *   workspace   device scratch of hb_prefill_workspace_size() bytes or more
+ *               (NULL allowed when that size is 0); contents need not be
+ *               initialised and are clobbered
+ */
+hb_status hb_prefill_state(const hb_config* cfg, int32_t batch,
+                           const int32_t* slot_idx, const void* k,
+                           const void* v, int64_t total_tokens,
+                           const int64_t* cu_seqlens, int64_t max_seqlen, const void* W, float* S_pool,
+                           float* Z_pool, int32_t num_slots,
+                           int32_t accumulate, void* workspace,
+                           size_t workspace_bytes, hb_stream_t stream);
+
+/* Bytes of workspace hb_prefill_state needs for this shape (may be 0).
+ * Returns 0 as well for arguments hb_prefill_state would reject. */
+size_t hb_prefill_workspace_size(const hb_config* cfg, int32_t batch,
+                                 int64_t max_seqlen);
+
+/* hb_state_zero — clear S and Z of the listed slots (a new request with no
+ * prompt, or a finished request's slot being recycled). */
+hb_status hb_state_zero(const hb_config* cfg, int32_t batch,
+                        const int32_t* slot_idx, float* S_pool, float* Z_pool,
+                        int32_t num_slots, hb_stream_t stream);
+
+/*
+ * hb_softmax_kv_attend — the full-prefix softmax attention that block-hybrid
+ * attention replaces (arXiv abstract: every denoising step still attends to
+ * all previous blocks; gist.science technical summary, problem statement).
+ * Comparison path only. Query i of request b attends, unmasked, to the
+ * request's P_b cached keys followed by the L keys of its active block.
+ *   k_cache, v_cache [total_prefix, H, d] activation dtype, packed per request
+ *                    (NULL allowed when total_prefix == 0)
+ *   cu_prefix        [batch + 1] int64, device (P_b = cu_prefix[b+1]-cu_prefix[b]);
+ *                    rows outside [0, total_prefix) are flagged, never read
+ *   max_prefix       host upper bound on any P_b (sizes the grid); a request
+ *                    with P_b > max_prefix or P_b < 0 gets no output written
+ *                    and is flagged as HB_ERR_DEVICE_BOUNDS
+ *   q, k, v          [batch, L, H, d]; o [batch, L, H, d] written
+ *   workspace        device scratch of hb_softmax_kv_workspace_size() bytes
+ */
+hb_status hb_softmax_kv_attend(const hb_config* cfg, int32_t batch,
+                               const void* k_cache, const void* v_cache,
+                               int64_t total_prefix, const int64_t* cu_prefix,
+                               int64_t max_prefix,
+                               const void* q, const void* k, const void* v,
+                               void* o, void* workspace,
+                               size_t workspace_bytes, hb_stream_t stream);
+
+/* Bytes of workspace hb_softmax_kv_attend needs for this shape (may be 0). */
+size_t hb_softmax_kv_workspace_size(const hb_config* cfg, int32_t batch,
+                                    int64_t max_prefix);
+
+/*
+ * hb_get_device_status — synchronise `stream`, then read and clear the
+ * current device's status word. Returns HB_OK when no device-side fault was
+ * recorded since the last call, else HB_ERR_DEVICE_BOUNDS or HB_ERR_TIMEOUT
+ * (bounds first when both were seen), or HB_ERR_CUDA if the synchronisation
+ * itself failed.
+ */
+hb_status hb_get_device_status(hb_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* hb_status_string(hb_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HB_H_ */

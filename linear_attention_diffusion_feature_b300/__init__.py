@@ -1,0 +1,26 @@
+"""Block-hybrid attention for blockwise diffusion language models on B300.
+
+Exact bidirectional softmax within the active block, a Hedgehog linear read
+of a fixed-size per-head state for all committed blocks, and a gated merge,
+as hand-written sm_103a CUDA kernels behind the C ABI of ``libhb.so``
+(``include/hb.h``). This package is the Python binding of that library.
+"""
+
+from .hb import (  # noqa: F401
+    DTYPE_BF16,
+    DTYPE_FP32,
+    MERGE_CONVEX,
+    MERGE_SHARED_NORM,
+    Config,
+    HBError,
+    hb_block_attend,
+    hb_commit_block,
+    hb_feature_map,
+    hb_get_device_status,
+    hb_prefill_state,
+    hb_prefill_workspace_size,
+    hb_softmax_kv_attend,
+    hb_softmax_kv_workspace_size,
+    hb_state_zero,
+    hb_status_string,
+)

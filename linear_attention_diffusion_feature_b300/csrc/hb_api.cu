@@ -1,0 +1,280 @@
+// The C ABI of libhb.so (include/hb.h): host-side validation, the per-device
+// status word, and dispatch to the kernels. No entry point allocates memory
+// or synchronises, except hb_get_device_status.
+#include <math.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "hb_fast.cuh"
+#include "hb_internal.cuh"
+
+namespace hb {
+
+// Device-side fault bits (kStatusBounds, kStatusTimeout). One instance per
+// device context; kernels receive its device address as an argument.
+__device__ unsigned g_status_word;
+
+namespace {
+
+std::mutex g_mu;
+
+cudaError_t status_word_ptr(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::map<int, unsigned*> cache;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_status_word);
+  if (e != cudaSuccess) return e;
+  cache[dev] = static_cast<unsigned*>(p);
+  *out = static_cast<unsigned*>(p);
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+hb_status check_config(const hb_config* c, Shape* s) {
+  if (!c) return HB_ERR_INVALID_ARG;
+  if (c->dtype != HB_DTYPE_BF16 && c->dtype != HB_DTYPE_FP32) return HB_ERR_INVALID_ARG;
+  if (c->merge != HB_MERGE_SHARED_NORM && c->merge != HB_MERGE_CONVEX) return HB_ERR_INVALID_ARG;
+  if (!(c->scale >= 0.f) || isinf(c->scale)) return HB_ERR_INVALID_ARG;
+  if (c->num_heads < 1 || c->num_heads > 1024) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (c->head_dim < 16 || c->head_dim > 128 || c->head_dim % 16) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (c->feat_half < 8 || c->feat_half > 64 || c->feat_half % 8) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (c->block_len < 1 || c->block_len > 64) return HB_ERR_UNSUPPORTED_SHAPE;
+  s->H = c->num_heads;
+  s->d = c->head_dim;
+  s->f = c->feat_half;
+  s->F = 2 * c->feat_half;
+  s->L = c->block_len;
+  s->scale = c->scale > 0.f ? c->scale : 1.f / sqrtf((float)c->head_dim);
+  s->dtype = c->dtype;
+  s->merge = c->merge;
+  return HB_OK;
+}
+
+// All listed pointers non-null and 16-byte aligned.
+hb_status check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p) return HB_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return HB_ERR_MISALIGNED;
+  return HB_OK;
+}
+
+hb_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HB_OK : HB_ERR_CUDA; }
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* fn, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& have = done[{fn, dev}];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+}  // namespace hb
+
+using hb::Shape;
+
+extern "C" {
+
+hb_status hb_feature_map(const hb_config* cfg, int64_t n_tokens, const void* x, const void* W,
+                         float* phi, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (n_tokens < 0) return HB_ERR_INVALID_ARG;
+  if ((r = hb::check_ptrs({W})) != HB_OK) return r;
+  if (n_tokens == 0) return HB_OK;
+  if ((r = hb::check_ptrs({x, phi})) != HB_OK) return r;
+  if (n_tokens > (int64_t)16 * 0x7fffffff) return HB_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_feature_map_ok(s))
+    return hb::from_cuda(hb::launch_feature_map_fast(s, n_tokens, x, W, phi, st));
+  return hb::from_cuda(hb::launch_feature_map_generic(s, n_tokens, x, W, phi, st));
+}
+
+hb_status hb_block_attend(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                          const void* q, const void* k, const void* v, const float* S_pool,
+                          const float* Z_pool, int32_t num_slots, const void* W,
+                          const float* gate_logits, void* o, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits, o})) != HB_OK)
+    return r;
+  unsigned* status = nullptr;
+  cudaError_t e = hb::status_word_ptr(&status);
+  if (e != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_attend_ok(s))
+    return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
+                                                num_slots, W, gate_logits, o, status, st));
+  return hb::from_cuda(hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
+                                                 num_slots, W, gate_logits, o, status, st));
+}
+
+hb_status hb_commit_block(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                          const void* k, const void* v, const void* W, float* S_pool,
+                          float* Z_pool, int32_t num_slots, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, k, v, W, S_pool, Z_pool})) != HB_OK) return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_state_ok(s))
+    return hb::from_cuda(hb::launch_commit_fast(s, batch, slot_idx, k, v, W, S_pool, Z_pool,
+                                                num_slots, status, st));
+  return hb::from_cuda(hb::launch_state_accumulate_generic(
+      s, batch, slot_idx, k, v, (int64_t)batch * s.L, nullptr, s.L, W, S_pool, Z_pool,
+      num_slots, 1, status, st));
+}
+
+size_t hb_prefill_workspace_size(const hb_config* cfg, int32_t batch, int64_t max_seqlen) {
+  Shape s;
+  if (hb::check_config(cfg, &s) != HB_OK || batch <= 0 || max_seqlen < 0) return 0;
+  return hb::fast_state_ok(s) ? hb::prefill_fast_workspace_bytes(s, batch, max_seqlen) : 0;
+}
+
+hb_status hb_prefill_state(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                           const void* k, const void* v, int64_t total_tokens,
+                           const int64_t* cu_seqlens, int64_t max_seqlen, const void* W, float* S_pool, float* Z_pool,
+                           int32_t num_slots, int32_t accumulate, void* workspace,
+                           size_t workspace_bytes, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0 || max_seqlen < 0 || total_tokens < 0) return HB_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, cu_seqlens, W, S_pool, Z_pool})) != HB_OK) return r;
+  // k/v may be absent when there are no prompt tokens at all.
+  if (total_tokens > 0 && (r = hb::check_ptrs({k, v})) != HB_OK) return r;
+  const size_t need = hb_prefill_workspace_size(cfg, batch, max_seqlen);
+  if (need > 0) {
+    if (workspace_bytes < need) return HB_ERR_WORKSPACE;
+    if ((r = hb::check_ptrs({workspace})) != HB_OK) return r;
+  }
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_state_ok(s))
+    return hb::from_cuda(hb::launch_prefill_fast(s, batch, slot_idx, k, v, total_tokens,
+                                                 cu_seqlens, max_seqlen,
+                                                 W, S_pool, Z_pool, num_slots, accumulate,
+                                                 workspace, status, st));
+  return hb::from_cuda(hb::launch_state_accumulate_generic(s, batch, slot_idx, k, v, total_tokens,
+                                                           cu_seqlens, max_seqlen, W, S_pool,
+                                                           Z_pool,
+                                                           num_slots, accumulate, status, st));
+}
+
+hb_status hb_state_zero(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                        float* S_pool, float* Z_pool, int32_t num_slots, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, S_pool, Z_pool})) != HB_OK) return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  return hb::from_cuda(hb::launch_state_zero(s, batch, slot_idx, S_pool, Z_pool, num_slots,
+                                             status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t hb_softmax_kv_workspace_size(const hb_config* cfg, int32_t batch, int64_t max_prefix) {
+  Shape s;
+  if (hb::check_config(cfg, &s) != HB_OK || batch <= 0 || max_prefix < 0) return 0;
+  return hb::fast_softmax_kv_ok(s) ? hb::softmax_kv_fast_workspace_bytes(s, batch, max_prefix)
+                                   : 0;
+}
+
+hb_status hb_softmax_kv_attend(const hb_config* cfg, int32_t batch, const void* k_cache,
+                               const void* v_cache, int64_t total_prefix,
+                               const int64_t* cu_prefix, int64_t max_prefix,
+                               const void* q, const void* k, const void* v, void* o,
+                               void* workspace, size_t workspace_bytes, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || max_prefix < 0 || total_prefix < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({cu_prefix, q, k, v, o})) != HB_OK) return r;
+  if (total_prefix > 0 && (r = hb::check_ptrs({k_cache, v_cache})) != HB_OK) return r;
+  const size_t need = hb_softmax_kv_workspace_size(cfg, batch, max_prefix);
+  if (need > 0) {
+    if (workspace_bytes < need) return HB_ERR_WORKSPACE;
+    if ((r = hb::check_ptrs({workspace})) != HB_OK) return r;
+  }
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_softmax_kv_ok(s))
+    return hb::from_cuda(hb::launch_softmax_kv_fast(s, batch, k_cache, v_cache, total_prefix,
+                                                    cu_prefix,
+                                                    max_prefix, q, k, v, o, workspace, status,
+                                                    st));
+  return hb::from_cuda(hb::launch_softmax_kv_generic(s, batch, k_cache, v_cache, total_prefix,
+                                                     cu_prefix,
+                                                     max_prefix, q, k, v, o, status, st));
+}
+
+hb_status hb_get_device_status(hb_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return HB_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, hb::g_status_word, sizeof(word)) != cudaSuccess)
+    return HB_ERR_CUDA;
+  if (word) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(hb::g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+      return HB_ERR_CUDA;
+  }
+  if (word & hb::kStatusBounds) return HB_ERR_DEVICE_BOUNDS;
+  if (word & hb::kStatusTimeout) return HB_ERR_TIMEOUT;
+  return HB_OK;
+}
+
+const char* hb_status_string(hb_status status) {
+  switch (status) {
+    case HB_OK: return "ok";
+    case HB_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
+    case HB_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (H, d, f or L)";
+    case HB_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case HB_ERR_CUDA: return "CUDA runtime error";
+    case HB_ERR_DEVICE_BOUNDS: return "device saw an index or length out of range";
+    case HB_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case HB_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

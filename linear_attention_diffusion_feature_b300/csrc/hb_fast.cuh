@@ -1,0 +1,43 @@
+// Tensor-core kernels of block-hybrid attention for the production shape
+// (bf16 activations, d = 128, f = 64, F = 128, L = 32) and their dispatch
+// predicates. Every other shape or dtype goes to the generic kernels.
+#pragma once
+
+#include "hb_internal.cuh"
+
+namespace hb {
+
+inline bool production_shape(const Shape& s) {
+  return s.dtype == HB_DTYPE_BF16 && s.d == 128 && s.f == 64 && s.L == 32;
+}
+
+bool fast_feature_map_ok(const Shape& s);
+bool fast_attend_ok(const Shape& s);
+bool fast_state_ok(const Shape& s);
+bool fast_softmax_kv_ok(const Shape& s);
+
+cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, const void* W,
+                                    float* phi, cudaStream_t st);
+cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
+                               const void* k, const void* v, const float* S_pool,
+                               const float* Z_pool, int num_slots, const void* W,
+                               const float* gate, void* o, unsigned* status, cudaStream_t st);
+cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                               const void* v, const void* W, float* S_pool, float* Z_pool,
+                               int num_slots, unsigned* status, cudaStream_t st);
+size_t prefill_fast_workspace_bytes(const Shape& s, int batch, int64_t max_seqlen);
+cudaError_t launch_prefill_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                                const void* v, int64_t total_tokens, const int64_t* cu_seqlens,
+                                int64_t max_seqlen,
+                                const void* W, float* S_pool, float* Z_pool, int num_slots,
+                                int accumulate, void* workspace, unsigned* status,
+                                cudaStream_t st);
+size_t softmax_kv_fast_workspace_bytes(const Shape& s, int batch, int64_t max_prefix);
+cudaError_t launch_softmax_kv_fast(const Shape& s, int batch, const void* k_cache,
+                                   const void* v_cache, int64_t total_prefix,
+                                   const int64_t* cu_prefix,
+                                   int64_t max_prefix, const void* q, const void* k,
+                                   const void* v, void* o, void* workspace, unsigned* status,
+                                   cudaStream_t st);
+
+}  // namespace hb

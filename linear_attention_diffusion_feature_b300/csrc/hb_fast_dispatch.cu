@@ -1,0 +1,39 @@
+// Dispatch predicates of the tensor-core kernels. A predicate turns true once
+// its kernel exists and has passed parity against the oracle; until then the
+// generic kernels serve that entry point.
+#include "hb_fast.cuh"
+
+namespace hb {
+
+bool fast_feature_map_ok(const Shape&) { return false; }
+bool fast_attend_ok(const Shape&) { return false; }
+bool fast_state_ok(const Shape&) { return false; }
+bool fast_softmax_kv_ok(const Shape&) { return false; }
+
+cudaError_t launch_feature_map_fast(const Shape&, int64_t, const void*, const void*, float*,
+                                    cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_attend_fast(const Shape&, int, const int32_t*, const void*, const void*,
+                               const void*, const float*, const float*, int, const void*,
+                               const float*, void*, unsigned*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+cudaError_t launch_commit_fast(const Shape&, int, const int32_t*, const void*, const void*,
+                               const void*, float*, float*, int, unsigned*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+size_t prefill_fast_workspace_bytes(const Shape&, int, int64_t) { return 0; }
+cudaError_t launch_prefill_fast(const Shape&, int, const int32_t*, const void*, const void*,
+                                int64_t, const int64_t*, int64_t, const void*, float*, float*, int, int,
+                                void*, unsigned*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+size_t softmax_kv_fast_workspace_bytes(const Shape&, int, int64_t) { return 0; }
+cudaError_t launch_softmax_kv_fast(const Shape&, int, const void*, const void*, int64_t,
+                                   const int64_t*, int64_t, const void*, const void*, const void*, void*, void*,
+                                   unsigned*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+
+}  // namespace hb

@@ -1,0 +1,227 @@
+"""Python binding of libhb.so with the C ABI's names (include/hb.h).
+
+Argument marshalling only: every function checks that the torch tensors it is
+given live on the current CUDA device with the dtype, shape and contiguity the
+C ABI expects (a wrong size would otherwise become an out-of-bounds access on
+the device), passes their pointers and the current stream to the library, and
+raises ``HBError`` on a non-zero status. All arithmetic runs in the CUDA
+kernels of libhb.so; there is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+DTYPE_BF16 = 0
+DTYPE_FP32 = 1
+MERGE_SHARED_NORM = 0
+MERGE_CONVEX = 1
+
+_TORCH_DTYPE = {DTYPE_BF16: torch.bfloat16, DTYPE_FP32: torch.float32}
+
+
+class HBError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _lib.load()
+        msg = lib.hb_status_string(status).decode()
+        super().__init__(f"{where}: {_lib.STATUS_NAMES.get(status, status)} ({msg})")
+        self.status = status
+
+
+@dataclass(frozen=True)
+class Config:
+    """``hb_config``: H heads, head dim d, half feature width f (F = 2f),
+    block length L, activation dtype, merge form, block softmax scale
+    (0 means 1/sqrt(d))."""
+
+    num_heads: int
+    head_dim: int
+    feat_half: int
+    block_len: int
+    dtype: int = DTYPE_BF16
+    merge: int = MERGE_SHARED_NORM
+    scale: float = 0.0
+
+    @property
+    def F(self) -> int:
+        return 2 * self.feat_half
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.dtype]
+
+    def c(self) -> _lib.HBConfig:
+        return _lib.HBConfig(self.num_heads, self.head_dim, self.feat_half, self.block_len,
+                             self.dtype, self.merge, self.scale)
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor, got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _raise(status: int, where: str) -> None:
+    if status != _lib.HB_OK:
+        raise HBError(status, where)
+
+
+def hb_feature_map(cfg: Config, x: torch.Tensor, W: torch.Tensor, phi: torch.Tensor = None,
+                   stream=None) -> torch.Tensor:
+    """phi(x) = [softmax(x W_h), softmax(-x W_h)]: x [n, H, d] -> phi [n, H, 2f] fp32."""
+    n = x.shape[0]
+    H, d, f = cfg.num_heads, cfg.head_dim, cfg.feat_half
+    _check(x, "x", cfg.torch_dtype, (n, H, d))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    if phi is None:
+        phi = torch.empty((n, H, 2 * f), dtype=torch.float32, device=x.device)
+    _check(phi, "phi", torch.float32, (n, H, 2 * f))
+    lib = _lib.load()
+    _raise(lib.hb_feature_map(ctypes.byref(cfg.c()), n, _ptr(x), _ptr(W), _ptr(phi),
+                              _stream(stream)), "hb_feature_map")
+    return phi
+
+
+def _check_state(cfg, S_pool, Z_pool):
+    if S_pool.dim() != 4:
+        raise ValueError("S_pool: expected [num_slots, H, F, d]")
+    num_slots = S_pool.shape[0]
+    _check(S_pool, "S_pool", torch.float32, (num_slots, cfg.num_heads, cfg.F, cfg.head_dim))
+    _check(Z_pool, "Z_pool", torch.float32, (num_slots, cfg.num_heads, cfg.F))
+    return num_slots
+
+
+def hb_block_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits, o=None,
+                    stream=None) -> torch.Tensor:
+    """Block-hybrid attention of the active block: q/k/v [B, L, H, d] -> o."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(S_pool), _ptr(Z_pool), num_slots, _ptr(W),
+                               _ptr(gate_logits), _ptr(o), _stream(stream)), "hb_block_attend")
+    return o
+
+
+def hb_commit_block(cfg: Config, slot_idx, k, v, W, S_pool, Z_pool, stream=None) -> None:
+    """S += sum_t phi(k_t) v_t^T, Z += sum_t phi(k_t) for each listed slot."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(k, "k", cfg.torch_dtype, (B, L, H, d))
+    _check(v, "v", cfg.torch_dtype, (B, L, H, d))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    lib = _lib.load()
+    _raise(lib.hb_commit_block(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(k), _ptr(v),
+                               _ptr(W), _ptr(S_pool), _ptr(Z_pool), num_slots, _stream(stream)),
+           "hb_commit_block")
+
+
+def hb_prefill_workspace_size(cfg: Config, batch: int, max_seqlen: int) -> int:
+    return int(_lib.load().hb_prefill_workspace_size(ctypes.byref(cfg.c()), batch, max_seqlen))
+
+
+def hb_prefill_state(cfg: Config, slot_idx, k, v, cu_seqlens, max_seqlen: int, W, S_pool,
+                     Z_pool, accumulate: bool = False, workspace=None, stream=None) -> None:
+    """Ingest packed prompts k/v [total, H, d] (request b owns rows
+    cu_seqlens[b]:cu_seqlens[b+1]) into the listed slots."""
+    B = slot_idx.shape[0]
+    H, d, f = cfg.num_heads, cfg.head_dim, cfg.feat_half
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,))
+    total = k.shape[0]
+    _check(k, "k", cfg.torch_dtype, (total, H, d))
+    _check(v, "v", cfg.torch_dtype, (total, H, d))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    need = hb_prefill_workspace_size(cfg, B, max_seqlen)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _raise(lib.hb_prefill_state(ctypes.byref(cfg.c()), B, _ptr(slot_idx),
+                                _ptr(k) if total else None, _ptr(v) if total else None,
+                                total, _ptr(cu_seqlens), max_seqlen, _ptr(W), _ptr(S_pool),
+                                _ptr(Z_pool), num_slots, int(bool(accumulate)), _ptr(workspace),
+                                ws_bytes, _stream(stream)), "hb_prefill_state")
+
+
+def hb_state_zero(cfg: Config, slot_idx, S_pool, Z_pool, stream=None) -> None:
+    B = slot_idx.shape[0]
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    lib = _lib.load()
+    _raise(lib.hb_state_zero(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(S_pool),
+                             _ptr(Z_pool), num_slots, _stream(stream)), "hb_state_zero")
+
+
+def hb_softmax_kv_workspace_size(cfg: Config, batch: int, max_prefix: int) -> int:
+    return int(_lib.load().hb_softmax_kv_workspace_size(ctypes.byref(cfg.c()), batch, max_prefix))
+
+
+def hb_softmax_kv_attend(cfg: Config, k_cache, v_cache, cu_prefix, max_prefix: int, q, k, v,
+                         o=None, workspace=None, stream=None) -> torch.Tensor:
+    """Comparison path: full-prefix softmax attention of the active block over a
+    packed KV cache [total_prefix, H, d] followed by the block itself."""
+    B = q.shape[0]
+    H, d, L = cfg.num_heads, cfg.head_dim, cfg.block_len
+    _check(cu_prefix, "cu_prefix", torch.int64, (B + 1,))
+    total = k_cache.shape[0]
+    _check(k_cache, "k_cache", cfg.torch_dtype, (total, H, d))
+    _check(v_cache, "v_cache", cfg.torch_dtype, (total, H, d))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    need = hb_softmax_kv_workspace_size(cfg, B, max_prefix)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _raise(lib.hb_softmax_kv_attend(ctypes.byref(cfg.c()), B, _ptr(k_cache) if total else None,
+                                    _ptr(v_cache) if total else None, total, _ptr(cu_prefix),
+                                    max_prefix, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(workspace), ws_bytes, _stream(stream)),
+           "hb_softmax_kv_attend")
+    return o
+
+
+def hb_get_device_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status code."""
+    return int(_lib.load().hb_get_device_status(_stream(stream)))
+
+
+def hb_status_string(status: int) -> str:
+    return _lib.load().hb_status_string(status).decode()

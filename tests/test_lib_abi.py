@@ -1,0 +1,157 @@
+"""libhb.so loads, exports every entry point include/hb.h declares, and its
+host-side validation rejects bad arguments before touching CUDA (CPU only:
+no call here reaches a kernel launch or any CUDA runtime call)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from linear_attention_diffusion_feature_b300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hb.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hb_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("hb_feature_map", "hb_block_attend", "hb_commit_block", "hb_prefill_state",
+                     "hb_softmax_kv_attend", "hb_state_zero", "hb_get_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (hb_[a-z_]+)\b", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for name in declared_functions():
+        assert hasattr(lib, name)
+
+
+def test_binding_covers_exactly_the_header():
+    assert sorted(_lib.SIGNATURES) == declared_functions()
+
+
+def test_library_has_no_driver_or_torch_dependency():
+    out = subprocess.run(["ldd", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libtorch" not in out and "libc10" not in out
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.hb_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.hb_status_string(99) == b"unknown status"
+
+
+def _cfg(**kw):
+    base = dict(num_heads=16, head_dim=128, feat_half=64, block_len=32, dtype=0, merge=0, scale=0.0)
+    base.update(kw)
+    return _lib.HBConfig(**base)
+
+
+# Fake, never dereferenced device addresses: validation fails or returns
+# early before any pointer is used.
+A = ctypes.c_void_p(0x10000)      # 16-byte aligned
+M = ctypes.c_void_p(0x10008)      # misaligned
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=8), 2), (dict(head_dim=136), 2), (dict(head_dim=72), 2),
+    (dict(feat_half=4), 2), (dict(feat_half=72), 2), (dict(feat_half=12), 2),
+    (dict(block_len=0), 2), (dict(block_len=65), 2), (dict(num_heads=0), 2),
+    (dict(dtype=7), 1), (dict(merge=3), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+])
+def test_attend_rejects_bad_config(lib, kw, code):
+    c = _cfg(**kw)
+    r = lib.hb_block_attend(ctypes.byref(c), 1, A, A, A, A, A, A, 1, A, A, A, None)
+    assert r == code
+
+
+def test_attend_null_config(lib):
+    assert lib.hb_block_attend(None, 1, A, A, A, A, A, A, 1, A, A, A, None) == 1
+
+
+def test_attend_pointer_checks(lib):
+    c = _cfg()
+    assert lib.hb_block_attend(ctypes.byref(c), 1, A, None, A, A, A, A, 1, A, A, A, None) == 1
+    assert lib.hb_block_attend(ctypes.byref(c), 1, A, A, A, M, A, A, 1, A, A, A, None) == 3
+    assert lib.hb_block_attend(ctypes.byref(c), -1, A, A, A, A, A, A, 1, A, A, A, None) == 1
+    # batch 0 is a no-op that succeeds without looking at the pointers
+    assert lib.hb_block_attend(ctypes.byref(c), 0, None, None, None, None, None, None, 0, None,
+                               None, None, None) == 0
+
+
+def test_commit_and_zero_checks(lib):
+    c = _cfg()
+    assert lib.hb_commit_block(ctypes.byref(c), 2, A, A, None, A, A, A, 4, None) == 1
+    assert lib.hb_commit_block(ctypes.byref(c), 2, A, A, A, A, M, A, 4, None) == 3
+    assert lib.hb_commit_block(ctypes.byref(c), 0, None, None, None, None, None, None, 0, None) == 0
+    assert lib.hb_state_zero(ctypes.byref(c), 1, A, None, A, 1, None) == 1
+    assert lib.hb_state_zero(ctypes.byref(c), 0, None, None, None, 0, None) == 0
+
+
+def test_prefill_checks(lib):
+    c = _cfg()
+    # negative sizes, bad accumulate flag
+    assert lib.hb_prefill_state(ctypes.byref(c), 1, A, A, A, -1, A, 8, A, A, A, 1, 0, None, 0,
+                                None) == 1
+    assert lib.hb_prefill_state(ctypes.byref(c), 1, A, A, A, 8, A, -8, A, A, A, 1, 0, None, 0,
+                                None) == 1
+    assert lib.hb_prefill_state(ctypes.byref(c), 1, A, A, A, 8, A, 8, A, A, A, 1, 2, None, 0,
+                                None) == 1
+    # tokens present but k missing
+    assert lib.hb_prefill_state(ctypes.byref(c), 1, A, None, A, 8, A, 8, A, A, A, 1, 0, None, 0,
+                                None) == 1
+    need = lib.hb_prefill_workspace_size(ctypes.byref(c), 8, 8192)
+    if need:
+        assert lib.hb_prefill_state(ctypes.byref(c), 8, A, A, A, 65536, A, 8192, A, A, A, 8, 0,
+                                    A, need - 16, None) == 7
+
+
+def test_softmax_kv_checks(lib):
+    c = _cfg()
+    assert lib.hb_softmax_kv_attend(ctypes.byref(c), 1, A, A, 8, None, 8, A, A, A, A, None, 0,
+                                    None) == 1
+    assert lib.hb_softmax_kv_attend(ctypes.byref(c), 1, None, A, 8, A, 8, A, A, A, A, None, 0,
+                                    None) == 1
+    assert lib.hb_softmax_kv_attend(ctypes.byref(c), 1, A, A, 8, A, 8, A, M, A, A, None, 0,
+                                    None) == 3
+
+
+def test_feature_map_checks(lib):
+    c = _cfg()
+    assert lib.hb_feature_map(ctypes.byref(c), -1, A, A, A, None) == 1
+    assert lib.hb_feature_map(ctypes.byref(c), 0, None, A, None, None) == 0
+    assert lib.hb_feature_map(ctypes.byref(c), 4, A, M, A, None) == 3
+    assert lib.hb_feature_map(ctypes.byref(_cfg(feat_half=100)), 4, A, A, A, None) == 2
+
+
+def test_workspace_size_queries_reject_bad_args(lib):
+    assert lib.hb_prefill_workspace_size(None, 8, 8192) == 0
+    assert lib.hb_prefill_workspace_size(ctypes.byref(_cfg(head_dim=8)), 8, 8192) == 0
+    assert lib.hb_softmax_kv_workspace_size(ctypes.byref(_cfg()), -1, 2048) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libhb.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load()
