@@ -92,13 +92,20 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0:  # sampler is up
+                time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def mark(self):
+        """Start of the timed region: earlier samples are dropped."""
+        self.lines = []
 
     def _read(self):
         for line in self.proc.stdout:
@@ -209,19 +216,17 @@ def run_ours(args, world, rank, local):
         hb.hb_commit_block(cfg, ly["commit_slots"], ly["commit_k"], ly["commit_v"], ly["W"],
                            ly["S"], ly["Z"])
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    _barrier(world)
-
     # timed region: K steps, events around every attend launch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        for i in range(args.warmup):
+            step(i)
         torch.cuda.synchronize()
         _barrier(world)
+        clocks.mark()
         start.record(stream)
         for i in range(args.steps):
             step(args.warmup + i, evs[i])
@@ -303,17 +308,18 @@ def run_e2e(args, cfg, layers, device):
                            ly["S"], ly["Z"])
         host_o.copy_(ly["o"], non_blocking=True)
 
+    n_steps = min(args.steps, 200)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(n_steps):
         step(i)
     end.record(stream)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / args.steps
+    ms = start.elapsed_time(end) / n_steps
     return {"value": B * L / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
@@ -403,8 +409,8 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
-    ap.add_argument("--warmup", type=int, default=6)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -6,17 +6,11 @@
 namespace hb {
 
 bool fast_feature_map_ok(const Shape&) { return false; }
-bool fast_attend_ok(const Shape&) { return false; }
 bool fast_state_ok(const Shape&) { return false; }
 bool fast_softmax_kv_ok(const Shape&) { return false; }
 
 cudaError_t launch_feature_map_fast(const Shape&, int64_t, const void*, const void*, float*,
                                     cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-cudaError_t launch_attend_fast(const Shape&, int, const int32_t*, const void*, const void*,
-                               const void*, const float*, const float*, int, const void*,
-                               const float*, void*, unsigned*, cudaStream_t) {
   return cudaErrorNotSupported;
 }
 cudaError_t launch_commit_fast(const Shape&, int, const int32_t*, const void*, const void*,
