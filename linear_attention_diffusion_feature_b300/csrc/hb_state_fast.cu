@@ -1,0 +1,505 @@
+// State commit and prompt ingestion for the production shape (bf16,
+// d = 128, f = 64, F = 128) on the 5th-generation tensor cores.
+//
+// Definitions (pith.science review of arXiv 2608.06628, "What carries the
+// argument"; gist.science technical summary, state-compression bullet):
+//   S += sum_t phi(k_t) v_t^T,  Z += sum_t phi(k_t),
+//   phi(k) = [softmax(k W_h), softmax(-k W_h)].
+// A prompt is committed context, so ingesting it is the same sum over all of
+// its tokens; the sum does not depend on how the tokens are chunked.
+//
+// One CTA per (request, head, token split); it streams its tokens in chunks
+// of RB rows (128 for prompts, 32 for a committed block):
+//   warp 0   TMA producer: k and v chunks into a two-stage ring (two
+//            SWIZZLE_128B boxes of 64 columns each), W_h once;
+//   warp 1   owns TMEM (512 columns) and issues tcgen05.mma from one thread:
+//              U    [128 tok x 64]  = K W_h            (A K-major, B MN-major)
+//              Sacc [128 F x 128 d] += phi^T V          (A, B MN-major)
+//              Zacc [128 F x 16]    += phi^T 1          (B = constant ones)
+//            U is double-buffered, so the next chunk's K W_h overlaps the
+//            epilogue of the current one;
+//   warps 2-5 epilogue: each thread owns one token (one TMEM lane), loads its
+//            64 values of u, takes both softmaxes in registers and writes
+//            phi to shared memory as a bf16 pair hi + lo (phi = hi + lo to
+//            ~2^-17 relative), so the fp32 state meets a 1e-4 bound although
+//            the tensor cores take bf16 operands; v is exact in bf16.
+// At the end the epilogue reads Sacc/Zacc (thread = row of S), stages the
+// tile through swizzled shared memory and writes S/Z (or a partial sum for
+// the fixed-order split reduction) with coalesced 16-byte stores.
+#include <float.h>
+
+#include "hb_fast.cuh"
+#include "hb_ptx.cuh"
+
+namespace hb {
+namespace {
+
+using namespace ptx;
+
+constexpr int kD = 128, kFH = 64, kF = 128;
+constexpr int kThreads = 192;
+constexpr int kTargetCtas = 148;  // SMs of a B300; splits aim to fill them once
+
+// Shared-memory layout (bytes from a 1024-aligned base).
+constexpr int kOffK = 0;            // 2 stages x 2 boxes x [128 rows][128 B]
+constexpr int kOffV = 65536;        // same
+constexpr int kOffW = 131072;       // [128 d rows][64 bf16]
+constexpr int kOffPhiHi = 147456;   // 2 atoms (F 0-63, 64-127) x [128 tok][128 B]
+constexpr int kOffPhiLo = 180224;
+constexpr int kOffOnes = 212992;    // [16 rows][128 B] of bf16 1.0
+constexpr int kOffBar = 215040;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
+
+// mbarrier slots
+enum { kKvFull0 = 0, kKvFull1, kKvEmpty0, kKvEmpty1, kWFull, kUFull0, kUFull1, kUEmpty0,
+       kUEmpty1, kPhiFull, kPhiEmpty, kAccFull, kNumBars };
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColZ = 128, kColU = 256;
+
+constexpr int kPartialFloats = kF * kD + kF;  // one partial state: S then Z
+
+struct Maps {
+  CUtensorMap k;  // [rows][H][d] bf16, box {64, 1, RB}
+  CUtensorMap v;
+  CUtensorMap W;  // [H*d][f] bf16, box {64, 128}
+};
+
+struct Args {
+  int H, num_slots, RB, splits, accumulate;
+  int64_t total_rows, max_len;
+  const int32_t* slot_idx;
+  const int64_t* cu;  // nullptr: request b owns rows [b*RB, b*RB + RB)
+  float* S_pool;
+  float* Z_pool;
+  float* ws;          // partial sums when splits > 1
+  unsigned* status;
+};
+
+__device__ __forceinline__ bool unit_range(const Args& a, int b, int64_t* row0, int64_t* cnt) {
+  if (a.cu) {
+    *row0 = a.cu[b];
+    *cnt = a.cu[b + 1] - *row0;
+  } else {
+    *row0 = (int64_t)b * a.RB;
+    *cnt = a.RB;
+  }
+  const int slot = a.slot_idx[b];
+  return slot >= 0 && slot < a.num_slots && *cnt >= 0 && *cnt <= a.max_len && *row0 >= 0 &&
+         *row0 + *cnt <= a.total_rows;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_state_tc(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int64_t row0, cnt;
+  if (!unit_range(a, b, &row0, &cnt)) {
+    if (threadIdx.x == 0 && split == 0) atomicOr(a.status, kStatusBounds);
+    return;
+  }
+  const int slot = a.slot_idx[b];
+  const int RB = a.RB;
+  const int64_t n_chunks = (cnt + RB - 1) / RB;
+  const int64_t c_begin = n_chunks * split / a.splits;
+  const int64_t c_end = n_chunks * (split + 1) / a.splits;
+  const int n_my = (int)(c_end - c_begin);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[kKvFull0], 1);
+    mbar_init(&bar[kKvFull1], 1);
+    mbar_init(&bar[kKvEmpty0], 1);
+    mbar_init(&bar[kKvEmpty1], 1);
+    mbar_init(&bar[kWFull], 1);
+    mbar_init(&bar[kUFull0], 1);
+    mbar_init(&bar[kUFull1], 1);
+    mbar_init(&bar[kUEmpty0], 4);
+    mbar_init(&bar[kUEmpty1], 4);
+    mbar_init(&bar[kPhiFull], 4);
+    mbar_init(&bar[kPhiEmpty], 1);
+    mbar_init(&bar[kAccFull], 1);
+    fence_mbar_init();
+  }
+  if (warp >= 2) {  // constant ones tile (B operand of the Z contraction)
+    const uint32_t ones = smem_u32(smem + kOffOnes);
+    const uint32_t one2 = 0x3F803F80u;  // two bf16 1.0
+    for (int i = threadIdx.x - 64; i < 2048 / 16; i += 128)
+      st_shared_v4(ones + i * 16, one2, one2, one2, one2);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_my > 0) {
+      prefetch_tmap(&maps.k);
+      prefetch_tmap(&maps.v);
+      mbar_arrive_expect_tx(&bar[kWFull], 16384);
+      tma_load_2d(smem + kOffW, &maps.W, 0, h * kD, &bar[kWFull]);
+      for (int c = 0; c < n_my; ++c) {
+        const int s = c & 1, use = c >> 1;
+        if (use > 0 && !mbar_wait(&bar[kKvEmpty0 + s], (use - 1) & 1)) {
+          atomicOr(a.status, kStatusTimeout);
+          break;
+        }
+        const int row = (int)(row0 + (c_begin + c) * RB);
+        mbar_arrive_expect_tx(&bar[kKvFull0 + s], 4 * RB * 128);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          tma_load_3d(smem + kOffK + s * 32768 + j * 16384, &maps.k, 64 * j, h, row,
+                      &bar[kKvFull0 + s]);
+          tma_load_3d(smem + kOffV + s * 32768 + j * 16384, &maps.v, 64 * j, h, row,
+                      &bar[kKvFull0 + s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_my > 0) {
+      constexpr uint32_t idU = umma_idesc_bf16(128, kFH, 0, 1);
+      constexpr uint32_t idS = umma_idesc_bf16(128, kD, 1, 1);
+      constexpr uint32_t idZ = umma_idesc_bf16(128, 16, 1, 0);
+      const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+      const uint32_t sW = smem_u32(smem + kOffW);
+      const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
+      const uint64_t dOnes = umma_desc_sw128(smem_u32(smem + kOffOnes), 0, 1024);
+      bool ok = mbar_wait(&bar[kWFull], 0);
+      auto mma2 = [&](int cc) -> bool {
+        if (!mbar_wait(&bar[kPhiFull], cc & 1)) return false;
+        tc_fence_after();
+        const int64_t valid64 = cnt - (c_begin + cc) * RB;
+        const int valid = valid64 < RB ? (int)valid64 : RB;
+        const int ksteps = (valid + 15) >> 4;
+        const uint32_t vb = sV + (cc & 1) * 32768;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint64_t aHi = umma_desc_sw128(sHi + ks * 2048, 16384, 1024);
+          const uint64_t aLo = umma_desc_sw128(sLo + ks * 2048, 16384, 1024);
+          const uint64_t bV = umma_desc_sw128(vb + ks * 2048, 16384, 1024);
+          const uint32_t acc = (cc == 0 && ks == 0) ? 0u : 1u;
+          umma_bf16(tbase + kColS, aHi, bV, idS, acc);
+          umma_bf16(tbase + kColS, aLo, bV, idS, 1u);
+          umma_bf16(tbase + kColZ, aHi, dOnes, idZ, acc);
+          umma_bf16(tbase + kColZ, aLo, dOnes, idZ, 1u);
+        }
+        umma_commit(&bar[kPhiEmpty]);
+        umma_commit(&bar[kKvEmpty0 + (cc & 1)]);
+        return true;
+      };
+      for (int c = 0; ok && c < n_my; ++c) {
+        const int s = c & 1;
+        if (!mbar_wait(&bar[kKvFull0 + s], (c >> 1) & 1)) { ok = false; break; }
+        if (c >= 2 && !mbar_wait(&bar[kUEmpty0 + s], ((c >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = sK + s * 32768;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t aK = umma_desc_sw128(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 0, 1024);
+          const uint64_t bW = umma_desc_sw128(sW + ks * 2048, 16384, 1024);
+          umma_bf16(tbase + kColU + 64 * s, aK, bW, idU, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar[kUFull0 + s]);
+        if (c >= 1 && !mma2(c - 1)) { ok = false; break; }
+      }
+      if (ok) ok = mma2(n_my - 1);
+      if (!ok) atomicOr(a.status, kStatusTimeout);
+      umma_commit(&bar[kAccFull]);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int tok = 32 * quad + lane;  // TMEM lane = token row (chunks) = F row (final)
+    const uint32_t lane_bits = (uint32_t)(32 * quad) << 16;
+    const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
+    bool ok = true;
+    for (int c = 0; c < n_my; ++c) {
+      const int s = c & 1;
+      if (!mbar_wait(&bar[kUFull0 + s], (c >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      float u[64];
+      {
+        float (&u0)[32] = *reinterpret_cast<float(*)[32]>(&u[0]);
+        float (&u1)[32] = *reinterpret_cast<float(*)[32]>(&u[32]);
+        tmem_ld32(tbase + lane_bits + kColU + 64 * s, u0);
+        tmem_ld32(tbase + lane_bits + kColU + 64 * s + 32, u1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kUEmpty0 + s]);
+
+      const int64_t valid64 = cnt - (c_begin + c) * RB;
+      const int valid = valid64 < RB ? (int)valid64 : RB;
+      const bool live = tok < valid;
+      float mx = -FLT_MAX, mn = FLT_MAX;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        mx = fmaxf(mx, u[j]);
+        mn = fminf(mn, u[j]);
+      }
+      float e[64];
+      float sp = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        e[j] = expf(u[j] - mx);
+        sp += e[j];
+      }
+      if (c >= 1 && !mbar_wait(&bar[kPhiEmpty], (c - 1) & 1)) { ok = false; break; }
+      // positive half -> atom 0, negated half -> atom 1
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1) {
+          sp = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            e[j] = expf(mn - u[j]);
+            sp += e[j];
+          }
+        }
+        const float inv = 1.f / sp;
+        const uint32_t rowoff = half * 16384 + tok * 128;
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {
+          uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+          if (live) {  // dead rows stay exact zeros whatever u held
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const float p0 = e[8 * k8 + 2 * p] * inv, p1 = e[8 * k8 + 2 * p + 1] * inv;
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+              const float2 hf = __bfloat1622float2(hi);
+              hw[p] = *reinterpret_cast<const uint32_t*>(&hi);
+              lw[p] = pack_bf16(p0 - hf.x, p1 - hf.y);
+            }
+          }
+          const uint32_t off = rowoff + ((k8 ^ (tok & 7)) << 4);
+          st_shared_v4(sHi + off, hw[0], hw[1], hw[2], hw[3]);
+          st_shared_v4(sLo + off, lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+      if (valid < RB) {
+        // Rows past the end of the request inside the last 16-token step:
+        // their phi is 0; clear v there too so foreign or fill rows cannot
+        // inject a non-finite value into the products.
+        const int vend = (valid + 15) & ~15;
+        if (tok >= valid && tok < vend) {
+          if (!mbar_wait(&bar[kKvFull0 + s], (c >> 1) & 1)) { ok = false; break; }
+          const uint32_t vrow = smem_u32(smem + kOffV + s * 32768) + tok * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            st_shared_v4(vrow + j * 16, 0u, 0u, 0u, 0u);
+            st_shared_v4(vrow + 16384 + j * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kPhiFull]);
+    }
+    if (!ok) atomicOr(a.status, kStatusTimeout);
+
+    // ---- final: row `tok` of S (F index) and Z_tok, staged for coalescing
+    const bool have = n_my > 0 && ok && mbar_wait(&bar[kAccFull], 0);
+    if (n_my > 0 && ok && !have) atomicOr(a.status, kStatusTimeout);
+    tc_fence_after();
+    const uint32_t stage = smem_u32(smem + kOffK);  // reused: all MMAs are done
+    float z = 0.f;
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float r[32];
+      if (have) {
+        tmem_ld32(tbase + lane_bits + kColS + 32 * part, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const int chunk = 8 * part + q4;
+        st_shared_v4(stage + tok * 512 + ((chunk ^ (tok & 31)) << 4), __float_as_uint(r[4 * q4]),
+                     __float_as_uint(r[4 * q4 + 1]), __float_as_uint(r[4 * q4 + 2]),
+                     __float_as_uint(r[4 * q4 + 3]));
+      }
+    }
+    if (have) {
+      z = tmem_ld1(tbase + lane_bits + kColZ);
+      tmem_wait_ld();
+    }
+    tc_fence_before();
+    named_bar_sync(1, 128);
+
+    const size_t unit = (size_t)slot * a.H + h;
+    float* Sdst;
+    float* Zdst;
+    bool add_old;
+    if (a.splits > 1) {
+      float* p = a.ws + ((size_t)(b * a.H + h) * a.splits + split) * kPartialFloats;
+      Sdst = p;
+      Zdst = p + kF * kD;
+      add_old = false;
+    } else {
+      Sdst = a.S_pool + unit * kF * kD;
+      Zdst = a.Z_pool + unit * kF;
+      add_old = a.accumulate != 0;
+    }
+    const int ew = warp - 2;
+    for (int r = ew; r < kF; r += 4) {
+      float4 v = ld_shared_v4f(stage + r * 512 + ((lane ^ (r & 31)) << 4));
+      float4* dst = reinterpret_cast<float4*>(Sdst + r * kD) + lane;
+      if (add_old) {
+        const float4 o = *dst;
+        v.x += o.x;
+        v.y += o.y;
+        v.z += o.z;
+        v.w += o.w;
+      }
+      *dst = v;
+    }
+    Zdst[tok] = add_old ? Zdst[tok] + z : z;
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// Sums the split partials of each unit in split order and writes S/Z.
+__global__ void __launch_bounds__(256) k_state_reduce(const __grid_constant__ Args a) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  int64_t row0, cnt;
+  if (!unit_range(a, b, &row0, &cnt)) return;  // flagged by k_state_tc
+  const int slot = a.slot_idx[b];
+  const float4* part =
+      reinterpret_cast<const float4*>(a.ws + (size_t)(b * a.H + h) * a.splits * kPartialFloats);
+  const size_t unit = (size_t)slot * a.H + h;
+  float4* S = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD);
+  float4* Z = reinterpret_cast<float4*>(a.Z_pool + unit * kF);
+  constexpr int n4 = kPartialFloats / 4;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < a.splits; ++j) {
+      const float4 p = part[(size_t)j * n4 + i];
+      acc.x += p.x;
+      acc.y += p.y;
+      acc.z += p.z;
+      acc.w += p.w;
+    }
+    float4* dst = i < kF * kD / 4 ? S + i : Z + (i - kF * kD / 4);
+    if (a.accumulate) {
+      const float4 o = *dst;
+      acc.x += o.x;
+      acc.y += o.y;
+      acc.z += o.z;
+      acc.w += o.w;
+    }
+    *dst = acc;
+  }
+}
+
+int splits_for(int batch, int H, int64_t max_seqlen) {
+  const int64_t units = (int64_t)batch * H;
+  const int64_t chunks = (max_seqlen + 127) / 128;
+  int64_t s = kTargetCtas / (units > 0 ? units : 1);
+  if (s > chunks) s = chunks;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : (int)s;
+}
+
+cudaError_t launch_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                      const void* v, int64_t total_rows, const int64_t* cu, int64_t max_len,
+                      int RB, int splits, const void* W, float* S_pool, float* Z_pool,
+                      int num_slots, int accumulate, float* ws, unsigned* status,
+                      cudaStream_t st) {
+  Maps maps;
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)total_rows};
+    const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)RB};
+    if (!encode_tmap(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)kFH, (uint64_t)s.H * kD};
+    const uint64_t strides[1] = {kFH * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap(&maps.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  Args a;
+  a.H = s.H;
+  a.num_slots = num_slots;
+  a.RB = RB;
+  a.splits = splits;
+  a.accumulate = accumulate;
+  a.total_rows = total_rows;
+  a.max_len = max_len;
+  a.slot_idx = slot_idx;
+  a.cu = cu;
+  a.S_pool = S_pool;
+  a.Z_pool = Z_pool;
+  a.ws = ws;
+  a.status = status;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_state_tc), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_state_tc<<<dim3(splits, s.H, batch), kThreads, kSmemBytes, st>>>(maps, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (splits > 1) {
+    k_state_reduce<<<dim3(s.H, batch), 256, 0, st>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+bool fast_state_ok(const Shape& s) { return production_shape(s); }
+
+cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                               const void* v, const void* W, float* S_pool, float* Z_pool,
+                               int num_slots, unsigned* status, cudaStream_t st) {
+  const int64_t rows = (int64_t)batch * s.L;
+  if (rows >= (int64_t)1 << 31 || batch > 65535)
+    return launch_state_accumulate_generic(s, batch, slot_idx, k, v, rows, nullptr, s.L, W,
+                                           S_pool, Z_pool, num_slots, 1, status, st);
+  return launch_tc(s, batch, slot_idx, k, v, rows, nullptr, s.L, s.L, 1, W, S_pool, Z_pool,
+                   num_slots, 1, nullptr, status, st);
+}
+
+size_t prefill_fast_workspace_bytes(const Shape& s, int batch, int64_t max_seqlen) {
+  const int sp = splits_for(batch, s.H, max_seqlen);
+  return sp > 1 ? (size_t)batch * s.H * sp * kPartialFloats * sizeof(float) : 0;
+}
+
+cudaError_t launch_prefill_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                                const void* v, int64_t total_tokens, const int64_t* cu_seqlens,
+                                int64_t max_seqlen, const void* W, float* S_pool, float* Z_pool,
+                                int num_slots, int accumulate, void* workspace, unsigned* status,
+                                cudaStream_t st) {
+  if (total_tokens == 0 || total_tokens >= (int64_t)1 << 31 || batch > 65535)
+    return launch_state_accumulate_generic(s, batch, slot_idx, k, v, total_tokens, cu_seqlens,
+                                           max_seqlen, W, S_pool, Z_pool, num_slots, accumulate,
+                                           status, st);
+  const int sp = splits_for(batch, s.H, max_seqlen);
+  return launch_tc(s, batch, slot_idx, k, v, total_tokens, cu_seqlens, max_seqlen, 128, sp, W,
+                   S_pool, Z_pool, num_slots, accumulate, static_cast<float*>(workspace), status,
+                   st);
+}
+
+}  // namespace hb
