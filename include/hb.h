@@ -19,7 +19,8 @@
  * Memory.      Every pointer except `cfg` is a DEVICE pointer on the current
  *              CUDA device, owned by the caller, 16-byte aligned. The library
  *              allocates nothing; the only device memory it owns is a
- *              file-scope status word per device.
+ *              file-scope status word per device and the fixed scratch array
+ *              of hb_prefill_state_noalloc.
  * Layouts.     Row-major, outermost index first. Activations (q, k, v, o, x)
  *              are [tokens, H, d] of the activation dtype (`cfg->dtype`).
  *              W is [H, d, f] of the activation dtype. The state pool is
@@ -186,6 +187,39 @@ hb_status hb_prefill_state(const hb_config* cfg, int32_t batch,
  * Returns 0 as well for arguments hb_prefill_state would reject. */
 size_t hb_prefill_workspace_size(const hb_config* cfg, int32_t batch,
                                  int64_t max_seqlen);
+
+/*
+ * hb_prefill_state_noalloc — hb_prefill_state for callers that cannot call
+ * cudaMalloc: a plug-in whose host engine owns all device memory and gives it
+ * no allocator, or a latency-critical serving loop where an allocation could
+ * synchronise the device. The pages have no counterpart; it is a deployment
+ * variant of hb_prefill_state with the same arguments, meaning and result,
+ * minus the workspace.
+ *   Scratch   the split partial sums live in one file-scope device array of
+ *             HB_PREFILL_NOALLOC_SCRATCH_BYTES (10 MiB). Every GPU that loads
+ *             the library holds it until the process exits. The call itself
+ *             allocates nothing (no cudaMalloc, no allocating library call).
+ *   Limit     a shape whose hb_prefill_workspace_size() exceeds that size is
+ *             rejected with HB_ERR_WORKSPACE before anything is launched. For
+ *             d = 128, f = 64 in bf16 the need never exceeds ~9.8 MB; every
+ *             other shape needs none.
+ *   Set-up    the first call on a device that needs scratch looks up the
+ *             array's device address (with that device current) and caches
+ *             it; make that first call before any stream capture.
+ *   Sharing   every call on a device uses the same array. Calls whose kernels
+ *             overlap on the GPU (different streams, no ordering between
+ *             them) race on it; order them on one stream or with events.
+ *             Nothing in the array needs to start at zero: each call writes
+ *             every partial it reads back.
+ */
+#define HB_PREFILL_NOALLOC_SCRATCH_BYTES (10u * 1024u * 1024u)
+hb_status hb_prefill_state_noalloc(const hb_config* cfg, int32_t batch,
+                                   const int32_t* slot_idx, const void* k,
+                                   const void* v, int64_t total_tokens,
+                                   const int64_t* cu_seqlens, int64_t max_seqlen,
+                                   const void* W, float* S_pool, float* Z_pool,
+                                   int32_t num_slots, int32_t accumulate,
+                                   hb_stream_t stream);
 
 /* hb_state_zero — clear S and Z of the listed slots (a new request with no
  * prompt, or a finished request's slot being recycled). */

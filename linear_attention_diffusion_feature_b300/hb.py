@@ -177,6 +177,30 @@ def hb_prefill_state(cfg: Config, slot_idx, k, v, cu_seqlens, max_seqlen: int, W
                                 ws_bytes, _stream(stream)), "hb_prefill_state")
 
 
+def hb_prefill_state_noalloc(cfg: Config, slot_idx, k, v, cu_seqlens, max_seqlen: int, W,
+                             S_pool, Z_pool, accumulate: bool = False, stream=None) -> None:
+    """hb_prefill_state without a workspace, for callers that cannot allocate
+    device memory: the split partial sums go to the library's fixed scratch
+    array (HB_PREFILL_NOALLOC_SCRATCH_BYTES). Calls that overlap on the GPU
+    share that array and race; a shape that needs more scratch is rejected."""
+    B = slot_idx.shape[0]
+    H, d, f = cfg.num_heads, cfg.head_dim, cfg.feat_half
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,))
+    total = k.shape[0]
+    _check(k, "k", cfg.torch_dtype, (total, H, d))
+    _check(v, "v", cfg.torch_dtype, (total, H, d))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    lib = _lib.load()
+    _raise(lib.hb_prefill_state_noalloc(ctypes.byref(cfg.c()), B, _ptr(slot_idx),
+                                        _ptr(k) if total else None, _ptr(v) if total else None,
+                                        total, _ptr(cu_seqlens), max_seqlen, _ptr(W),
+                                        _ptr(S_pool), _ptr(Z_pool), num_slots,
+                                        int(bool(accumulate)), _stream(stream)),
+           "hb_prefill_state_noalloc")
+
+
 def hb_state_zero(cfg: Config, slot_idx, S_pool, Z_pool, stream=None) -> None:
     B = slot_idx.shape[0]
     _check(slot_idx, "slot_idx", torch.int32, (B,))
