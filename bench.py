@@ -324,6 +324,277 @@ def run_e2e(args, cfg, layers, device):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+# ------------------------------------------------------ other workloads
+
+def _timed(fn, steps, warmup, stream):
+    """CUDA-event time of each of ``steps`` calls of ``fn`` after ``warmup``
+    untimed calls; returns the per-call times in ms."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _graph_ms(fn, per_graph, replays, warmup, stream):
+    """Device time per call of ``fn`` with the host out of the loop: ``fn`` is
+    called ``warmup`` times, then ``per_graph`` calls are captured into one CUDA
+    graph, which is replayed ``replays`` times between two events."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(replays):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (replays * per_graph)
+
+
+def _median(xs):
+    ys = sorted(xs)
+    return ys[len(ys) // 2]
+
+
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1800.0, "fallback"
+
+
+def run_prefill(args):
+    """Prompt ingestion: 8 prompts x 8,192 tokens, 16 heads, d=128, f=64,
+    overwrite S/Z (k, v are 537 MB, well above the 126 MB L2)."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = inputs.prompt_ingestion(device=device)
+    t = w.tensors
+    nB, T = w.meta["B"], w.meta["T"]
+    cfg = hb.Config(H, D, FH, L)
+    S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
+    Z = torch.empty((nB, H, F), dtype=torch.float32, device=device)
+    sl = torch.arange(nB, dtype=torch.int32, device=device)
+    need = hb.hb_prefill_workspace_size(cfg, nB, T)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        hb.hb_prefill_state(cfg, sl, t["k"], t["v"], t["cu_seqlens"], T, t["W"], S, Z,
+                            workspace=ws)
+
+    with ClockSampler(0) as clocks:
+        ms = _timed(call, args.steps, args.warmup, stream)
+    assert hb.hb_get_device_status() == 0
+    med = _median(ms)
+    tokens = nB * T
+    nbytes = 2 * tokens * H * D * 2 + nB * H * (F * D + F) * 4 + H * D * FH * 2
+    # tensor work as issued: U = K W (2 d f), phi^T V and phi^T 1 with phi split hi + lo
+    flops = tokens * H * (2 * D * FH + 2 * 2 * F * D + 2 * 2 * F * 16)
+    peak, kind = _peaks()
+    tpeak, tkind = _tensor_peak()
+    achieved = nbytes / (med / 1e3) / 1e9
+    line = {
+        "metric": "prompt-ingestion tokens/s and HBM GB/s", "value": tokens / (med / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": med, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prompt ingestion: hb_prefill_state, 8 prompts x 8,192 tokens, "
+                               "16 heads, d=128, f=64, overwrite", "l2": "inputs 537 MB > L2"},
+        "roofline": {"kernel": "hb_prefill_state", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": med,
+                     "traffic": _traffic("hb_prefill_state"),
+                     "tensor": {"flops_per_launch": flops,
+                                "achieved_tflops": flops / (med / 1e3) / 1e12,
+                                "peak_tflops": tpeak, "peak_kind": tkind,
+                                "frac": flops / (med / 1e3) / 1e12 / tpeak}},
+        "gpu_launches": args.steps * (2 if need else 1),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(max_seconds=args.cpu_seconds)
+    return line
+
+
+def run_decode(args):
+    """Single-layer decode step: 1 request, 16 heads, 2,048-token state,
+    one hb_block_attend (latency) and one hb_commit_block."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = inputs.single_layer(device=device)
+    t = w.tensors
+    cfg = hb.Config(H, D, FH, L)
+    S = torch.zeros((1, H, F, D), dtype=torch.float32, device=device)
+    Z = torch.zeros((1, H, F), dtype=torch.float32, device=device)
+    sl = torch.zeros(1, dtype=torch.int32, device=device)
+    for blk in range(t["commit_k"].shape[0]):
+        hb.hb_commit_block(cfg, sl, t["commit_k"][blk], t["commit_v"][blk], t["W"], S, Z)
+    o = torch.empty_like(t["q"])
+    stream = torch.cuda.current_stream()
+
+    def attend():
+        hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"], o=o)
+
+    S2, Z2 = S.clone(), Z.clone()
+
+    def commit():
+        hb.hb_commit_block(cfg, sl, t["k"], t["v"], t["W"], S2, Z2)
+
+    # launch-to-launch device time: 50 calls per CUDA graph, host out of the loop
+    reps = max(1, args.steps // 50)
+    a_ms = _graph_ms(attend, 50, reps, args.warmup, stream)
+    c_ms = _graph_ms(commit, 50, reps, args.warmup, stream)
+    # the same calls issued one by one from Python, for context
+    a_host = _median(_timed(attend, min(args.steps, 200), args.warmup, stream))
+    assert hb.hb_get_device_status() == 0
+    nbytes = ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W
+    peak, kind = _peaks()
+    return {
+        "metric": "single-layer decode: active-block tokens/s (attend latency)",
+        "value": L / (a_ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": a_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "single-layer decode: 1 request, 16 heads, d=128, f=64, L=32, "
+                               "2,048-token state from 64 commits",
+                   "l2": "state 1 MB stays L2-resident between calls (latency measurement)"},
+        "roofline": {"kernel": "hb_block_attend", "bound": "hbm",
+                     "achieved": nbytes / (a_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": nbytes / (a_ms / 1e3) / 1e9 / peak, "peak_kind": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": a_ms,
+                     "traffic": None},
+        "components": {"attend_us": a_ms * 1e3, "commit_us": c_ms * 1e3,
+                       "attend_us_eager_python": a_host * 1e3,
+                       "timing": "CUDA graph of 50 back-to-back calls, replayed"},
+        "gpu_launches": 2 * 50 * reps,
+    }
+
+
+def run_stack(args):
+    """6 linearized layers, P=2,048-token prefixes, B in {1, 16, 64, 256}:
+    one stack step = hb_block_attend of all 6 layers, timed against
+    hb_softmax_kv_attend of the same 6 layers over the same prefixes kept as
+    a KV cache."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    cfg = hb.Config(H, D, FH, L)
+    stream = torch.cuda.current_stream()
+    peak, kind = _peaks()
+    sweep = []
+    P = 2048
+    for nB in args.stack_batches:
+        layers = []
+        for layer in range(N_LAYERS):
+            w = inputs.stack_layer(layer, nB, device=device, P=P)
+            t = w.tensors
+            S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
+            Z = torch.empty((nB, H, F), dtype=torch.float32, device=device)
+            sl = torch.arange(nB, dtype=torch.int32, device=device)
+            hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P,
+                                t["W"], S, Z)
+            need = hb.hb_softmax_kv_workspace_size(cfg, nB, P)
+            layers.append(dict(t=t, S=S, Z=Z, sl=sl, o=torch.empty_like(t["q"]),
+                               ws=torch.empty(max(need, 16), dtype=torch.uint8, device=device)))
+        torch.cuda.synchronize()
+
+        def hybrid():
+            for ly in layers:
+                t = ly["t"]
+                hb.hb_block_attend(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S"], ly["Z"],
+                                   t["W"], t["gate"], o=ly["o"])
+
+        def softmax():
+            for ly in layers:
+                t = ly["t"]
+                hb.hb_softmax_kv_attend(cfg, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P,
+                                        t["q"], t["k"], t["v"], o=ly["o"], workspace=ly["ws"])
+
+        reps = max(3, min(args.steps, 200))
+        h_ms = _graph_ms(hybrid, 1, reps, args.warmup, stream)
+        s_ms = _graph_ms(softmax, 1, max(3, reps // 4), args.warmup, stream)
+        assert hb.hb_get_device_status() == 0
+        hb_bytes = N_LAYERS * (nB * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W)
+        sm_bytes = N_LAYERS * nB * ((P + L) * H * D * 2 * 2 + 2 * L * H * D * 2)
+        sweep.append({
+            "batch": nB, "hybrid_ms": h_ms, "softmax_kv_ms": s_ms,
+            "hybrid_tokens_per_s": nB * L / (h_ms / 1e3),
+            "softmax_kv_tokens_per_s": nB * L / (s_ms / 1e3),
+            "speedup": s_ms / h_ms,
+            "hybrid_gbs": hb_bytes / (h_ms / 1e3) / 1e9,
+            "softmax_kv_gbs": sm_bytes / (s_ms / 1e3) / 1e9,
+            "hybrid_frac": hb_bytes / (h_ms / 1e3) / 1e9 / peak,
+            "softmax_kv_frac": sm_bytes / (s_ms / 1e3) / 1e9 / peak,
+        })
+        del layers
+        torch.cuda.empty_cache()
+    top = sweep[-1]
+    return {
+        "metric": "6-layer hybrid stack: active-block tokens/s vs softmax over KV cache",
+        "value": top["hybrid_tokens_per_s"], "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": top["hybrid_ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "6 linearized layers x 16 heads, d=128, f=64, L=32, 2,048-token "
+                               "prefixes; stack step = 6 attends", "batches": args.stack_batches,
+                   "timing": "each stack step captured as one CUDA graph and replayed",
+                   "l2": "6 layers' states and KV caches exceed L2 from B=16 on"},
+        "roofline": {"kernel": "hb_block_attend", "bound": "hbm", "achieved": top["hybrid_gbs"],
+                     "peak": peak, "unit": "GB/s", "frac": top["hybrid_frac"],
+                     "peak_kind": kind, "traffic": None},
+        "sweep": sweep,
+        "gpu_launches": N_LAYERS * args.steps,
+    }
+
+
+def cpu_baseline_prefill(max_seconds: float = 15.0, T: int = 256):
+    """The oracle's prefill on one 256-token prompt of the same shape."""
+    import numpy as np
+
+    import oracle.block_hybrid as ob
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    w = inputs.prompt_ingestion(device="cpu", B=1, T=T)
+    k = w.tensors["k"].to(torch.float64).numpy()
+    v = w.tensors["v"].to(torch.float64).numpy()
+    W = w.tensors["W"].to(torch.float64).numpy()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        ob.prefill(k, v, W)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= max_seconds or reps >= 1000:
+            break
+    del np
+    return {"value": reps * T / el, "unit": "tokens/s", "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} x one {T}-token prompt, 16 heads, fp64 numpy oracle, {el:.1f} s"}
+
+
 # ----------------------------------------------------------- CPU oracle arm
 
 def _oracle_sample(n_req: int, seed: int = 2):
@@ -414,6 +685,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack"],
+                    default="step",
+                    help="step: continuous-batching step (default); decode: single-layer "
+                         "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
+                         "softmax over a KV cache")
+    ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -422,6 +699,12 @@ def main(argv=None):
         line = run_reference(args, world, rank)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return 0
+    if args.workload != "step":
+        if world > 1:
+            ap.error("--workload other than step runs on one GPU")
+        runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack}
+        print(json.dumps(runner[args.workload](args)), flush=True)
         return 0
     if world > 1:
         import torch.distributed as dist

@@ -81,7 +81,8 @@ __device__ __forceinline__ uint32_t s_off(int k, int n) {
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
                   int merge, const int32_t* __restrict__ slot_idx,
-                  const float* __restrict__ Z_pool, const float* __restrict__ gate,
+                  const float* __restrict__ S_pool, const float* __restrict__ Z_pool,
+                  const float* __restrict__ gate,
                   __nv_bfloat16* __restrict__ o, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -106,43 +107,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop; lane 0 issues the copies. Slot indices
+    // are read 32 units at a time (lane j holds the slot of local unit
+    // 32w + j), and each unit's tiles are prefetched into L2 two units
+    // before their TMA load is issued, so that more than one unit per SM is
+    // in flight from DRAM while the consumers work.
     if (lane == 0) {
       prefetch_tmap(&maps.S);
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
       prefetch_tmap(&maps.v);
       prefetch_tmap(&maps.W);
-      int i = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
-        const int s = i & 1, n = i >> 1;
-        if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
-          atomicOr(status, kStatusTimeout);
-          break;
-        }
-        const int b = u / H, h = u - b * H;
-        const int slot = slot_idx[b];
+    }
+    const int first = blockIdx.x, stride = gridDim.x;
+    const int n_local = first < units ? (units - first + stride - 1) / stride : 0;
+    int win = -1, win_slot = -1;
+    auto slot_of = [&](int i) -> int {  // warp-uniform i, called in increasing order
+      if ((i >> 5) != win) {
+        win = i >> 5;
+        const int uu = first + (32 * win + lane) * stride;
+        win_slot = uu < units ? slot_idx[uu / H] : -1;
+      }
+      return __shfl_sync(0xffffffffu, win_slot, i & 31);
+    };
+    auto l2_prefetch = [&](int i, int slot) {
+      const int uu = first + i * stride;
+      const int b = uu / H, h = uu - b * H;
+      if (lane != 0 || slot < 0 || slot >= num_slots) return;
+      const size_t unit = (size_t)slot * H + h;
+      prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
+      prefetch_l2(Z_pool + unit * kF, kF * 4);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        prefetch_l2_3d(&maps.q, 64 * j, h, b * kL);
+        prefetch_l2_3d(&maps.k, 64 * j, h, b * kL);
+        prefetch_l2_3d(&maps.v, 64 * j, h, b * kL);
+      }
+    };
+    int slot_cur = n_local > 0 ? slot_of(0) : -1;
+    int slot_next = n_local > 1 ? slot_of(1) : -1;
+    if (n_local > 1) l2_prefetch(1, slot_next);
+    for (int i = 0; i < n_local; ++i) {
+      const int s = i & 1, n = i >> 1;
+      bool ok = true;
+      if (lane == 0 && n > 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        if (lane == 0) atomicOr(status, kStatusTimeout);
+        break;
+      }
+      const int u = first + i * stride;
+      const int b = u / H, h = u - b * H;
+      const int slot = slot_cur;
+      if (lane == 0) {
         uint8_t* st = smem + s * kStageStride;
         if (slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
           mbar_arrive(&full[s]);
-          continue;
-        }
-        meta[s] = 1;
-        mbar_arrive_expect_tx(&full[s], kTxBytes);
-        const int srow = (slot * H + h) * kF;
+        } else {
+          meta[s] = 1;
+          mbar_arrive_expect_tx(&full[s], kTxBytes);
+          const int srow = (slot * H + h) * kF;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &full[s]);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &full[s]);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, b * kL, &full[s]);
-          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, b * kL, &full[s]);
-          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, b * kL, &full[s]);
+          for (int j = 0; j < 2; ++j) {
+            tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, b * kL, &full[s]);
+            tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, b * kL, &full[s]);
+            tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, b * kL, &full[s]);
+          }
+          tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &full[s]);
+          bulk_load(st + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &full[s]);
         }
-        tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &full[s]);
-        bulk_load(st + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &full[s]);
       }
+      const int ahead = i + 2;
+      const int slot_ahead = ahead < n_local ? slot_of(ahead) : -1;
+      if (ahead < n_local) l2_prefetch(ahead, slot_ahead);
+      slot_cur = slot_next;
+      slot_next = slot_ahead;
     }
     return;
   }
@@ -158,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int i = 0;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
     const int s = i & 1, n = i >> 1;
+    // the gate is read before the wait so its latency hides behind it
+    const float gl = gate[u % H];
     if (!mbar_wait(&full[s], n & 1)) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
       break;
@@ -210,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc_s[r] *= scale;
+      for (int r = 0; r < 4; ++r) acc_s[r] *= scale;  // scale * log2(e): scores in base 2
       const int R0 = 16 * mt + g, R1 = R0 + 8;
       {
         float mx0 = fmaxf(fmaxf(acc_u[0][0], acc_u[0][1]), fmaxf(acc_u[1][0], acc_u[1][1]));
@@ -253,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          fmaxf(part(kSMax, R, 2), part(kSMax, R, 3)));
         }
         float sp[2] = {0.f, 0.f}, sm[2] = {0.f, 0.f}, dp[2] = {0.f, 0.f}, dm[2] = {0.f, 0.f};
+        // e^{x - M} = 2^{x log2(e) - M log2(e)}: one FMA and one ex2 each
+        const float op[2] = {-Mp[0] * kLog2e, -Mp[1] * kLog2e};
+        const float om[2] = {-Mm[0] * kLog2e, -Mm[1] * kLog2e};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
@@ -260,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hr = r >> 1;
             const int c = 16 * nq + 8 * nt + 2 * t + (r & 1);
             const float x = acc_u[nt][r];
-            const float e1 = expf(x - Mp[hr]);
-            const float e2 = expf(-x - Mm[hr]);
+            const float e1 = ex2_approx(fmaf(x, kLog2e, op[hr]));
+            const float e2 = ex2_approx(fmaf(-x, kLog2e, om[hr]));
             ep[nt][r] = e1;
             em[nt][r] = e2;
             sp[hr] += e1;
@@ -272,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float p[4], ss[2];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = expf(acc_s[r] - Ms[r >> 1]);
+        for (int r = 0; r < 4; ++r) p[r] = ex2_approx(acc_s[r] - Ms[r >> 1]);
         ss[0] = p[0] + p[1];
         ss[1] = p[2] + p[3];
 #pragma unroll
@@ -324,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (warp == 0) {
           const int R = lane;
+          const float aux = merge == HB_MERGE_SHARED_NORM ? log_sigmoid(gl) : sigmoid(gl);
           float m = part(kSMax, R, 0), ps = 0.f, sp = 0.f, sm = 0.f, dp = 0.f, dm = 0.f;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -334,9 +383,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             dp += part(kDenP, R, j);
             dm += part(kDenM, R, j);
           }
-          fin[R] = m;
-          fin[32 + R] = ps;
-          fin[64 + R] = dp / sp + dm / sm;
+          // Per-row coefficients of the merge, o = cU * U + cN * num, with
+          // U = sum_j e^{s_ij - m} v_j, P = ps = sum_j e^{s_ij - m}, m the row
+          // max (natural units), num = phi^T S, den = phi^T Z.
+          const float den = dp / sp + dm / sm;
+          const float mnat = m * kLn2;
+          float cU, cN;
+          if (merge == HB_MERGE_SHARED_NORM) {
+            // (w e^m U + num) / (w e^m P + den) with log w = aux, rescaled by
+            // e^{-lam} or e^{lam} (lam = aux + m) so nothing overflows
+            const float lam = aux + mnat;
+            if (lam >= 0.f) {
+              const float r = expf(-lam);
+              cU = 1.f / (ps + r * den);
+              cN = r * cU;
+            } else {
+              const float r = expf(lam);
+              cN = 1.f / (r * ps + den);
+              cU = r * cN;
+            }
+          } else if (den > 0.f) {
+            cU = aux / ps;
+            cN = (1.f - aux) / den;
+          } else {  // nothing committed: the linear branch is dropped
+            cU = 1.f / ps;
+            cN = 0.f;
+          }
+          fin[R] = cU;
+          fin[32 + R] = cN;
         }
       }
       named_bar_sync(1, kConsumers);
@@ -386,30 +460,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
+      // the stage (S, V) is no longer read: hand it back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
       // ---- merge and store o
-      const float gl = gate[h];
-      const float aux = merge == HB_MERGE_SHARED_NORM ? log_sigmoid(gl) : sigmoid(gl);
 #pragma unroll
       for (int m2 = 0; m2 < 2; ++m2) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int R = 16 * m2 + g + 8 * hr;
-          const float m = fin[R], P = fin[32 + R], den = fin[64 + R];
+          const float cU = fin[R], cN = fin[32 + R];
           __nv_bfloat16* orow = o + ((size_t)(b * kL + R) * H + h) * kD;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const int c = 16 * warp + 8 * nt + 2 * t;
-            const float o0 = merge_out(merge, acc_v[m2][nt][2 * hr], P, m, acc_n[m2][nt][2 * hr],
-                                       den, aux);
-            const float o1 = merge_out(merge, acc_v[m2][nt][2 * hr + 1], P, m,
-                                       acc_n[m2][nt][2 * hr + 1], den, aux);
+            const float o0 = fmaf(cU, acc_v[m2][nt][2 * hr], cN * acc_n[m2][nt][2 * hr]);
+            const float o1 = fmaf(cU, acc_v[m2][nt][2 * hr + 1], cN * acc_n[m2][nt][2 * hr + 1]);
             *reinterpret_cast<__nv_bfloat162*>(orow + c) = __floats2bfloat162_rn(o0, o1);
           }
         }
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -466,8 +541,9 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   }
   const int units = batch * s.H;
   const int grid = units < g_num_sms ? units : g_num_sms;
-  k_attend_fast<<<grid, kThreads, kSmemBytes, st>>>(maps, batch, s.H, num_slots, s.scale, s.merge,
-                                                    slot_idx, Z_pool, gate,
+  k_attend_fast<<<grid, kThreads, kSmemBytes, st>>>(maps, batch, s.H, num_slots,
+                                                    s.scale * kLog2e, s.merge,
+                                                    slot_idx, S_pool, Z_pool, gate,
                                                     reinterpret_cast<__nv_bfloat16*>(o), status);
   return cudaGetLastError();
 }

@@ -25,6 +25,11 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);
+// One 32-token block per (request, head), two CTAs per SM (hb_commit_fast.cu).
+bool commit_tc_fits(const Shape& s, int batch, int num_slots);
+cudaError_t launch_commit_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
+                             const void* v, const void* W, float* S_pool, float* Z_pool,
+                             int num_slots, unsigned* status, cudaStream_t st);
 size_t prefill_fast_workspace_bytes(const Shape& s, int batch, int64_t max_seqlen);
 cudaError_t launch_prefill_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                 const void* v, int64_t total_tokens, const int64_t* cu_seqlens,

@@ -6,17 +6,9 @@
 namespace hb {
 
 bool fast_feature_map_ok(const Shape&) { return false; }
-bool fast_softmax_kv_ok(const Shape&) { return false; }
 
 cudaError_t launch_feature_map_fast(const Shape&, int64_t, const void*, const void*, float*,
                                     cudaStream_t) {
   return cudaErrorNotSupported;
 }
-size_t softmax_kv_fast_workspace_bytes(const Shape&, int, int64_t) { return 0; }
-cudaError_t launch_softmax_kv_fast(const Shape&, int, const void*, const void*, int64_t,
-                                   const int64_t*, int64_t, const void*, const void*, const void*, void*, void*,
-                                   unsigned*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
 }  // namespace hb

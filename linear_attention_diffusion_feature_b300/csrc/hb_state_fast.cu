@@ -48,12 +48,13 @@ constexpr int kOffPhiHi = 147456;   // 2 atoms (F 0-63, 64-127) x [128 tok][128 
 constexpr int kOffPhiLo = 180224;
 constexpr int kOffOnes = 212992;    // [16 rows][128 B] of bf16 1.0
 constexpr int kOffBar = 215040;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kOffZOld = kOffBar + 256;  // [128] fp32: Z before this call (accumulating)
+constexpr int kSmemBytes = kOffZOld + 512 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
 // mbarrier slots
 enum { kKvFull0 = 0, kKvFull1, kKvEmpty0, kKvEmpty1, kWFull, kUFull0, kUFull1, kUEmpty0,
-       kUEmpty1, kPhiFull, kPhiEmpty, kAccFull, kNumBars };
+       kUEmpty1, kPhiFull, kPhiEmpty, kAccFull, kOldFull, kNumBars };
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[kPhiFull], 4);
     mbar_init(&bar[kPhiEmpty], 1);
     mbar_init(&bar[kAccFull], 1);
+    mbar_init(&bar[kOldFull], 1);
     fence_mbar_init();
   }
   if (warp >= 2) {  // constant ones tile (B operand of the Z contraction)
@@ -141,8 +143,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  // Accumulating into S/Z (a commit, or a prefill with accumulate = 1 and
+  // no split) needs the old state tile. A commit has exactly one chunk, so
+  // the second stage of the k/v ring is free from the start: the old rows
+  // 0-63 go to the k half, rows 64-127 to the v half, fetched now so the
+  // copy overlaps the whole contraction. A prompt uses both stages, so its
+  // old tile is only prefetched into L2 here and copied into the k region
+  // once the last MMA has finished.
+  const bool add_old = a.splits == 1 && a.accumulate != 0;
+  const bool commit_shape = a.cu == nullptr;
+  const size_t unit_off = (size_t)slot * a.H + h;
+  const float* S_old = a.S_pool + unit_off * kF * kD;
+  const float* Z_old = a.Z_pool + unit_off * kF;
+  uint8_t* old_lo = smem + (commit_shape ? kOffK + 32768 : kOffK);
+  uint8_t* old_hi = smem + (commit_shape ? kOffV + 32768 : kOffK + 32768);
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    if (lane == 0 && add_old) {
+      if (commit_shape) {
+        mbar_arrive_expect_tx(&bar[kOldFull], 2 * 32768 + 512);
+        bulk_load(old_lo, S_old, 32768, &bar[kOldFull]);
+        bulk_load(old_hi, S_old + 64 * kD, 32768, &bar[kOldFull]);
+        bulk_load(smem + kOffZOld, Z_old, 512, &bar[kOldFull]);
+      } else {
+        prefetch_l2(S_old, kF * kD * 4);
+        prefetch_l2(Z_old, kF * 4);
+      }
+    }
     if (lane == 0 && n_my > 0) {
       prefetch_tmap(&maps.k);
       prefetch_tmap(&maps.v);
@@ -242,32 +270,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t valid64 = cnt - (c_begin + c) * RB;
       const int valid = valid64 < RB ? (int)valid64 : RB;
       const bool live = tok < valid;
+      // Rows at or past the end of the last 16-token MMA step are never read
+      // by the phi^T V contraction, so their threads skip the softmaxes.
+      const bool used = tok < ((valid + 15) & ~15);
       float mx = -FLT_MAX, mn = FLT_MAX;
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         mx = fmaxf(mx, u[j]);
         mn = fminf(mn, u[j]);
       }
+      // e^{u - max} = 2^{u log2(e) - max log2(e)}: one FMA and one ex2 each
       float e[64];
       float sp = 0.f;
+      if (live) {
+        const float off = -mx * kLog2e;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        e[j] = expf(u[j] - mx);
-        sp += e[j];
+        for (int j = 0; j < 64; ++j) {
+          e[j] = ex2_approx(fmaf(u[j], kLog2e, off));
+          sp += e[j];
+        }
       }
       if (c >= 1 && !mbar_wait(&bar[kPhiEmpty], (c - 1) & 1)) { ok = false; break; }
       // positive half -> atom 0, negated half -> atom 1
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        if (half == 1) {
+        if (!used) break;
+        if (half == 1 && live) {
           sp = 0.f;
+          const float off = mn * kLog2e;
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
-            e[j] = expf(mn - u[j]);
+            e[j] = ex2_approx(fmaf(-u[j], kLog2e, off));
             sp += e[j];
           }
         }
-        const float inv = 1.f / sp;
+        const float inv = live ? 1.f / sp : 0.f;
         const uint32_t rowoff = half * 16384 + tok * 128;
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8) {
@@ -312,7 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool have = n_my > 0 && ok && mbar_wait(&bar[kAccFull], 0);
     if (n_my > 0 && ok && !have) atomicOr(a.status, kStatusTimeout);
     tc_fence_after();
-    const uint32_t stage = smem_u32(smem + kOffK);  // reused: all MMAs are done
+    if (add_old && !commit_shape && threadIdx.x == 64) {
+      // every MMA and TMA load has completed (kAccFull), so the k region is free
+      mbar_arrive_expect_tx(&bar[kOldFull], 2 * 32768 + 512);
+      bulk_load(old_lo, S_old, 32768, &bar[kOldFull]);
+      bulk_load(old_hi, S_old + 64 * kD, 32768, &bar[kOldFull]);
+      bulk_load(smem + kOffZOld, Z_old, 512, &bar[kOldFull]);
+    }
+    const uint32_t stage = smem_u32(smem + kOffPhiHi);  // 64 KiB, free once the MMAs are done
     float z = 0.f;
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
@@ -337,36 +381,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
     }
     tc_fence_before();
+    bool have_old = false;
+    if (add_old) {
+      have_old = mbar_wait(&bar[kOldFull], 0);
+      if (!have_old) atomicOr(a.status, kStatusTimeout);
+    }
     named_bar_sync(1, 128);
 
-    const size_t unit = (size_t)slot * a.H + h;
     float* Sdst;
     float* Zdst;
-    bool add_old;
     if (a.splits > 1) {
       float* p = a.ws + ((size_t)(b * a.H + h) * a.splits + split) * kPartialFloats;
       Sdst = p;
       Zdst = p + kF * kD;
-      add_old = false;
     } else {
-      Sdst = a.S_pool + unit * kF * kD;
-      Zdst = a.Z_pool + unit * kF;
-      add_old = a.accumulate != 0;
+      Sdst = a.S_pool + unit_off * kF * kD;
+      Zdst = a.Z_pool + unit_off * kF;
     }
-    const int ew = warp - 2;
-    for (int r = ew; r < kF; r += 4) {
-      float4 v = ld_shared_v4f(stage + r * 512 + ((lane ^ (r & 31)) << 4));
-      float4* dst = reinterpret_cast<float4*>(Sdst + r * kD) + lane;
-      if (add_old) {
-        const float4 o = *dst;
-        v.x += o.x;
-        v.y += o.y;
-        v.z += o.z;
-        v.w += o.w;
+    if (add_old && !have_old) {
+      // the old tile never arrived: leave S/Z as they were (flagged above)
+    } else {
+      const int ew = warp - 2;
+      const uint32_t olo = smem_u32(old_lo), ohi = smem_u32(old_hi);
+#pragma unroll 4
+      for (int r = ew; r < kF; r += 4) {
+        float4 v = ld_shared_v4f(stage + r * 512 + ((lane ^ (r & 31)) << 4));
+        if (add_old) {
+          const float4 o = ld_shared_v4f((r < 64 ? olo + r * 512 : ohi + (r - 64) * 512) + lane * 16);
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        reinterpret_cast<float4*>(Sdst + r * kD)[lane] = v;
       }
-      *dst = v;
+      const float* zold = reinterpret_cast<const float*>(smem + kOffZOld);
+      Zdst[tok] = add_old ? zold[tok] + z : z;
     }
-    Zdst[tok] = add_old ? Zdst[tok] + z : z;
   }
 
   __syncthreads();
@@ -474,6 +525,8 @@ bool fast_state_ok(const Shape& s) { return production_shape(s); }
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st) {
+  if (commit_tc_fits(s, batch, num_slots))
+    return launch_commit_tc(s, batch, slot_idx, k, v, W, S_pool, Z_pool, num_slots, status, st);
   const int64_t rows = (int64_t)batch * s.L;
   if (rows >= (int64_t)1 << 31 || batch > 65535)
     return launch_state_accumulate_generic(s, batch, slot_idx, k, v, rows, nullptr, s.L, W,
