@@ -11,16 +11,27 @@
 // 2/3 of the bytes), so the kernel is a persistent streaming pipeline:
 //   * one CTA per SM, 9 warps: warp 8 is the producer, warps 0-7 compute;
 //   * a two-stage shared-memory ring; each stage holds one (request, head)
-//     unit: S (four 16 KiB SWIZZLE_128B TMA boxes), q, k, v (two 4 KiB boxes
-//     each), W_h (16 KiB) and Z (512 B bulk copy), all arriving on one
-//     mbarrier;
-//   * the producer issues unit i+1's loads while the consumers compute
-//     unit i; consumers release a stage through a second mbarrier;
+//     unit in two parts with their own mbarriers: the head (q, k, v as two
+//     4 KiB SWIZZLE_128B boxes each, W_h 16 KiB, Z 512 B) and S (four 16 KiB
+//     SWIZZLE_128B boxes); the feature map and block softmax run on the head
+//     while S is still arriving;
+//   * the producer reads slot indices ahead, prefetches the tiles of the
+//     units two steps ahead into L2, and issues unit i+1's loads while the
+//     consumers compute unit i; consumers release a stage through a third
+//     mbarrier as soon as S and V have been read;
+//   * once q and k have been used their bytes hold the unit's feature map,
+//     block probabilities and row sums;
 //   * all four contractions (qW, qk^T, phi(q)S, PV) run on bf16 mma.sync with
-//     fp32 accumulation; S is converted fp32 -> bf16 pairs as it is read
-//     from shared memory (the swizzle makes those reads conflict-free);
-//   * both softmaxes of phi and the block softmax use fp32 expf; the merge
-//     is the overflow-free rescaled form in merge_out().
+//     fp32 accumulation. The two halves of phi(q) enter the S contraction
+//     unnormalised and in separate accumulators; their normalisers, the
+//     block softmax normaliser, phi(q)^T Z and the gate fold into three
+//     per-row coefficients of the merge. S is converted fp32 -> bf16 pairs
+//     as it is read from shared memory, two columns per 8-byte load (the
+//     output columns of a warp are interleaved so that one thread's columns
+//     are adjacent), conflict-free thanks to the swizzle;
+//   * exponentials are 2^x on the special-function unit with log2(e) folded
+//     into the operands; the shared-normaliser merge is rescaled so that
+//     nothing overflows.
 #include <float.h>
 
 #include "hb_fast.cuh"
@@ -42,23 +53,26 @@ constexpr int kOffQ = 65536;                // 2 x [32 tokens][64 bf16], SW128
 constexpr int kOffK = kOffQ + 8192;
 constexpr int kOffV = kOffK + 8192;
 constexpr int kOffW = kOffV + 8192;         // [128 d-rows][64 bf16], SW128
-constexpr int kOffZ = kOffW + 16384;        // [128] fp32
-constexpr int kTxBytes = kOffZ + 512;       // every byte of a stage comes by TMA
-constexpr int kStageStride = 107520;        // 105 KiB
-// Shared buffers of the consumers.
-constexpr int kOffPhi = 2 * kStageStride;   // 2 x [32][64 bf16], SW128 (phi(q) as bf16)
-constexpr int kOffP = kOffPhi + 8192;       // [32][40 bf16]: e^{s - m}, 80-byte rows
+constexpr int kStageStride = kOffW + 16384; // 104 KiB
+constexpr int kHeadBytes = 3 * 8192 + 16384;
+constexpr int kSBytes = 65536;
+// Consumer scratch inside the stage, valid once phase A is done with q and k:
+constexpr int kOffPhi = kOffQ;              // 2 x [32][64 bf16], SW128: e^{u - max}, e^{min - u}
+constexpr int kOffP = kOffK;                // [32][40 bf16]: 2^{s - m}, 80-byte rows
 constexpr int kPitchP = 80;
-constexpr int kOffStats = kOffP + 32 * kPitchP;
-// stats (floats): 8 partial arrays [32 rows][4 quarters], then 3 finals [32]
-enum { kPMax = 0, kPMin, kSMax, kSumP, kSumM, kDenP, kDenM, kSumS, kNumPart };
-constexpr int kOffFin = kOffStats + kNumPart * 32 * 4 * 4;
-constexpr int kOffBar = kOffFin + 3 * 32 * 4;
-constexpr int kOffMeta = kOffBar + 4 * 8;
+constexpr int kOffSums = kOffK + 32 * kPitchP;  // 5 x [32 rows][4 parts] fp32
+static_assert(kOffSums + 5 * 32 * 4 * 4 <= kOffV, "scratch overflows the k tile");
+// Shared area after the two stages.
+constexpr int kOffZ = 2 * kStageStride;     // 2 x [128] fp32 (per stage)
+constexpr int kOffPart = kOffZ + 1024;      // max, min of u; max of s: 3 x [32 rows][4 parts]
+constexpr int kOffFin = kOffPart + 3 * 512; // merge coefficients: 3 x [32]
+constexpr int kOffBar = kOffFin + 3 * 128;
+constexpr int kOffMeta = kOffBar + 6 * 8;
 constexpr int kSmemUsed = kOffMeta + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
-static_assert(kTxBytes <= kStageStride, "stage overflow");
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
+
+enum { kSumP = 0, kSumM, kDenP, kDenM, kSumS };
 
 struct Maps {
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
@@ -77,6 +91,11 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 __device__ __forceinline__ uint32_t s_off(int k, int n) {
   return (uint32_t)((n >> 5) * 16384 + k * 128 + ((((n & 31) >> 2) ^ (k & 7)) << 4) + (n & 3) * 4);
 }
+// Byte offset of v[key][n] (bf16) in the two SW128 boxes of the v tile.
+__device__ __forceinline__ uint32_t v_off(int key, int n) {
+  return (uint32_t)((n >> 6) * 4096 + key * 128 + ((((n & 63) >> 3) ^ (key & 7)) << 4) +
+                    (n & 7) * 2);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
@@ -87,31 +106,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + 2;
+  uint64_t* head_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* s_full = head_full + 2;
+  uint64_t* empty = head_full + 4;
   int* meta = reinterpret_cast<int*>(smem + kOffMeta);
-  float* stats = reinterpret_cast<float*>(smem + kOffStats);
-  float* fin = reinterpret_cast<float*>(smem + kOffFin);
+  float* pmax = reinterpret_cast<float*>(smem + kOffPart);  // [32][4]
+  float* pmin = pmax + 128;                                 // [32][4]
+  float* smax = pmin + 128;                                 // [32][4]
+  float* fin = reinterpret_cast<float*>(smem + kOffFin);    // cU, cP, cM: [3][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = batch * H;
 
   if (threadIdx.x == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(&empty[0], kConsumerWarps);
-    mbar_init(&empty[1], kConsumerWarps);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&head_full[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    // The whole warp runs the loop; lane 0 issues the copies. Slot indices
-    // are read 32 units at a time (lane j holds the slot of local unit
-    // 32w + j), and each unit's tiles are prefetched into L2 two units
-    // before their TMA load is issued, so that more than one unit per SM is
-    // in flight from DRAM while the consumers work.
+    // The whole warp runs the loop; lane 0 issues the copies. A unit's q, k,
+    // v and W_h do not depend on its state slot, so they are issued before
+    // the slot index is known. Slot indices are read 32 units at a time
+    // (lane j holds the slot of local unit 32w + j), and each unit's tiles
+    // are prefetched into L2 two units before their TMA load is issued.
     if (lane == 0) {
       prefetch_tmap(&maps.S);
       prefetch_tmap(&maps.q);
@@ -144,9 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_l2_3d(&maps.v, 64 * j, h, b * kL);
       }
     };
-    int slot_cur = n_local > 0 ? slot_of(0) : -1;
-    int slot_next = n_local > 1 ? slot_of(1) : -1;
-    if (n_local > 1) l2_prefetch(1, slot_next);
+    int slot_next = -1;
     for (int i = 0; i < n_local; ++i) {
       const int s = i & 1, n = i >> 1;
       bool ok = true;
@@ -157,266 +178,271 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int u = first + i * stride;
       const int b = u / H, h = u - b * H;
-      const int slot = slot_cur;
+      uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
-        uint8_t* st = smem + s * kStageStride;
+        mbar_expect_tx(&head_full[s], kHeadBytes);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, b * kL, &head_full[s]);
+          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, b * kL, &head_full[s]);
+          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, b * kL, &head_full[s]);
+        }
+        tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
+      }
+      const int slot = i == 0 ? slot_of(0) : slot_next;
+      if (lane == 0) {
         if (slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
-          mbar_arrive(&full[s]);
+          mbar_arrive(&head_full[s]);
+          mbar_arrive(&s_full[s]);
         } else {
           meta[s] = 1;
-          mbar_arrive_expect_tx(&full[s], kTxBytes);
+          mbar_expect_tx(&head_full[s], 512);
+          bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
+                    &head_full[s]);
+          mbar_arrive(&head_full[s]);
+          mbar_arrive_expect_tx(&s_full[s], kSBytes);
           const int srow = (slot * H + h) * kF;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &full[s]);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, b * kL, &full[s]);
-            tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, b * kL, &full[s]);
-            tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, b * kL, &full[s]);
-          }
-          tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &full[s]);
-          bulk_load(st + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &full[s]);
+            tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
         }
       }
-      const int ahead = i + 2;
-      const int slot_ahead = ahead < n_local ? slot_of(ahead) : -1;
-      if (ahead < n_local) l2_prefetch(ahead, slot_ahead);
-      slot_cur = slot_next;
-      slot_next = slot_ahead;
+      if (i + 1 < n_local) slot_next = slot_of(i + 1);
+      if (i == 0 && n_local > 1) l2_prefetch(1, slot_next);
+      if (i + 2 < n_local) l2_prefetch(i + 2, slot_of(i + 2));
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  // Warp w: row tile mt = w & 1 (rows 16 mt .. 16 mt + 15), column quarter
+  // nq = w >> 1 of u = q W_h (16 of 64 columns) and keys 8 nq .. 8 nq + 7 of
+  // the block scores; in phase D, output columns 16 w .. 16 w + 15 of both
+  // row tiles, interleaved: physical column 16 w + 2 c + j is column c of
+  // n-tile j.
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t sPhi = smem_u32(smem + kOffPhi);
-  const uint32_t sP = smem_u32(smem + kOffP);
-  auto part = [&](int which, int row, int quarter) -> float& {
-    return stats[(which * 32 + row) * 4 + quarter];
-  };
+  const int mt = warp & 1, nq = warp >> 1;
+  const int c0 = 16 * warp;
 
+  // A wait that runs out does not leave the loop on its own: the warp goes on
+  // to the next named barrier, which also votes, and all warps leave
+  // together (a warp left behind at a named barrier would never return).
   int i = 0;
+  bool aborted = false;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
     const int s = i & 1, n = i >> 1;
     // the gate is read before the wait so its latency hides behind it
     const float gl = gate[u % H];
-    if (!mbar_wait(&full[s], n & 1)) {
-      if (lane == 0) atomicOr(status, kStatusTimeout);
+    const bool head_ok = mbar_wait(&head_full[s], n & 1);
+    uint8_t* st = smem + s * kStageStride;
+    const uint32_t sS = smem_u32(st + kOffS);
+    const uint32_t sQ = smem_u32(st + kOffQ);
+    const uint32_t sK = smem_u32(st + kOffK);
+    const uint32_t sV = smem_u32(st + kOffV);
+    const uint32_t sW = smem_u32(st + kOffW);
+    const uint32_t sPhi = smem_u32(st + kOffPhi);
+    const uint32_t sP = smem_u32(st + kOffP);
+    float* sums = reinterpret_cast<float*>(st + kOffSums);  // [5][32][4]
+    const float* sZ = reinterpret_cast<const float*>(smem + kOffZ + s * 512);
+    const int b = u / H, h = u - b * H;
+    const int R0 = 16 * mt + g, R1 = R0 + 8;
+
+    // ---- phase A: u = q W_h (16 rows x 16 cols per warp) and
+    //      s = q k^T (16 rows x 8 keys per warp)
+    float acc_u[2][4] = {}, acc_s[4] = {};
+    {
+      const int arow = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk += 2) {
+        uint32_t a0[4], a1[4];
+        {
+          const int ch = 2 * kk + (lane >> 4);
+          ldsm_x4(sQ + (ch >> 3) * 4096 + sw128(arow, ch & 7), a0[0], a0[1], a0[2], a0[3]);
+          const int ch1 = ch + 2;
+          ldsm_x4(sQ + (ch1 >> 3) * 4096 + sw128(arow, ch1 & 7), a1[0], a1[1], a1[2], a1[3]);
+        }
+        // k^T fragments for keys 8nq..8nq+7, two k16 steps at once
+        uint32_t kb[4];
+        {
+          const int krow = 8 * nq + (lane & 7);
+          const int ch = 2 * kk + (lane >> 3);
+          ldsm_x4(sK + (ch >> 3) * 4096 + sw128(krow, ch & 7), kb[0], kb[1], kb[2], kb[3]);
+        }
+        mma_bf16(acc_s, a0, kb[0], kb[1]);
+        mma_bf16(acc_s, a1, kb[2], kb[3]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int k16 = kk + half;
+          uint32_t wb[4];
+          const int mtx = lane >> 3;
+          const int krow = 16 * k16 + (mtx & 1) * 8 + (lane & 7);
+          const int nch = 2 * nq + (mtx >> 1);
+          ldsm_x4_t(sW + sw128(krow, nch), wb[0], wb[1], wb[2], wb[3]);
+          mma_bf16(acc_u[0], half ? a1 : a0, wb[0], wb[1]);
+          mma_bf16(acc_u[1], half ? a1 : a0, wb[2], wb[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc_s[r] *= scale;  // scale * log2(e): scores in base 2
+    {
+      float mx0 = fmaxf(fmaxf(acc_u[0][0], acc_u[0][1]), fmaxf(acc_u[1][0], acc_u[1][1]));
+      float mx1 = fmaxf(fmaxf(acc_u[0][2], acc_u[0][3]), fmaxf(acc_u[1][2], acc_u[1][3]));
+      float mn0 = fminf(fminf(acc_u[0][0], acc_u[0][1]), fminf(acc_u[1][0], acc_u[1][1]));
+      float mn1 = fminf(fminf(acc_u[0][2], acc_u[0][3]), fminf(acc_u[1][2], acc_u[1][3]));
+      float sm0 = fmaxf(acc_s[0], acc_s[1]), sm1 = fmaxf(acc_s[2], acc_s[3]);
+#pragma unroll
+      for (int o2 = 1; o2 < 4; o2 <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, o2));
+        mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, o2));
+        sm0 = fmaxf(sm0, __shfl_xor_sync(0xffffffffu, sm0, o2));
+        sm1 = fmaxf(sm1, __shfl_xor_sync(0xffffffffu, sm1, o2));
+      }
+      if (t == 0) {
+        pmax[R0 * 4 + nq] = mx0;
+        pmax[R1 * 4 + nq] = mx1;
+        pmin[R0 * 4 + nq] = mn0;
+        pmin[R1 * 4 + nq] = mn1;
+        smax[R0 * 4 + nq] = sm0;
+        smax[R1 * 4 + nq] = sm1;
+      }
+    }
+    // q and k are no longer read after this barrier
+    if (named_bar_any(1, kConsumers, !head_ok)) {
+      if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+      aborted = true;
       break;
     }
-    if (meta[s]) {
-      uint8_t* st = smem + s * kStageStride;
-      const uint32_t sS = smem_u32(st + kOffS);
-      const uint32_t sQ = smem_u32(st + kOffQ);
-      const uint32_t sK = smem_u32(st + kOffK);
-      const uint32_t sV = smem_u32(st + kOffV);
-      const uint32_t sW = smem_u32(st + kOffW);
-      const float* sZ = reinterpret_cast<const float*>(st + kOffZ);
-      const int b = u / H, h = u - b * H;
 
-      // ---- phase A: u = q W_h (16 rows x 16 cols per warp) and
-      //      s = q k^T (16 rows x 8 keys per warp)
-      const int mt = warp & 1, nq = warp >> 1;
-      float acc_u[2][4] = {}, acc_s[4] = {};
-      {
-        const int arow = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+    // ---- phase B: unnormalised exponentials of both halves of phi(q), their
+    //      partial sums and partial dot products with Z; P = 2^{s - m}
+    {
+      float op[2], om[2], Ms[2];
 #pragma unroll
-        for (int kk = 0; kk < 8; kk += 2) {
-          uint32_t a0[4], a1[4];
-          {
-            const int ch = 2 * kk + (lane >> 4);
-            ldsm_x4(sQ + (ch >> 3) * 4096 + sw128(arow, ch & 7), a0[0], a0[1], a0[2], a0[3]);
-            const int ch1 = ch + 2;
-            ldsm_x4(sQ + (ch1 >> 3) * 4096 + sw128(arow, ch1 & 7), a1[0], a1[1], a1[2], a1[3]);
-          }
-          // k^T fragments for keys 8nq..8nq+7, two k16 steps at once
-          uint32_t kb[4];
-          {
-            const int krow = 8 * nq + (lane & 7);
-            const int ch = 2 * kk + (lane >> 3);
-            ldsm_x4(sK + (ch >> 3) * 4096 + sw128(krow, ch & 7), kb[0], kb[1], kb[2], kb[3]);
-          }
-          mma_bf16(acc_s, a0, kb[0], kb[1]);
-          mma_bf16(acc_s, a1, kb[2], kb[3]);
+      for (int hr = 0; hr < 2; ++hr) {
+        const int R = hr ? R1 : R0;
+        const float4 a = *reinterpret_cast<const float4*>(pmax + R * 4);
+        const float4 c = *reinterpret_cast<const float4*>(pmin + R * 4);
+        const float4 f = *reinterpret_cast<const float4*>(smax + R * 4);
+        op[hr] = -fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)) * kLog2e;
+        om[hr] = fminf(fminf(c.x, c.y), fminf(c.z, c.w)) * kLog2e;
+        Ms[hr] = fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w));
+      }
+      float sp[2] = {0.f, 0.f}, sm[2] = {0.f, 0.f}, dp[2] = {0.f, 0.f}, dm[2] = {0.f, 0.f};
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int k16 = kk + half;
-            uint32_t wb[4];
-            const int mtx = lane >> 3;
-            const int krow = 16 * k16 + (mtx & 1) * 8 + (lane & 7);
-            const int nch = 2 * nq + (mtx >> 1);
-            ldsm_x4_t(sW + sw128(krow, nch), wb[0], wb[1], wb[2], wb[3]);
-            mma_bf16(acc_u[0], half ? a1 : a0, wb[0], wb[1]);
-            mma_bf16(acc_u[1], half ? a1 : a0, wb[2], wb[3]);
-          }
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * nq + 8 * nt + 2 * t;
+        const float2 zp = *reinterpret_cast<const float2*>(sZ + c);
+        const float2 zm = *reinterpret_cast<const float2*>(sZ + kFH + c);
+        float ep[4], em[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int hr = r >> 1;
+          const float x = acc_u[nt][r];
+          ep[r] = ex2_approx(fmaf(x, kLog2e, op[hr]));   // e^{u - max u}
+          em[r] = ex2_approx(fmaf(-x, kLog2e, om[hr]));  // e^{min u - u}
+          sp[hr] += ep[r];
+          sm[hr] += em[r];
+          dp[hr] = fmaf(ep[r], (r & 1) ? zp.y : zp.x, dp[hr]);
+          dm[hr] = fmaf(em[r], (r & 1) ? zm.y : zm.x, dm[hr]);
+        }
+        const uint32_t off0 = sw128(R0, c >> 3) + (c & 7) * 2;
+        const uint32_t off1 = sw128(R1, c >> 3) + (c & 7) * 2;
+        st_shared_u32(sPhi + off0, pack_bf16(ep[0], ep[1]));
+        st_shared_u32(sPhi + off1, pack_bf16(ep[2], ep[3]));
+        st_shared_u32(sPhi + 4096 + off0, pack_bf16(em[0], em[1]));
+        st_shared_u32(sPhi + 4096 + off1, pack_bf16(em[2], em[3]));
+      }
+      float p[4], ss[2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) p[r] = ex2_approx(acc_s[r] - Ms[r >> 1]);
+      ss[0] = p[0] + p[1];
+      ss[1] = p[2] + p[3];
+#pragma unroll
+      for (int o2 = 1; o2 < 4; o2 <<= 1) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          sp[hr] += __shfl_xor_sync(0xffffffffu, sp[hr], o2);
+          sm[hr] += __shfl_xor_sync(0xffffffffu, sm[hr], o2);
+          dp[hr] += __shfl_xor_sync(0xffffffffu, dp[hr], o2);
+          dm[hr] += __shfl_xor_sync(0xffffffffu, dm[hr], o2);
+          ss[hr] += __shfl_xor_sync(0xffffffffu, ss[hr], o2);
         }
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc_s[r] *= scale;  // scale * log2(e): scores in base 2
-      const int R0 = 16 * mt + g, R1 = R0 + 8;
-      {
-        float mx0 = fmaxf(fmaxf(acc_u[0][0], acc_u[0][1]), fmaxf(acc_u[1][0], acc_u[1][1]));
-        float mx1 = fmaxf(fmaxf(acc_u[0][2], acc_u[0][3]), fmaxf(acc_u[1][2], acc_u[1][3]));
-        float mn0 = fminf(fminf(acc_u[0][0], acc_u[0][1]), fminf(acc_u[1][0], acc_u[1][1]));
-        float mn1 = fminf(fminf(acc_u[0][2], acc_u[0][3]), fminf(acc_u[1][2], acc_u[1][3]));
-        float sm0 = fmaxf(acc_s[0], acc_s[1]), sm1 = fmaxf(acc_s[2], acc_s[3]);
-#pragma unroll
-        for (int o2 = 1; o2 < 4; o2 <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-          mn0 = fminf(mn0, __shfl_xor_sync(0xffffffffu, mn0, o2));
-          mn1 = fminf(mn1, __shfl_xor_sync(0xffffffffu, mn1, o2));
-          sm0 = fmaxf(sm0, __shfl_xor_sync(0xffffffffu, sm0, o2));
-          sm1 = fmaxf(sm1, __shfl_xor_sync(0xffffffffu, sm1, o2));
-        }
-        if (t == 0) {
-          part(kPMax, R0, nq) = mx0;
-          part(kPMax, R1, nq) = mx1;
-          part(kPMin, R0, nq) = mn0;
-          part(kPMin, R1, nq) = mn1;
-          part(kSMax, R0, nq) = sm0;
-          part(kSMax, R1, nq) = sm1;
-        }
-      }
-      named_bar_sync(1, kConsumers);
-
-      // ---- phase B: exponentials, partial sums, partial phi^T Z, P = e^{s-m}
-      float ep[2][4], em[2][4];
-      {
-        float Mp[2], Mm[2], Ms[2];
+      if (t == 0) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int R = hr ? R1 : R0;
-          Mp[hr] = fmaxf(fmaxf(part(kPMax, R, 0), part(kPMax, R, 1)),
-                         fmaxf(part(kPMax, R, 2), part(kPMax, R, 3)));
-          Mm[hr] = -fminf(fminf(part(kPMin, R, 0), part(kPMin, R, 1)),
-                          fminf(part(kPMin, R, 2), part(kPMin, R, 3)));
-          Ms[hr] = fmaxf(fmaxf(part(kSMax, R, 0), part(kSMax, R, 1)),
-                         fmaxf(part(kSMax, R, 2), part(kSMax, R, 3)));
-        }
-        float sp[2] = {0.f, 0.f}, sm[2] = {0.f, 0.f}, dp[2] = {0.f, 0.f}, dm[2] = {0.f, 0.f};
-        // e^{x - M} = 2^{x log2(e) - M log2(e)}: one FMA and one ex2 each
-        const float op[2] = {-Mp[0] * kLog2e, -Mp[1] * kLog2e};
-        const float om[2] = {-Mm[0] * kLog2e, -Mm[1] * kLog2e};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int hr = r >> 1;
-            const int c = 16 * nq + 8 * nt + 2 * t + (r & 1);
-            const float x = acc_u[nt][r];
-            const float e1 = ex2_approx(fmaf(x, kLog2e, op[hr]));
-            const float e2 = ex2_approx(fmaf(-x, kLog2e, om[hr]));
-            ep[nt][r] = e1;
-            em[nt][r] = e2;
-            sp[hr] += e1;
-            sm[hr] += e2;
-            dp[hr] = fmaf(e1, sZ[c], dp[hr]);
-            dm[hr] = fmaf(e2, sZ[kFH + c], dm[hr]);
-          }
-        }
-        float p[4], ss[2];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = ex2_approx(acc_s[r] - Ms[r >> 1]);
-        ss[0] = p[0] + p[1];
-        ss[1] = p[2] + p[3];
-#pragma unroll
-        for (int o2 = 1; o2 < 4; o2 <<= 1) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            sp[hr] += __shfl_xor_sync(0xffffffffu, sp[hr], o2);
-            sm[hr] += __shfl_xor_sync(0xffffffffu, sm[hr], o2);
-            dp[hr] += __shfl_xor_sync(0xffffffffu, dp[hr], o2);
-            dm[hr] += __shfl_xor_sync(0xffffffffu, dm[hr], o2);
-            ss[hr] += __shfl_xor_sync(0xffffffffu, ss[hr], o2);
-          }
-        }
-        if (t == 0) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int R = hr ? R1 : R0;
-            part(kSumP, R, nq) = sp[hr];
-            part(kSumM, R, nq) = sm[hr];
-            part(kDenP, R, nq) = dp[hr];
-            part(kDenM, R, nq) = dm[hr];
-            part(kSumS, R, nq) = ss[hr];
-          }
-        }
-        const int key = 8 * nq + 2 * t;
-        st_shared_u32(sP + R0 * kPitchP + key * 2, pack_bf16(p[0], p[1]));
-        st_shared_u32(sP + R1 * kPitchP + key * 2, pack_bf16(p[2], p[3]));
-      }
-      named_bar_sync(1, kConsumers);
-
-      // ---- phase C: phi(q) = e / sum -> bf16 in shared memory; row finals
-      {
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int R = hr ? R1 : R0;
-          const float ip = 1.f / (part(kSumP, R, 0) + part(kSumP, R, 1) + part(kSumP, R, 2) +
-                                  part(kSumP, R, 3));
-          const float im = 1.f / (part(kSumM, R, 0) + part(kSumM, R, 1) + part(kSumM, R, 2) +
-                                  part(kSumM, R, 3));
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int c = 16 * nq + 8 * nt + 2 * t;  // even column of the pair
-            const int chunk = c >> 3;                // 0..7 within the 64-wide box
-            const uint32_t off = sw128(R, chunk) + (c & 7) * 2;
-            st_shared_u32(sPhi + off, pack_bf16(ep[nt][2 * hr] * ip, ep[nt][2 * hr + 1] * ip));
-            st_shared_u32(sPhi + 4096 + off,
-                          pack_bf16(em[nt][2 * hr] * im, em[nt][2 * hr + 1] * im));
-          }
-        }
-        if (warp == 0) {
-          const int R = lane;
-          const float aux = merge == HB_MERGE_SHARED_NORM ? log_sigmoid(gl) : sigmoid(gl);
-          float m = part(kSMax, R, 0), ps = 0.f, sp = 0.f, sm = 0.f, dp = 0.f, dm = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            m = fmaxf(m, part(kSMax, R, j));
-            ps += part(kSumS, R, j);
-            sp += part(kSumP, R, j);
-            sm += part(kSumM, R, j);
-            dp += part(kDenP, R, j);
-            dm += part(kDenM, R, j);
-          }
-          // Per-row coefficients of the merge, o = cU * U + cN * num, with
-          // U = sum_j e^{s_ij - m} v_j, P = ps = sum_j e^{s_ij - m}, m the row
-          // max (natural units), num = phi^T S, den = phi^T Z.
-          const float den = dp / sp + dm / sm;
-          const float mnat = m * kLn2;
-          float cU, cN;
-          if (merge == HB_MERGE_SHARED_NORM) {
-            // (w e^m U + num) / (w e^m P + den) with log w = aux, rescaled by
-            // e^{-lam} or e^{lam} (lam = aux + m) so nothing overflows
-            const float lam = aux + mnat;
-            if (lam >= 0.f) {
-              const float r = expf(-lam);
-              cU = 1.f / (ps + r * den);
-              cN = r * cU;
-            } else {
-              const float r = expf(lam);
-              cN = 1.f / (r * ps + den);
-              cU = r * cN;
-            }
-          } else if (den > 0.f) {
-            cU = aux / ps;
-            cN = (1.f - aux) / den;
-          } else {  // nothing committed: the linear branch is dropped
-            cU = 1.f / ps;
-            cN = 0.f;
-          }
-          fin[R] = cU;
-          fin[32 + R] = cN;
+          sums[(kSumP * 32 + R) * 4 + nq] = sp[hr];
+          sums[(kSumM * 32 + R) * 4 + nq] = sm[hr];
+          sums[(kDenP * 32 + R) * 4 + nq] = dp[hr];
+          sums[(kDenM * 32 + R) * 4 + nq] = dm[hr];
+          sums[(kSumS * 32 + R) * 4 + nq] = ss[hr];
         }
       }
-      named_bar_sync(1, kConsumers);
+      const int key = 8 * nq + 2 * t;
+      st_shared_u32(sP + R0 * kPitchP + key * 2, pack_bf16(p[0], p[1]));
+      st_shared_u32(sP + R1 * kPitchP + key * 2, pack_bf16(p[2], p[3]));
+    }
+    named_bar_sync(1, kConsumers);
 
-      // ---- phase D: num = phi(q) S and U = P V for columns 16w..16w+15
-      float acc_n[2][2][4] = {}, acc_v[2][2][4] = {};
+    // ---- per-row merge coefficients (lanes 0-3 of warp w: rows 4w .. 4w+3),
+    //      o = cU U + cP num+ + cM num-, with U = sum_j e^{s_ij - m} v_j,
+    //      num+- the contractions of the unnormalised halves with S
+    if (lane < 4) {
+      const int R = 4 * warp + lane;
+      const float4 a = *reinterpret_cast<const float4*>(sums + (kSumP * 32 + R) * 4);
+      const float4 c = *reinterpret_cast<const float4*>(sums + (kSumM * 32 + R) * 4);
+      const float4 d = *reinterpret_cast<const float4*>(sums + (kDenP * 32 + R) * 4);
+      const float4 e = *reinterpret_cast<const float4*>(sums + (kDenM * 32 + R) * 4);
+      const float4 f = *reinterpret_cast<const float4*>(sums + (kSumS * 32 + R) * 4);
+      const float4 m4 = *reinterpret_cast<const float4*>(smax + R * 4);
+      const float sp = (a.x + a.y) + (a.z + a.w), sm = (c.x + c.y) + (c.z + c.w);
+      const float ps = (f.x + f.y) + (f.z + f.w);
+      const float isp = 1.f / sp, ism = 1.f / sm;
+      const float den = ((d.x + d.y) + (d.z + d.w)) * isp + ((e.x + e.y) + (e.z + e.w)) * ism;
+      const float mnat = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)) * kLn2;
+      float cU, cN;
+      if (merge == HB_MERGE_SHARED_NORM) {
+        // (w e^m U + num) / (w e^m P + den) with log w = log sigmoid(alpha),
+        // rescaled by e^{-lam} or e^{lam} (lam = log w + m) so nothing overflows
+        const float lam = log_sigmoid(gl) + mnat;
+        if (lam >= 0.f) {
+          const float r = expf(-lam);
+          cU = 1.f / (ps + r * den);
+          cN = r * cU;
+        } else {
+          const float r = expf(lam);
+          cN = 1.f / (r * ps + den);
+          cU = r * cN;
+        }
+      } else {
+        const float w = sigmoid(gl);
+        if (den > 0.f) {
+          cU = w / ps;
+          cN = (1.f - w) / den;
+        } else {  // nothing committed: the linear branch is dropped
+          cU = 1.f / ps;
+          cN = 0.f;
+        }
+      }
+      fin[R] = cU;
+      fin[32 + R] = cN * isp;
+      fin[64 + R] = cN * ism;
+    }
+
+    // ---- phase D: num+- = e+- S and U = P V for columns 16w .. 16w + 15
+    // (a unit with a bad slot, flagged by the producer, runs on stale bytes
+    // and writes nothing)
+    const bool s_ok = mbar_wait(&s_full[s], n & 1);
+    const int valid = meta[s];  // read before the stage is handed back
+    float acc_p[2][2][4] = {}, acc_m[2][2][4] = {}, acc_v[2][2][4] = {};
+    {
+      const int col = c0 + 2 * g;  // and col + 1: columns g of n-tiles 0 and 1
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t a[2][4];
@@ -428,62 +454,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                   a[m2][3]);
         }
         const int k0 = 16 * kk + 2 * t;
+        const float2 r0 = ld_shared_v2f(sS + s_off(k0, col));
+        const float2 r1 = ld_shared_v2f(sS + s_off(k0 + 1, col));
+        const float2 r8 = ld_shared_v2f(sS + s_off(k0 + 8, col));
+        const float2 r9 = ld_shared_v2f(sS + s_off(k0 + 9, col));
+        const uint32_t b00 = pack_bf16(r0.x, r1.x), b01 = pack_bf16(r8.x, r9.x);
+        const uint32_t b10 = pack_bf16(r0.y, r1.y), b11 = pack_bf16(r8.y, r9.y);
+        float (&acc)[2][2][4] = kk < 4 ? acc_p : acc_m;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int col = 16 * warp + 8 * nt + g;
-          const uint32_t b0 = pack_bf16(ld_shared_f32(sS + s_off(k0, col)),
-                                        ld_shared_f32(sS + s_off(k0 + 1, col)));
-          const uint32_t b1 = pack_bf16(ld_shared_f32(sS + s_off(k0 + 8, col)),
-                                        ld_shared_f32(sS + s_off(k0 + 9, col)));
-          mma_bf16(acc_n[0][nt], a[0], b0, b1);
-          mma_bf16(acc_n[1][nt], a[1], b0, b1);
+        for (int m2 = 0; m2 < 2; ++m2) {
+          mma_bf16(acc[m2][0], a[m2], b00, b01);
+          mma_bf16(acc[m2][1], a[m2], b10, b11);
         }
       }
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        uint32_t a[2][4];
+        const int key = 16 * kk + 2 * t;
+        const uint32_t w0 = ld_shared_u32(sV + v_off(key, col));
+        const uint32_t w1 = ld_shared_u32(sV + v_off(key + 1, col));
+        const uint32_t w8 = ld_shared_u32(sV + v_off(key + 8, col));
+        const uint32_t w9 = ld_shared_u32(sV + v_off(key + 9, col));
+        const uint32_t b00 = __byte_perm(w0, w1, 0x5410), b01 = __byte_perm(w8, w9, 0x5410);
+        const uint32_t b10 = __byte_perm(w0, w1, 0x7632), b11 = __byte_perm(w8, w9, 0x7632);
 #pragma unroll
         for (int m2 = 0; m2 < 2; ++m2) {
+          uint32_t a[4];
           const int arow = 16 * m2 + (lane & 7) + 8 * ((lane >> 3) & 1);
           const int ch = 2 * kk + (lane >> 4);
-          ldsm_x4(sP + arow * kPitchP + ch * 16, a[m2][0], a[m2][1], a[m2][2], a[m2][3]);
-        }
-        uint32_t vb[4];
-        const int mtx = lane >> 3;
-        const int vrow = 16 * kk + (mtx & 1) * 8 + (lane & 7);
-        const int dch = 2 * warp + (mtx >> 1);
-        ldsm_x4_t(sV + (dch >> 3) * 4096 + sw128(vrow, dch & 7), vb[0], vb[1], vb[2], vb[3]);
-#pragma unroll
-        for (int m2 = 0; m2 < 2; ++m2) {
-          mma_bf16(acc_v[m2][0], a[m2], vb[0], vb[1]);
-          mma_bf16(acc_v[m2][1], a[m2], vb[2], vb[3]);
+          ldsm_x4(sP + arow * kPitchP + ch * 16, a[0], a[1], a[2], a[3]);
+          mma_bf16(acc_v[m2][0], a, b00, b01);
+          mma_bf16(acc_v[m2][1], a, b10, b11);
         }
       }
+    }
+    // the stage is no longer read: hand it back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    // every row's coefficients are in fin after this barrier
+    if (named_bar_any(1, kConsumers, !s_ok)) {
+      if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+      aborted = true;
+      break;
+    }
+    if (!valid) continue;
 
-      // the stage (S, V) is no longer read: hand it back to the producer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-
-      // ---- merge and store o
+    // ---- merge and store o: thread holds columns c0 + 4t .. c0 + 4t + 3
 #pragma unroll
-      for (int m2 = 0; m2 < 2; ++m2) {
+    for (int m2 = 0; m2 < 2; ++m2) {
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int R = 16 * m2 + g + 8 * hr;
-          const float cU = fin[R], cN = fin[32 + R];
-          __nv_bfloat16* orow = o + ((size_t)(b * kL + R) * H + h) * kD;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int R = 16 * m2 + g + 8 * hr;
+        const float cU = fin[R], cP = fin[32 + R], cM = fin[64 + R];
+        float ov[4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int c = 16 * warp + 8 * nt + 2 * t;
-            const float o0 = fmaf(cU, acc_v[m2][nt][2 * hr], cN * acc_n[m2][nt][2 * hr]);
-            const float o1 = fmaf(cU, acc_v[m2][nt][2 * hr + 1], cN * acc_n[m2][nt][2 * hr + 1]);
-            *reinterpret_cast<__nv_bfloat162*>(orow + c) = __floats2bfloat162_rn(o0, o1);
-          }
+        for (int q = 0; q < 4; ++q) {
+          const int j = q & 1, e = 2 * hr + (q >> 1);
+          ov[q] = fmaf(cU, acc_v[m2][j][e], fmaf(cP, acc_p[m2][j][e], cM * acc_m[m2][j][e]));
         }
+        uint2 pk;
+        pk.x = pack_bf16(ov[0], ov[1]);
+        pk.y = pack_bf16(ov[2], ov[3]);
+        *reinterpret_cast<uint2*>(o + ((size_t)(b * kL + R) * H + h) * kD + c0 + 4 * t) = pk;
       }
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  if (aborted && threadIdx.x == 0) {
+    // let the copies of this unit and the next, if issued, land before the
+    // CTA exits (each wait is bounded too)
+    for (int j = i; j <= i + 1 && blockIdx.x + j * gridDim.x < units; ++j) {
+      mbar_wait(&head_full[j & 1], (j >> 1) & 1);
+      mbar_wait(&s_full[j & 1], (j >> 1) & 1);
     }
   }
 }

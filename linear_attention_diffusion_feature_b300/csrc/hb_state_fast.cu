@@ -176,12 +176,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.v);
       mbar_arrive_expect_tx(&bar[kWFull], 16384);
       tma_load_2d(smem + kOffW, &maps.W, 0, h * kD, &bar[kWFull]);
+      // chunks c + 2 and c + 3 are prefetched into L2 while chunk c is
+      // loaded, so DRAM keeps streaming while the two-stage ring is full
+      auto l2_chunk = [&](int c) {
+        if (c >= n_my) return;
+        const int row = (int)(row0 + (c_begin + c) * RB);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          prefetch_l2_3d(&maps.k, 64 * j, h, row);
+          prefetch_l2_3d(&maps.v, 64 * j, h, row);
+        }
+      };
+      l2_chunk(1);
+      l2_chunk(2);
       for (int c = 0; c < n_my; ++c) {
         const int s = c & 1, use = c >> 1;
         if (use > 0 && !mbar_wait(&bar[kKvEmpty0 + s], (use - 1) & 1)) {
           atomicOr(a.status, kStatusTimeout);
           break;
         }
+        l2_chunk(c + 3);
         const int row = (int)(row0 + (c_begin + c) * RB);
         mbar_arrive_expect_tx(&bar[kKvFull0 + s], 4 * RB * 128);
 #pragma unroll
