@@ -10,19 +10,26 @@
 //
 // One CTA per (request, head, token split); it streams its tokens in chunks
 // of RB rows (128 for prompts, 32 for a committed block):
-//   warp 0   TMA producer: k and v chunks into a two-stage ring (two
-//            SWIZZLE_128B boxes of 64 columns each), W_h once;
+//   warp 0   TMA producer of k (two-stage ring of two SWIZZLE_128B boxes of
+//            64 columns), W_h once; a k stage is refilled as soon as
+//            U = K W_h of the chunk it held is done;
+//   warp 2   TMA producer of v (same ring shape), refilled once phi^T V of
+//            its chunk is done;
 //   warp 1   owns TMEM (512 columns) and issues tcgen05.mma from one thread:
 //              U    [128 tok x 64]  = K W_h            (A K-major, B MN-major)
 //              Sacc [128 F x 128 d] += phi^T V          (A, B MN-major)
-//              Zacc [128 F x 16]    += phi^T 1          (B = constant ones)
 //            U is double-buffered, so the next chunk's K W_h overlaps the
-//            epilogue of the current one;
-//   warps 2-5 epilogue: each thread owns one token (one TMEM lane), loads its
-//            64 values of u, takes both softmaxes in registers and writes
-//            phi to shared memory as a bf16 pair hi + lo (phi = hi + lo to
-//            ~2^-17 relative), so the fp32 state meets a 1e-4 bound although
-//            the tensor cores take bf16 operands; v is exact in bf16.
+//            epilogue of the current one, and phi^T V runs per half-chunk
+//            (tokens 0-63, then 64-127) as soon as that half of phi is
+//            written;
+//   warps 3-18 epilogue: four threads share a token (one TMEM lane, 16 of
+//            the 64 columns of u each), exchange row max, min and sums
+//            through shared memory, take both softmaxes and write phi to
+//            shared memory as a bf16 pair hi + lo (phi = hi + lo to ~2^-17
+//            relative), so the fp32 state meets a 1e-4 bound although the
+//            tensor cores take bf16 operands; v is exact in bf16. Z is summed
+//            from the same fp32 phi values in registers and reduced across
+//            threads once at the end.
 // At the end the epilogue reads Sacc/Zacc (thread = row of S), stages the
 // tile through swizzled shared memory and writes S/Z (or a partial sum for
 // the fixed-order split reduction) with coalesced 16-byte stores.
@@ -37,7 +44,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kD = 128, kFH = 64, kF = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 96 + 512;  // k producer, MMA, v producer, 16 epilogue warps
 constexpr int kTargetCtas = 148;  // SMs of a B300; splits aim to fill them once
 
 // Shared-memory layout (bytes from a 1024-aligned base).
@@ -46,19 +53,21 @@ constexpr int kOffV = 65536;        // same
 constexpr int kOffW = 131072;       // [128 d rows][64 bf16]
 constexpr int kOffPhiHi = 147456;   // 2 atoms (F 0-63, 64-127) x [128 tok][128 B]
 constexpr int kOffPhiLo = 180224;
-constexpr int kOffOnes = 212992;    // [16 rows][128 B] of bf16 1.0
+constexpr int kOffZq = 212992;      // [4 token quarters][128 F] fp32: Z partial sums
 constexpr int kOffBar = 215040;
 constexpr int kOffZOld = kOffBar + 256;  // [128] fp32: Z before this call (accumulating)
-constexpr int kSmemBytes = kOffZOld + 512 + 1024;
+constexpr int kOffX = kOffZOld + 512;    // epilogue exchange: 4 x [4 sub][128 tok] fp32
+constexpr int kSmemBytes = kOffX + 8192 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
 // mbarrier slots
-enum { kKvFull0 = 0, kKvFull1, kKvEmpty0, kKvEmpty1, kWFull, kUFull0, kUFull1, kUEmpty0,
-       kUEmpty1, kPhiFull, kPhiEmpty, kAccFull, kOldFull, kNumBars };
+enum { kKFull0 = 0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+       kWFull, kUFull0, kUFull1, kUEmpty0,
+       kUEmpty1, kPhiFullA, kPhiFullB, kPhiEmptyA, kPhiEmptyB, kAccFull, kOldFull, kNumBars };
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColZ = 128, kColU = 256;
+constexpr uint32_t kColS = 0, kColU = 256;
 
 constexpr int kPartialFloats = kF * kD + kF;  // one partial state: S then Z
 
@@ -115,27 +124,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_my = (int)(c_end - c_begin);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar[kKvFull0], 1);
-    mbar_init(&bar[kKvFull1], 1);
-    mbar_init(&bar[kKvEmpty0], 1);
-    mbar_init(&bar[kKvEmpty1], 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&bar[kKFull0 + j], 1);
+      mbar_init(&bar[kKEmpty0 + j], 1);
+      mbar_init(&bar[kVFull0 + j], 1);
+      mbar_init(&bar[kVEmpty0 + j], 1);
+    }
     mbar_init(&bar[kWFull], 1);
     mbar_init(&bar[kUFull0], 1);
     mbar_init(&bar[kUFull1], 1);
-    mbar_init(&bar[kUEmpty0], 4);
-    mbar_init(&bar[kUEmpty1], 4);
-    mbar_init(&bar[kPhiFull], 4);
-    mbar_init(&bar[kPhiEmpty], 1);
+    mbar_init(&bar[kUEmpty0], 16);
+    mbar_init(&bar[kUEmpty1], 16);
+    mbar_init(&bar[kPhiFullA], 8);
+    mbar_init(&bar[kPhiFullB], 8);
+    mbar_init(&bar[kPhiEmptyA], 1);
+    mbar_init(&bar[kPhiEmptyB], 1);
     mbar_init(&bar[kAccFull], 1);
     mbar_init(&bar[kOldFull], 1);
     fence_mbar_init();
-  }
-  if (warp >= 2) {  // constant ones tile (B operand of the Z contraction)
-    const uint32_t ones = smem_u32(smem + kOffOnes);
-    const uint32_t one2 = 0x3F803F80u;  // two bf16 1.0
-    for (int i = threadIdx.x - 64; i < 2048 / 16; i += 128)
-      st_shared_v4(ones + i * 16, one2, one2, one2, one2);
-    fence_proxy_async_smem();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -176,35 +182,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.v);
       mbar_arrive_expect_tx(&bar[kWFull], 16384);
       tma_load_2d(smem + kOffW, &maps.W, 0, h * kD, &bar[kWFull]);
-      // chunks c + 2 and c + 3 are prefetched into L2 while chunk c is
-      // loaded, so DRAM keeps streaming while the two-stage ring is full
-      auto l2_chunk = [&](int c) {
-        if (c >= n_my) return;
-        const int row = (int)(row0 + (c_begin + c) * RB);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          prefetch_l2_3d(&maps.k, 64 * j, h, row);
-          prefetch_l2_3d(&maps.v, 64 * j, h, row);
-        }
-      };
-      l2_chunk(1);
-      l2_chunk(2);
+      // k of chunk c is loaded as soon as U = K W_h of chunk c - 2 is done
+      // (it is not needed after that); chunk c + 3 is prefetched into L2
       for (int c = 0; c < n_my; ++c) {
         const int s = c & 1, use = c >> 1;
-        if (use > 0 && !mbar_wait(&bar[kKvEmpty0 + s], (use - 1) & 1)) {
+        if (use > 0 && !mbar_wait(&bar[kKEmpty0 + s], (use - 1) & 1)) {
           atomicOr(a.status, kStatusTimeout);
           break;
         }
-        l2_chunk(c + 3);
         const int row = (int)(row0 + (c_begin + c) * RB);
-        mbar_arrive_expect_tx(&bar[kKvFull0 + s], 4 * RB * 128);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          tma_load_3d(smem + kOffK + s * 32768 + j * 16384, &maps.k, 64 * j, h, row,
-                      &bar[kKvFull0 + s]);
-          tma_load_3d(smem + kOffV + s * 32768 + j * 16384, &maps.v, 64 * j, h, row,
-                      &bar[kKvFull0 + s]);
+        if (c + 3 < n_my) {
+          const int row3 = (int)(row0 + (c_begin + c + 3) * RB);
+          prefetch_l2_3d(&maps.k, 0, h, row3);
+          prefetch_l2_3d(&maps.k, 64, h, row3);
         }
+        mbar_arrive_expect_tx(&bar[kKFull0 + s], 2 * RB * 128);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(smem + kOffK + s * 32768 + j * 16384, &maps.k, 64 * j, h, row,
+                      &bar[kKFull0 + s]);
+      }
+    }
+  } else if (warp == 2) {
+    // ----------------------------------------------------- v producer
+    // v of chunk c is loaded once phi^T V of chunk c - 2 has completed
+    if (lane == 0 && n_my > 0) {
+      for (int c = 0; c < n_my; ++c) {
+        const int s = c & 1, use = c >> 1;
+        if (use > 0 && !mbar_wait(&bar[kVEmpty0 + s], (use - 1) & 1)) {
+          atomicOr(a.status, kStatusTimeout);
+          break;
+        }
+        const int row = (int)(row0 + (c_begin + c) * RB);
+        if (c + 3 < n_my) {
+          const int row3 = (int)(row0 + (c_begin + c + 3) * RB);
+          prefetch_l2_3d(&maps.v, 0, h, row3);
+          prefetch_l2_3d(&maps.v, 64, h, row3);
+        }
+        mbar_arrive_expect_tx(&bar[kVFull0 + s], 2 * RB * 128);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(smem + kOffV + s * 32768 + j * 16384, &maps.v, 64 * j, h, row,
+                      &bar[kVFull0 + s]);
       }
     }
   } else if (warp == 1) {
@@ -212,36 +231,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_my > 0) {
       constexpr uint32_t idU = umma_idesc_bf16(128, kFH, 0, 1);
       constexpr uint32_t idS = umma_idesc_bf16(128, kD, 1, 1);
-      constexpr uint32_t idZ = umma_idesc_bf16(128, 16, 1, 0);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sW = smem_u32(smem + kOffW);
       const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
-      const uint64_t dOnes = umma_desc_sw128(smem_u32(smem + kOffOnes), 0, 1024);
       bool ok = mbar_wait(&bar[kWFull], 0);
+      // Sacc += phi^T V for chunk cc, tokens 0-63 (half 0, k16 steps 0-3) as
+      // soon as their phi rows are written, then tokens 64-127, so the next
+      // chunk's first half can be written while the second is multiplied.
       auto mma2 = [&](int cc) -> bool {
-        if (!mbar_wait(&bar[kPhiFull], cc & 1)) return false;
-        tc_fence_after();
         const int64_t valid64 = cnt - (c_begin + cc) * RB;
         const int valid = valid64 < RB ? (int)valid64 : RB;
         const int ksteps = (valid + 15) >> 4;
         const uint32_t vb = sV + (cc & 1) * 32768;
-        for (int ks = 0; ks < ksteps; ++ks) {
-          const uint64_t aHi = umma_desc_sw128(sHi + ks * 2048, 16384, 1024);
-          const uint64_t aLo = umma_desc_sw128(sLo + ks * 2048, 16384, 1024);
-          const uint64_t bV = umma_desc_sw128(vb + ks * 2048, 16384, 1024);
-          const uint32_t acc = (cc == 0 && ks == 0) ? 0u : 1u;
-          umma_bf16(tbase + kColS, aHi, bV, idS, acc);
-          umma_bf16(tbase + kColS, aLo, bV, idS, 1u);
-          umma_bf16(tbase + kColZ, aHi, dOnes, idZ, acc);
-          umma_bf16(tbase + kColZ, aLo, dOnes, idZ, 1u);
+        if (!mbar_wait(&bar[kVFull0 + (cc & 1)], (cc >> 1) & 1)) return false;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (!mbar_wait(&bar[kPhiFullA + half], cc & 1)) return false;
+          tc_fence_after();
+          const int ks_end = ksteps < 4 * (half + 1) ? ksteps : 4 * (half + 1);
+          for (int ks = 4 * half; ks < ks_end; ++ks) {
+            const uint64_t aHi = umma_desc_sw128(sHi + ks * 2048, 16384, 1024);
+            const uint64_t aLo = umma_desc_sw128(sLo + ks * 2048, 16384, 1024);
+            const uint64_t bV = umma_desc_sw128(vb + ks * 2048, 16384, 1024);
+            umma_bf16(tbase + kColS, aHi, bV, idS, (cc == 0 && ks == 0) ? 0u : 1u);
+            umma_bf16(tbase + kColS, aLo, bV, idS, 1u);
+          }
+          umma_commit(&bar[kPhiEmptyA + half]);
         }
-        umma_commit(&bar[kPhiEmpty]);
-        umma_commit(&bar[kKvEmpty0 + (cc & 1)]);
+        umma_commit(&bar[kVEmpty0 + (cc & 1)]);
         return true;
       };
       for (int c = 0; ok && c < n_my; ++c) {
         const int s = c & 1;
-        if (!mbar_wait(&bar[kKvFull0 + s], (c >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(&bar[kKFull0 + s], (c >> 1) & 1)) { ok = false; break; }
         if (c >= 2 && !mbar_wait(&bar[kUEmpty0 + s], ((c >> 1) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kb = sK + s * 32768;
@@ -252,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tbase + kColU + 64 * s, aK, bW, idU, ks > 0 ? 1u : 0u);
         }
         umma_commit(&bar[kUFull0 + s]);
+        umma_commit(&bar[kKEmpty0 + s]);
         if (c >= 1 && !mma2(c - 1)) { ok = false; break; }
       }
       if (ok) ok = mma2(n_my - 1);
@@ -260,23 +283,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
+    // 16 warps. Warp w (3..18) reads TMEM lane quarter q = w % 4 (tokens
+    // 32q .. 32q + 31 of a chunk) and column slice sub = (w - 3) / 4 (16 of
+    // the 64 columns of u), so each token's two softmaxes are shared by four
+    // threads that exchange row max, min and sums through shared memory.
     const int quad = warp & 3;
-    const int tok = 32 * quad + lane;  // TMEM lane = token row (chunks) = F row (final)
+    const int ew = warp - 3;               // 0..15
+    const int sub = ew >> 2;
+    const int tok = 32 * quad + lane;      // TMEM lane = token row (chunks) = F row (final)
     const uint32_t lane_bits = (uint32_t)(32 * quad) << 16;
     const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
+    float* xmax = reinterpret_cast<float*>(smem + kOffX);  // [4 sub][128 tok]
+    float* xmin = xmax + 512;
+    float* xsp = xmin + 512;
+    float* xsm = xsp + 512;
+    // Tokens 0-63 (quarters 0, 1) and 64-127 (quarters 2, 3) form two
+    // independent halves with their own named barrier and phi barriers.
+    const int half_id = quad >> 1;
+    const int hbar = 1 + half_id;
+    // Z = sum_t phi(k_t): this thread's 32 columns of phi summed over every
+    // chunk it saw (same token row each time), reduced across threads at the end
+    float zacc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) zacc[j] = 0.f;
+    // A wait that runs out marks `ok` false for good; the threads still go
+    // through every named barrier, and the vote at the first barrier of the
+    // next chunk (or of the final phase) makes all of them leave together.
     bool ok = true;
     for (int c = 0; c < n_my; ++c) {
       const int s = c & 1;
-      if (!mbar_wait(&bar[kUFull0 + s], (c >> 1) & 1)) { ok = false; break; }
+      if (ok) ok = mbar_wait(&bar[kUFull0 + s], (c >> 1) & 1);
       tc_fence_after();
-      float u[64];
-      {
-        float (&u0)[32] = *reinterpret_cast<float(*)[32]>(&u[0]);
-        float (&u1)[32] = *reinterpret_cast<float(*)[32]>(&u[32]);
-        tmem_ld32(tbase + lane_bits + kColU + 64 * s, u0);
-        tmem_ld32(tbase + lane_bits + kColU + 64 * s + 32, u1);
-        tmem_wait_ld();
-      }
+      float u[16];
+      tmem_ld16(tbase + lane_bits + kColU + 64 * s + 16 * sub, u);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kUEmpty0 + s]);
@@ -289,81 +329,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool used = tok < ((valid + 15) & ~15);
       float mx = -FLT_MAX, mn = FLT_MAX;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int j = 0; j < 16; ++j) {
         mx = fmaxf(mx, u[j]);
         mn = fminf(mn, u[j]);
       }
-      // e^{u - max} = 2^{u log2(e) - max log2(e)}: one FMA and one ex2 each
-      float e[64];
-      float sp = 0.f;
-      if (live) {
-        const float off = -mx * kLog2e;
+      xmax[sub * 128 + tok] = mx;
+      xmin[sub * 128 + tok] = mn;
+      if (named_bar_any(hbar, 256, !ok)) break;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          e[j] = ex2_approx(fmaf(u[j], kLog2e, off));
-          sp += e[j];
-        }
+      for (int q = 0; q < 4; ++q) {
+        mx = fmaxf(mx, xmax[q * 128 + tok]);
+        mn = fminf(mn, xmin[q * 128 + tok]);
       }
-      if (c >= 1 && !mbar_wait(&bar[kPhiEmpty], (c - 1) & 1)) { ok = false; break; }
-      // positive half -> atom 0, negated half -> atom 1
+      // e^{u - max} and e^{min - u} as one FMA and one ex2 each
+      float ep[16], em[16], sp = 0.f, sm = 0.f;
+      const float op = -mx * kLog2e, om = mn * kLog2e;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (!used) break;
-        if (half == 1 && live) {
-          sp = 0.f;
-          const float off = mn * kLog2e;
+      for (int j = 0; j < 16; ++j) {
+        ep[j] = ex2_approx(fmaf(u[j], kLog2e, op));
+        em[j] = ex2_approx(fmaf(-u[j], kLog2e, om));
+        sp += ep[j];
+        sm += em[j];
+      }
+      xsp[sub * 128 + tok] = sp;
+      xsm[sub * 128 + tok] = sm;
+      named_bar_sync(hbar, 256);
+      sp = (xsp[tok] + xsp[128 + tok]) + (xsp[256 + tok] + xsp[384 + tok]);
+      sm = (xsm[tok] + xsm[128 + tok]) + (xsm[256 + tok] + xsm[384 + tok]);
+      const float ip = live ? 1.f / sp : 0.f, im = live ? 1.f / sm : 0.f;
+      if (ok && c >= 1) ok = mbar_wait(&bar[kPhiEmptyA + half_id], (c - 1) & 1);
+      if (used) {
+        // phi columns 16 sub .. 16 sub + 15 of each half: two 16-byte chunks
+        // per atom row; dead rows (live == false) are written as exact zeros
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            e[j] = ex2_approx(fmaf(-u[j], kLog2e, off));
-            sp += e[j];
-          }
-        }
-        const float inv = live ? 1.f / sp : 0.f;
-        const uint32_t rowoff = half * 16384 + tok * 128;
+        for (int half = 0; half < 2; ++half) {
+          const float* e = half ? em : ep;
+          const float inv = half ? im : ip;
 #pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-          uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-          if (live) {  // dead rows stay exact zeros whatever u held
+          for (int q = 0; q < 2; ++q) {
+            uint32_t hw[4], lw[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-              const float p0 = e[8 * k8 + 2 * p] * inv, p1 = e[8 * k8 + 2 * p + 1] * inv;
+              const float p0 = e[8 * q + 2 * p] * inv, p1 = e[8 * q + 2 * p + 1] * inv;
+              zacc[16 * half + 8 * q + 2 * p] += p0;
+              zacc[16 * half + 8 * q + 2 * p + 1] += p1;
               const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
               const float2 hf = __bfloat1622float2(hi);
               hw[p] = *reinterpret_cast<const uint32_t*>(&hi);
               lw[p] = pack_bf16(p0 - hf.x, p1 - hf.y);
             }
+            const int chunk = 2 * sub + q;
+            const uint32_t off = half * 16384 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+            st_shared_v4(sHi + off, hw[0], hw[1], hw[2], hw[3]);
+            st_shared_v4(sLo + off, lw[0], lw[1], lw[2], lw[3]);
           }
-          const uint32_t off = rowoff + ((k8 ^ (tok & 7)) << 4);
-          st_shared_v4(sHi + off, hw[0], hw[1], hw[2], hw[3]);
-          st_shared_v4(sLo + off, lw[0], lw[1], lw[2], lw[3]);
         }
       }
-      if (valid < RB) {
+      if (used && !live) {
         // Rows past the end of the request inside the last 16-token step:
-        // their phi is 0; clear v there too so foreign or fill rows cannot
-        // inject a non-finite value into the products.
-        const int vend = (valid + 15) & ~15;
-        if (tok >= valid && tok < vend) {
-          if (!mbar_wait(&bar[kKvFull0 + s], (c >> 1) & 1)) { ok = false; break; }
-          const uint32_t vrow = smem_u32(smem + kOffV + s * 32768) + tok * 128;
+        // their phi is 0; clear v there too (chunks 2 sub, 2 sub + 1 of both
+        // boxes) so foreign or fill rows cannot inject a non-finite value.
+        if (ok) ok = mbar_wait(&bar[kVFull0 + s], (c >> 1) & 1);
+        const uint32_t vrow = smem_u32(smem + kOffV + s * 32768) + tok * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            st_shared_v4(vrow + j * 16, 0u, 0u, 0u, 0u);
-            st_shared_v4(vrow + 16384 + j * 16, 0u, 0u, 0u, 0u);
-          }
+        for (int q = 0; q < 2; ++q) {
+          st_shared_v4(vrow + (2 * sub + q) * 16, 0u, 0u, 0u, 0u);
+          st_shared_v4(vrow + 16384 + (2 * sub + q) * 16, 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kPhiFull]);
+      if (lane == 0) mbar_arrive(&bar[kPhiFullA + half_id]);
     }
-    if (!ok) atomicOr(a.status, kStatusTimeout);
 
-    // ---- final: row `tok` of S (F index) and Z_tok, staged for coalescing
-    const bool have = n_my > 0 && ok && mbar_wait(&bar[kAccFull], 0);
-    if (n_my > 0 && ok && !have) atomicOr(a.status, kStatusTimeout);
+    // ---- final: rows 32 quad + lane of S (an F index), columns 32 sub ..
+    // 32 sub + 31, and Z, staged for coalesced stores
+    bool have = ok;
+    if (have && n_my > 0) have = mbar_wait(&bar[kAccFull], 0);
+    have = __all_sync(0xffffffffu, have);  // warp-uniform for the TMEM loads
     tc_fence_after();
-    if (add_old && !commit_shape && threadIdx.x == 64) {
+    if (add_old && !commit_shape && threadIdx.x == 96) {
       // every MMA and TMA load has completed (kAccFull), so the k region is free
       mbar_arrive_expect_tx(&bar[kOldFull], 2 * 32768 + 512);
       bulk_load(old_lo, S_old, 32768, &bar[kOldFull]);
@@ -371,12 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_load(smem + kOffZOld, Z_old, 512, &bar[kOldFull]);
     }
     const uint32_t stage = smem_u32(smem + kOffPhiHi);  // 64 KiB, free once the MMAs are done
-    float z = 0.f;
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
+    {
       float r[32];
-      if (have) {
-        tmem_ld32(tbase + lane_bits + kColS + 32 * part, r);
+      if (have && n_my > 0) {
+        tmem_ld32(tbase + lane_bits + kColS + 32 * sub, r);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -384,41 +427,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
-        const int chunk = 8 * part + q4;
+        const int chunk = 8 * sub + q4;
         st_shared_v4(stage + tok * 512 + ((chunk ^ (tok & 31)) << 4), __float_as_uint(r[4 * q4]),
                      __float_as_uint(r[4 * q4 + 1]), __float_as_uint(r[4 * q4 + 2]),
                      __float_as_uint(r[4 * q4 + 3]));
       }
     }
-    if (have) {
-      z = tmem_ld1(tbase + lane_bits + kColZ);
-      tmem_wait_ld();
+    // Z: reduce-scatter the 32 column sums across the warp's lanes (lane j
+    // ends with column j of its slice), then add the four token quarters.
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < o; ++j) {
+        const float send = upper ? zacc[j] : zacc[j + o];
+        const float keep = upper ? zacc[j + o] : zacc[j];
+        zacc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
     }
+    float* zq = reinterpret_cast<float*>(smem + kOffZq);  // [4 quarters][128 F]
+    {
+      const int F = lane < 16 ? 16 * sub + lane : kFH + 16 * sub + (lane - 16);
+      zq[quad * 128 + F] = zacc[0];
+    }
+    named_bar_sync(3, 512);
+    float z = 0.f;
+    if (sub == 0) z = (zq[tok] + zq[128 + tok]) + (zq[256 + tok] + zq[384 + tok]);
     tc_fence_before();
-    bool have_old = false;
-    if (add_old) {
-      have_old = mbar_wait(&bar[kOldFull], 0);
-      if (!have_old) atomicOr(a.status, kStatusTimeout);
-    }
-    named_bar_sync(1, 128);
-
-    float* Sdst;
-    float* Zdst;
-    if (a.splits > 1) {
-      float* p = a.ws + ((size_t)(b * a.H + h) * a.splits + split) * kPartialFloats;
-      Sdst = p;
-      Zdst = p + kF * kD;
+    bool have_old = true;
+    if (add_old && have) have_old = mbar_wait(&bar[kOldFull], 0);
+    const bool failed = named_bar_any(3, 512, !(have && have_old));
+    if (failed) {
+      if (threadIdx.x == 96) atomicOr(a.status, kStatusTimeout);
     } else {
-      Sdst = a.S_pool + unit_off * kF * kD;
-      Zdst = a.Z_pool + unit_off * kF;
-    }
-    if (add_old && !have_old) {
-      // the old tile never arrived: leave S/Z as they were (flagged above)
-    } else {
-      const int ew = warp - 2;
+      float* Sdst;
+      float* Zdst;
+      if (a.splits > 1) {
+        float* p = a.ws + ((size_t)(b * a.H + h) * a.splits + split) * kPartialFloats;
+        Sdst = p;
+        Zdst = p + kF * kD;
+      } else {
+        Sdst = a.S_pool + unit_off * kF * kD;
+        Zdst = a.Z_pool + unit_off * kF;
+      }
       const uint32_t olo = smem_u32(old_lo), ohi = smem_u32(old_hi);
 #pragma unroll 4
-      for (int r = ew; r < kF; r += 4) {
+      for (int r = ew; r < kF; r += 16) {
         float4 v = ld_shared_v4f(stage + r * 512 + ((lane ^ (r & 31)) << 4));
         if (add_old) {
           const float4 o = ld_shared_v4f((r < 64 ? olo + r * 512 : ohi + (r - 64) * 512) + lane * 16);
@@ -429,8 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         reinterpret_cast<float4*>(Sdst + r * kD)[lane] = v;
       }
-      const float* zold = reinterpret_cast<const float*>(smem + kOffZOld);
-      Zdst[tok] = add_old ? zold[tok] + z : z;
+      if (sub == 0) {
+        const float* zold = reinterpret_cast<const float*>(smem + kOffZOld);
+        Zdst[tok] = add_old ? zold[tok] + z : z;
+      }
     }
   }
 
