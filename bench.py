@@ -491,6 +491,43 @@ def run_decode(args):
     }
 
 
+def run_feature_map(args):
+    """Standalone feature map of one prompt-sized batch of keys: 65,536 tokens
+    x 16 heads, d=128, f=64 -> phi fp32 (x 268 MB in, phi 537 MB out)."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    n = 65536
+    cfg = hb.Config(H, D, FH, L)
+    x = inputs.draw(11, (n, H, D), torch.bfloat16, device="cuda")
+    W = inputs.draw(12, (H, D, FH), torch.bfloat16, device="cuda", std=D ** -0.5)
+    phi = torch.empty((n, H, F), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    with ClockSampler(0) as clocks:
+        ms = _timed(lambda: hb.hb_feature_map(cfg, x, W, phi), args.steps, args.warmup, stream)
+    assert hb.hb_get_device_status() == 0
+    med = _median(ms)
+    nbytes = n * H * D * 2 + n * H * F * 4 + H * D * FH * 2
+    peak, kind = _peaks()
+    achieved = nbytes / (med / 1e3) / 1e9
+    return {
+        "metric": "feature-map tokens/s and HBM GB/s", "value": n / (med / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": med, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "hb_feature_map: 65,536 tokens x 16 heads, d=128, f=64, "
+                               "bf16 in, fp32 phi out", "l2": "805 MB per call > L2"},
+        "roofline": {"kernel": "hb_feature_map", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": med,
+                     "traffic": _traffic("hb_feature_map")},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def run_stack(args):
     """6 linearized layers, P=2,048-token prefixes, B in {1, 16, 64, 256}:
     one stack step = hb_block_attend of all 6 layers, timed against
@@ -685,11 +722,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack"],
+    ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map"],
                     default="step",
                     help="step: continuous-batching step (default); decode: single-layer "
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
-                         "softmax over a KV cache")
+                         "softmax over a KV cache; feature_map: standalone phi")
     ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -703,7 +740,8 @@ def main(argv=None):
     if args.workload != "step":
         if world > 1:
             ap.error("--workload other than step runs on one GPU")
-        runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack}
+        runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack,
+                  "feature_map": run_feature_map}
         print(json.dumps(runner[args.workload](args)), flush=True)
         return 0
     if world > 1:

@@ -105,8 +105,11 @@ hb_status hb_feature_map(const hb_config* cfg, int64_t n_tokens, const void* x, 
   if ((r = hb::check_ptrs({x, phi})) != HB_OK) return r;
   if (n_tokens > (int64_t)16 * 0x7fffffff) return HB_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_feature_map_ok(s))
-    return hb::from_cuda(hb::launch_feature_map_fast(s, n_tokens, x, W, phi, st));
+  if (hb::fast_feature_map_ok(s)) {
+    unsigned* status = nullptr;
+    if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+    return hb::from_cuda(hb::launch_feature_map_fast(s, n_tokens, x, W, phi, status, st));
+  }
   return hb::from_cuda(hb::launch_feature_map_generic(s, n_tokens, x, W, phi, st));
 }
 

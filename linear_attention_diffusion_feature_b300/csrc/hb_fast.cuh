@@ -17,7 +17,7 @@ bool fast_state_ok(const Shape& s);
 bool fast_softmax_kv_ok(const Shape& s);
 
 cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, const void* W,
-                                    float* phi, cudaStream_t st);
+                                    float* phi, unsigned* status, cudaStream_t st);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
