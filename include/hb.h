@@ -140,6 +140,29 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch,
                           hb_stream_t stream);
 
 /*
+ * hb_block_attend_commit — hb_block_attend followed, for the requests whose
+ * block is finished, by hb_commit_block of that same block, in one pass over
+ * the state (gist.science technical summary, state-compression bullet: the
+ * state is updated only when a block is committed). Request b's output is
+ * computed against its state as it was before the call; then, if
+ * commit[b] != 0, S and Z of slot_idx[b] receive sum_t phi(k_t) v_t^T and
+ * sum_t phi(k_t) over this block's k, v. The state tile is read from HBM once
+ * and written back once, instead of being read again by a separate commit.
+ *   commit   [batch] int32, device: nonzero = this request commits its block
+ *   S_pool, Z_pool  read for every request, written for committing ones
+ *   other arguments as in hb_block_attend.
+ * A committing request's slot must not be read by any other request of the
+ * same call (distinct slots, as in hb_commit_block).
+ */
+hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
+                                 const int32_t* slot_idx, const void* q,
+                                 const void* k, const void* v, float* S_pool,
+                                 float* Z_pool, int32_t num_slots,
+                                 const void* W, const float* gate_logits,
+                                 const int32_t* commit, void* o,
+                                 hb_stream_t stream);
+
+/*
  * hb_commit_block — fold a finished block into the state (gist.science
  * technical summary, state-compression bullet: the states change only when a
  * block is committed; pith.science review, "What carries the argument":

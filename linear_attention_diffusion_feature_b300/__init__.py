@@ -14,6 +14,7 @@ from .hb import (  # noqa: F401
     Config,
     HBError,
     hb_block_attend,
+    hb_block_attend_commit,
     hb_commit_block,
     hb_feature_map,
     hb_get_device_status,

@@ -129,11 +129,42 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch, const int32_t* sl
   cudaError_t e = hb::status_word_ptr(&status);
   if (e != cudaSuccess) return HB_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_attend_ok(s))
+  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots))
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
-                                                num_slots, W, gate_logits, o, status, st));
+                                                num_slots, W, gate_logits, nullptr, o, status,
+                                                st));
   return hb::from_cuda(hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                  num_slots, W, gate_logits, o, status, st));
+}
+
+hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                                 const void* q, const void* k, const void* v, float* S_pool,
+                                 float* Z_pool, int32_t num_slots, const void* W,
+                                 const float* gate_logits, const int32_t* commit, void* o,
+                                 hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits, commit, o})) !=
+      HB_OK)
+    return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots))
+    return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
+                                                num_slots, W, gate_logits, commit, o, status,
+                                                st));
+  // other shapes: the attend pass reads every state, then the committing
+  // requests fold their block in, in stream order
+  cudaError_t e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots,
+                                            W, gate_logits, o, status, st);
+  if (e != cudaSuccess) return HB_ERR_CUDA;
+  return hb::from_cuda(hb::launch_commit_masked_generic(s, batch, slot_idx, commit, k, v, W,
+                                                        S_pool, Z_pool, num_slots, status, st));
 }
 
 hb_status hb_commit_block(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,

@@ -60,19 +60,25 @@ constexpr int kSBytes = 65536;
 constexpr int kOffPhi = kOffQ;              // 2 x [32][64 bf16], SW128: e^{u - max}, e^{min - u}
 constexpr int kOffP = kOffK;                // [32][40 bf16]: 2^{s - m}, 80-byte rows
 constexpr int kPitchP = 80;
-constexpr int kOffSums = kOffK + 32 * kPitchP;  // 5 x [32 rows][4 parts] fp32
-static_assert(kOffSums + 5 * 32 * 4 * 4 <= kOffV, "scratch overflows the k tile");
+constexpr int kOffSums = kOffK + 32 * kPitchP;  // 7 x [32 rows][4 parts] fp32
+static_assert(kOffSums + 7 * 32 * 4 * 4 <= kOffV, "scratch overflows the k tile");
+// Committing units only, once phase A is done with W_h: phi(k) as bf16 hi
+// and lo, each 2 x [32 tokens][64 bf16] SWIZZLE_128B.
+constexpr int kOffPhiKHi = kOffW;
+constexpr int kOffPhiKLo = kOffW + 8192;
 // Shared area after the two stages.
 constexpr int kOffZ = 2 * kStageStride;     // 2 x [128] fp32 (per stage)
-constexpr int kOffPart = kOffZ + 1024;      // max, min of u; max of s: 3 x [32 rows][4 parts]
-constexpr int kOffFin = kOffPart + 3 * 512; // merge coefficients: 3 x [32]
+constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, min of u(k): 5 x [32][4]
+constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
+constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients: 3 x [32]
 constexpr int kOffBar = kOffFin + 3 * 128;
-constexpr int kOffMeta = kOffBar + 6 * 8;
+constexpr int kOffMeta = kOffBar + 6 * 8;   // per stage: flags, slot
 constexpr int kSmemUsed = kOffMeta + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
-enum { kSumP = 0, kSumM, kDenP, kDenM, kSumS };
+enum { kSumP = 0, kSumM, kDenP, kDenM, kSumS, kSumPK, kSumMK };
+enum : int { kUnitValid = 1, kUnitCommit = 2 };  // meta flags of a stage
 
 struct Maps {
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
@@ -97,11 +103,15 @@ __device__ __forceinline__ uint32_t v_off(int key, int n) {
                     (n & 7) * 2);
 }
 
+// kCommit = false: attend only (commit_mask is ignored; S_pool and Z_pool are
+// not written). kCommit = true: requests with commit_mask[b] != 0 also fold
+// their block into the state after their output has been formed.
+template <bool kCommit>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
                   int merge, const int32_t* __restrict__ slot_idx,
-                  const float* __restrict__ S_pool, const float* __restrict__ Z_pool,
-                  const float* __restrict__ gate,
+                  const int32_t* __restrict__ commit_mask, const float* __restrict__ S_pool,
+                  float* __restrict__ Z_pool, const float* __restrict__ gate,
                   __nv_bfloat16* __restrict__ o, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -113,6 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* pmax = reinterpret_cast<float*>(smem + kOffPart);  // [32][4]
   float* pmin = pmax + 128;                                 // [32][4]
   float* smax = pmin + 128;                                 // [32][4]
+  float* pmaxk = smax + 128;                                // [32][4]
+  float* pmink = pmaxk + 128;                               // [32][4]
+  float* zpart = reinterpret_cast<float*>(smem + kOffZPart);  // [2][128]
   float* fin = reinterpret_cast<float*>(smem + kOffFin);    // cU, cP, cM: [3][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,14 +157,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int first = blockIdx.x, stride = gridDim.x;
     const int n_local = first < units ? (units - first + stride - 1) / stride : 0;
-    int win = -1, win_slot = -1;
+    int win = -1, win_slot = -1, win_commit = 0;
     auto slot_of = [&](int i) -> int {  // warp-uniform i, called in increasing order
       if ((i >> 5) != win) {
         win = i >> 5;
         const int uu = first + (32 * win + lane) * stride;
         win_slot = uu < units ? slot_idx[uu / H] : -1;
+        win_commit = (kCommit && uu < units) ? commit_mask[uu / H] : 0;
       }
       return __shfl_sync(0xffffffffu, win_slot, i & 31);
+    };
+    auto commit_of = [&](int i) -> int {  // after slot_of(i), same window
+      return __shfl_sync(0xffffffffu, win_commit, i & 31);
     };
     auto l2_prefetch = [&](int i, int slot) {
       const int uu = first + i * stride;
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_l2_3d(&maps.v, 64 * j, h, b * kL);
       }
     };
-    int slot_next = -1;
+    int slot_next = -1, commit_next = 0;
     for (int i = 0; i < n_local; ++i) {
       const int s = i & 1, n = i >> 1;
       bool ok = true;
@@ -190,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
       }
       const int slot = i == 0 ? slot_of(0) : slot_next;
+      const int commit = i == 0 ? commit_of(0) : commit_next;
       if (lane == 0) {
         if (slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
@@ -197,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&head_full[s]);
           mbar_arrive(&s_full[s]);
         } else {
-          meta[s] = 1;
+          meta[s] = kUnitValid | (commit != 0 ? kUnitCommit : 0);
+          meta[2 + s] = slot;
           mbar_expect_tx(&head_full[s], 512);
           bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
                     &head_full[s]);
@@ -209,7 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
         }
       }
-      if (i + 1 < n_local) slot_next = slot_of(i + 1);
+      if (i + 1 < n_local) {
+        slot_next = slot_of(i + 1);
+        commit_next = commit_of(i + 1);
+      }
       if (i == 0 && n_local > 1) l2_prefetch(1, slot_next);
       if (i + 2 < n_local) l2_prefetch(i + 2, slot_of(i + 2));
     }
@@ -244,14 +266,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sW = smem_u32(st + kOffW);
     const uint32_t sPhi = smem_u32(st + kOffPhi);
     const uint32_t sP = smem_u32(st + kOffP);
-    float* sums = reinterpret_cast<float*>(st + kOffSums);  // [5][32][4]
-    const float* sZ = reinterpret_cast<const float*>(smem + kOffZ + s * 512);
+    float* sums = reinterpret_cast<float*>(st + kOffSums);  // [7][32][4]
+    float* sZ = reinterpret_cast<float*>(smem + kOffZ + s * 512);
     const int b = u / H, h = u - b * H;
     const int R0 = 16 * mt + g, R1 = R0 + 8;
+    // stage flags, valid once the head has landed (the producer writes them
+    // before it arrives on head_full)
+    const int flags = meta[s];
+    const bool cm = kCommit && (flags & kUnitCommit) != 0;  // this unit also commits its block
 
     // ---- phase A: u = q W_h (16 rows x 16 cols per warp) and
-    //      s = q k^T (16 rows x 8 keys per warp)
-    float acc_u[2][4] = {}, acc_s[4] = {};
+    //      s = q k^T (16 rows x 8 keys per warp); for a committing unit also
+    //      u_k = k W_h
+    float acc_u[2][4] = {}, acc_s[4] = {}, acc_uk[2][4] = {};
     {
       const int arow = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
@@ -272,6 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_bf16(acc_s, a0, kb[0], kb[1]);
         mma_bf16(acc_s, a1, kb[2], kb[3]);
+        uint32_t ka0[4], ka1[4];  // k rows as the A operand (committing units)
+        if (cm) {
+          const int ch = 2 * kk + (lane >> 4);
+          ldsm_x4(sK + (ch >> 3) * 4096 + sw128(arow, ch & 7), ka0[0], ka0[1], ka0[2], ka0[3]);
+          const int ch1 = ch + 2;
+          ldsm_x4(sK + (ch1 >> 3) * 4096 + sw128(arow, ch1 & 7), ka1[0], ka1[1], ka1[2], ka1[3]);
+        }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int k16 = kk + half;
@@ -282,6 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ldsm_x4_t(sW + sw128(krow, nch), wb[0], wb[1], wb[2], wb[3]);
           mma_bf16(acc_u[0], half ? a1 : a0, wb[0], wb[1]);
           mma_bf16(acc_u[1], half ? a1 : a0, wb[2], wb[3]);
+          if (cm) {
+            mma_bf16(acc_uk[0], half ? ka1 : ka0, wb[0], wb[1]);
+            mma_bf16(acc_uk[1], half ? ka1 : ka0, wb[2], wb[3]);
+          }
         }
       }
     }
@@ -310,6 +348,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         smax[R0 * 4 + nq] = sm0;
         smax[R1 * 4 + nq] = sm1;
       }
+      if (cm) {
+        float kx0 = fmaxf(fmaxf(acc_uk[0][0], acc_uk[0][1]), fmaxf(acc_uk[1][0], acc_uk[1][1]));
+        float kx1 = fmaxf(fmaxf(acc_uk[0][2], acc_uk[0][3]), fmaxf(acc_uk[1][2], acc_uk[1][3]));
+        float kn0 = fminf(fminf(acc_uk[0][0], acc_uk[0][1]), fminf(acc_uk[1][0], acc_uk[1][1]));
+        float kn1 = fminf(fminf(acc_uk[0][2], acc_uk[0][3]), fminf(acc_uk[1][2], acc_uk[1][3]));
+#pragma unroll
+        for (int o2 = 1; o2 < 4; o2 <<= 1) {
+          kx0 = fmaxf(kx0, __shfl_xor_sync(0xffffffffu, kx0, o2));
+          kx1 = fmaxf(kx1, __shfl_xor_sync(0xffffffffu, kx1, o2));
+          kn0 = fminf(kn0, __shfl_xor_sync(0xffffffffu, kn0, o2));
+          kn1 = fminf(kn1, __shfl_xor_sync(0xffffffffu, kn1, o2));
+        }
+        if (t == 0) {
+          pmaxk[R0 * 4 + nq] = kx0;
+          pmaxk[R1 * 4 + nq] = kx1;
+          pmink[R0 * 4 + nq] = kn0;
+          pmink[R1 * 4 + nq] = kn1;
+        }
+      }
     }
     // q and k are no longer read after this barrier
     if (named_bar_any(1, kConsumers, !head_ok)) {
@@ -319,7 +376,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- phase B: unnormalised exponentials of both halves of phi(q), their
-    //      partial sums and partial dot products with Z; P = 2^{s - m}
+    //      partial sums and partial dot products with Z; P = 2^{s - m}; for a
+    //      committing unit also the exponentials of both halves of phi(k)
+    float ekp[2][4], ekm[2][4];
+    if (cm) {
+      float okp[2], okm[2], skp[2] = {0.f, 0.f}, skm[2] = {0.f, 0.f};
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int R = hr ? R1 : R0;
+        const float4 a = *reinterpret_cast<const float4*>(pmaxk + R * 4);
+        const float4 c = *reinterpret_cast<const float4*>(pmink + R * 4);
+        okp[hr] = -fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)) * kLog2e;
+        okm[hr] = fminf(fminf(c.x, c.y), fminf(c.z, c.w)) * kLog2e;
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float x = acc_uk[nt][r];
+          ekp[nt][r] = ex2_approx(fmaf(x, kLog2e, okp[r >> 1]));
+          ekm[nt][r] = ex2_approx(fmaf(-x, kLog2e, okm[r >> 1]));
+          skp[r >> 1] += ekp[nt][r];
+          skm[r >> 1] += ekm[nt][r];
+        }
+#pragma unroll
+      for (int o2 = 1; o2 < 4; o2 <<= 1)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          skp[hr] += __shfl_xor_sync(0xffffffffu, skp[hr], o2);
+          skm[hr] += __shfl_xor_sync(0xffffffffu, skm[hr], o2);
+        }
+      if (t == 0) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int R = hr ? R1 : R0;
+          sums[(kSumPK * 32 + R) * 4 + nq] = skp[hr];
+          sums[(kSumMK * 32 + R) * 4 + nq] = skm[hr];
+        }
+      }
+    }
     {
       float op[2], om[2], Ms[2];
 #pragma unroll
@@ -390,6 +485,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(1, kConsumers);
 
+    // ---- committing unit: phi(k) = e / sum as bf16 hi + lo (phi = hi + lo to
+    //      about 2^-17 relative, so S meets a 1e-4 bound) for the state update,
+    //      and the column sums of phi(k) over this warp's 16 tokens for Z
+    if (cm) {
+      const uint32_t sKHi = smem_u32(st + kOffPhiKHi), sKLo = smem_u32(st + kOffPhiKLo);
+      float ip[2], im[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int R = hr ? R1 : R0;
+        const float4 a = *reinterpret_cast<const float4*>(sums + (kSumPK * 32 + R) * 4);
+        const float4 c = *reinterpret_cast<const float4*>(sums + (kSumMK * 32 + R) * 4);
+        ip[hr] = 1.f / ((a.x + a.y) + (a.z + a.w));
+        im[hr] = 1.f / ((c.x + c.y) + (c.z + c.w));
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * nq + 8 * nt + 2 * t;
+        float colp[2] = {0.f, 0.f}, colm[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int R = hr ? R1 : R0;
+          const float p0 = ekp[nt][2 * hr] * ip[hr], p1 = ekp[nt][2 * hr + 1] * ip[hr];
+          const float m0 = ekm[nt][2 * hr] * im[hr], m1 = ekm[nt][2 * hr + 1] * im[hr];
+          colp[0] += p0;
+          colp[1] += p1;
+          colm[0] += m0;
+          colm[1] += m1;
+          const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
+          const __nv_bfloat162 hm = __floats2bfloat162_rn(m0, m1);
+          const float2 fp = __bfloat1622float2(hp), fm = __bfloat1622float2(hm);
+          const uint32_t off = sw128(R, c >> 3) + (c & 7) * 2;
+          st_shared_u32(sKHi + off, *reinterpret_cast<const uint32_t*>(&hp));
+          st_shared_u32(sKHi + 4096 + off, *reinterpret_cast<const uint32_t*>(&hm));
+          st_shared_u32(sKLo + off, pack_bf16(p0 - fp.x, p1 - fp.y));
+          st_shared_u32(sKLo + 4096 + off, pack_bf16(m0 - fm.x, m1 - fm.y));
+        }
+        // sum over the 8 row groups g of this warp (lanes with the same t)
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          colp[0] += __shfl_xor_sync(0xffffffffu, colp[0], o2);
+          colp[1] += __shfl_xor_sync(0xffffffffu, colp[1], o2);
+          colm[0] += __shfl_xor_sync(0xffffffffu, colm[0], o2);
+          colm[1] += __shfl_xor_sync(0xffffffffu, colm[1], o2);
+        }
+        if (g == 0) {
+          zpart[mt * 128 + c] = colp[0];
+          zpart[mt * 128 + c + 1] = colp[1];
+          zpart[mt * 128 + kFH + c] = colm[0];
+          zpart[mt * 128 + kFH + c + 1] = colm[1];
+        }
+      }
+    }
+
     // ---- per-row merge coefficients (lanes 0-3 of warp w: rows 4w .. 4w+3),
     //      o = cU U + cP num+ + cM num-, with U = sum_j e^{s_ij - m} v_j,
     //      num+- the contractions of the unnormalised halves with S
@@ -401,32 +549,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 e = *reinterpret_cast<const float4*>(sums + (kDenM * 32 + R) * 4);
       const float4 f = *reinterpret_cast<const float4*>(sums + (kSumS * 32 + R) * 4);
       const float4 m4 = *reinterpret_cast<const float4*>(smax + R * 4);
+      // (approximate reciprocals and exponentials: ~1e-7 relative, far
+      // below what a bf16 output can show)
       const float sp = (a.x + a.y) + (a.z + a.w), sm = (c.x + c.y) + (c.z + c.w);
       const float ps = (f.x + f.y) + (f.z + f.w);
-      const float isp = 1.f / sp, ism = 1.f / sm;
+      const float isp = rcp_approx(sp), ism = rcp_approx(sm);
       const float den = ((d.x + d.y) + (d.z + d.w)) * isp + ((e.x + e.y) + (e.z + e.w)) * ism;
-      const float mnat = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)) * kLn2;
+      const float m2 = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));  // row max, base 2
       float cU, cN;
       if (merge == HB_MERGE_SHARED_NORM) {
         // (w e^m U + num) / (w e^m P + den) with log w = log sigmoid(alpha),
         // rescaled by e^{-lam} or e^{lam} (lam = log w + m) so nothing overflows
-        const float lam = log_sigmoid(gl) + mnat;
-        if (lam >= 0.f) {
-          const float r = expf(-lam);
-          cU = 1.f / (ps + r * den);
+        const float lam2 = log_sigmoid(gl) * kLog2e + m2;  // lam in base 2
+        if (lam2 >= 0.f) {
+          const float r = ex2_approx(-lam2);
+          cU = rcp_approx(fmaf(r, den, ps));
           cN = r * cU;
         } else {
-          const float r = expf(lam);
-          cN = 1.f / (r * ps + den);
+          const float r = ex2_approx(lam2);
+          cN = rcp_approx(fmaf(r, ps, den));
           cU = r * cN;
         }
       } else {
         const float w = sigmoid(gl);
         if (den > 0.f) {
-          cU = w / ps;
-          cN = (1.f - w) / den;
+          cU = w * rcp_approx(ps);
+          cN = (1.f - w) * rcp_approx(den);
         } else {  // nothing committed: the linear branch is dropped
-          cU = 1.f / ps;
+          cU = rcp_approx(ps);
           cN = 0.f;
         }
       }
@@ -487,9 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // the stage is no longer read: hand it back to the producer
+    // the stage is no longer read: hand it back to the producer (a
+    // committing unit keeps it until its new S has been stored)
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0 && !cm) mbar_arrive(&empty[s]);
     // every row's coefficients are in fin after this barrier
     if (named_bar_any(1, kConsumers, !s_ok)) {
       if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
@@ -517,6 +668,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint2*>(o + ((size_t)(b * kL + R) * H + h) * kD + c0 + 4 * t) = pk;
       }
     }
+
+    // ---- committing unit (after its output used the old state):
+    //      S += phi(k)^T V with phi(k) = hi + lo, Z += sum_t phi(k_t); the new
+    //      state is written over the old one in the stage and stored by TMA.
+    //      Warp w produces F rows 16w .. 16w + 15, all 128 columns.
+    if (cm) {
+      float acc[16][4];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      const uint32_t sKHi = smem_u32(st + kOffPhiKHi), sKLo = smem_u32(st + kOffPhiKLo);
+      const int mi = lane >> 3;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        // phi(k)^T fragments: rows F, columns tokens (transposed loads of [tok][F])
+        uint32_t ah[4], al[4];
+        {
+          const int tokr = 16 * kk + (mi >> 1) * 8 + (lane & 7);
+          const int ch = 2 * warp + (mi & 1);
+          const uint32_t off = (ch >> 3) * 4096 + sw128(tokr, ch & 7);
+          ldsm_x4_t(sKHi + off, ah[0], ah[1], ah[2], ah[3]);
+          ldsm_x4_t(sKLo + off, al[0], al[1], al[2], al[3]);
+        }
+#pragma unroll
+        for (int jp = 0; jp < 8; ++jp) {
+          uint32_t vb[4];
+          const int krow = 16 * kk + (mi & 1) * 8 + (lane & 7);
+          const int dch = 2 * jp + (mi >> 1);
+          ldsm_x4_t(sV + (dch >> 3) * 4096 + sw128(krow, dch & 7), vb[0], vb[1], vb[2], vb[3]);
+          mma_bf16(acc[2 * jp], ah, vb[0], vb[1]);
+          mma_bf16(acc[2 * jp], al, vb[0], vb[1]);
+          mma_bf16(acc[2 * jp + 1], ah, vb[2], vb[3]);
+          mma_bf16(acc[2 * jp + 1], al, vb[2], vb[3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const uint32_t a = sS + s_off(16 * warp + g + 8 * hr, 8 * j + 2 * t);
+          const float2 old = ld_shared_v2f(a);
+          st_shared_v2f(a, old.x + acc[j][2 * hr], old.y + acc[j][2 * hr + 1]);
+        }
+      if (threadIdx.x < kF) sZ[threadIdx.x] += zpart[threadIdx.x] + zpart[128 + threadIdx.x];
+      fence_proxy_async_smem();
+      named_bar_sync(1, kConsumers);
+      if (threadIdx.x == 0) {
+        const int uslot = meta[2 + s];
+        const int row = (uslot * H + h) * kF;
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) tma_store_2d(&maps.S, 32 * bx, row, st + kOffS + bx * 16384);
+        bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, sZ, kF * 4);
+        bulk_commit();
+        bulk_wait_read();  // the stage may be refilled only after this
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
   }
   if (aborted && threadIdx.x == 0) {
     // let the copies of this unit and the next, if issued, land before the
@@ -534,14 +742,16 @@ int g_num_sms = 0;
 
 bool fast_attend_ok(const Shape& s) { return production_shape(s); }
 
+bool attend_fast_fits(const Shape& s, int batch, int num_slots) {
+  return (int64_t)num_slots * s.H * kF < ((int64_t)1 << 31) &&
+         (int64_t)batch * kL < ((int64_t)1 << 31);
+}
+
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
-                               const float* gate, void* o, unsigned* status, cudaStream_t st) {
-  if ((int64_t)num_slots * s.H * kF >= (int64_t)1 << 31 ||
-      (int64_t)batch * kL >= (int64_t)1 << 31)
-    return launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
-                                 o, status, st);
+                               const float* gate, const int32_t* commit_mask, void* o,
+                               unsigned* status, cudaStream_t st) {
   Maps maps;
   {
     const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
@@ -570,7 +780,8 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_attend_fast), kSmemBytes);
+  auto* kernel = commit_mask ? k_attend_fast<true> : k_attend_fast<false>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   if (g_num_sms == 0) {
     int dev = 0, n = 0;
@@ -581,10 +792,9 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   }
   const int units = batch * s.H;
   const int grid = units < g_num_sms ? units : g_num_sms;
-  k_attend_fast<<<grid, kThreads, kSmemBytes, st>>>(maps, batch, s.H, num_slots,
-                                                    s.scale * kLog2e, s.merge,
-                                                    slot_idx, S_pool, Z_pool, gate,
-                                                    reinterpret_cast<__nv_bfloat16*>(o), status);
+  kernel<<<grid, kThreads, kSmemBytes, st>>>(
+      maps, batch, s.H, num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
+      const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o), status);
   return cudaGetLastError();
 }
 

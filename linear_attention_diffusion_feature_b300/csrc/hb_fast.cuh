@@ -18,10 +18,15 @@ bool fast_softmax_kv_ok(const Shape& s);
 
 cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, const void* W,
                                     float* phi, unsigned* status, cudaStream_t st);
+// commit_mask == nullptr: attend only (S_pool and Z_pool are not written).
+// Otherwise request b with commit_mask[b] != 0 also folds its block's k, v
+// into its state slot after its output has used the old state.
+bool attend_fast_fits(const Shape& s, int batch, int num_slots);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
-                               const float* gate, void* o, unsigned* status, cudaStream_t st);
+                               const float* gate, const int32_t* commit_mask, void* o,
+                               unsigned* status, cudaStream_t st);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);

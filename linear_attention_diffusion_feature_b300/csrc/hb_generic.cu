@@ -78,7 +78,8 @@ constexpr int kMaxE = 64;  // 128 * 128 / 256
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_state_accumulate_generic(
-    int H, int d, int f, int L, const int32_t* __restrict__ slot_idx, const T* __restrict__ k,
+    int H, int d, int f, int L, const int32_t* __restrict__ slot_idx,
+    const int32_t* __restrict__ mask, const T* __restrict__ k,
     const T* __restrict__ v, int64_t total_tokens, const int64_t* __restrict__ cu_seqlens,
     int64_t max_seqlen,
     const T* __restrict__ W, float* __restrict__ S_pool, float* __restrict__ Z_pool,
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) k_state_accumulate_generic(
   constexpr int CH = 16;
   const int F = 2 * f;
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (mask && mask[b] == 0) return;  // request b does not commit
   const int slot = slot_idx[b];
   int64_t row0, cnt;
   if (cu_seqlens) {
@@ -439,7 +441,8 @@ cudaError_t launch_feature_map_generic(const Shape& s, int64_t n, const void* x,
   return cudaGetLastError();
 }
 
-cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int32_t* slot_idx,
+static cudaError_t state_accumulate_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                            const int32_t* mask,
                                             const void* k, const void* v, int64_t total_tokens,
                                             const int64_t* cu_seqlens, int64_t max_seqlen,
                                             const void* W, float* S_pool, float* Z_pool,
@@ -454,19 +457,38 @@ cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int
   if (s.dtype == HB_DTYPE_BF16) {
     auto* fn = k_state_accumulate_generic<__nv_bfloat16>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
-    fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, (const __nv_bfloat16*)k,
+    fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, mask, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, total_tokens, cu_seqlens, maxlen,
                                      (const __nv_bfloat16*)W, S_pool, Z_pool, num_slots,
                                      accumulate, status);
   } else {
     auto* fn = k_state_accumulate_generic<float>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
-    fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, (const float*)k,
+    fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, mask, (const float*)k,
                                      (const float*)v, total_tokens, cu_seqlens, maxlen,
                                      (const float*)W,
                                      S_pool, Z_pool, num_slots, accumulate, status);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                            const void* k, const void* v, int64_t total_tokens,
+                                            const int64_t* cu_seqlens, int64_t max_seqlen,
+                                            const void* W, float* S_pool, float* Z_pool,
+                                            int num_slots, int accumulate, unsigned* status,
+                                            cudaStream_t st) {
+  return state_accumulate_generic(s, batch, slot_idx, nullptr, k, v, total_tokens, cu_seqlens,
+                                  max_seqlen, W, S_pool, Z_pool, num_slots, accumulate, status,
+                                  st);
+}
+
+cudaError_t launch_commit_masked_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                         const int32_t* mask, const void* k, const void* v,
+                                         const void* W, float* S_pool, float* Z_pool,
+                                         int num_slots, unsigned* status, cudaStream_t st) {
+  return state_accumulate_generic(s, batch, slot_idx, mask, k, v, (int64_t)batch * s.L, nullptr,
+                                  s.L, W, S_pool, Z_pool, num_slots, 1, status, st);
 }
 
 cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot_idx,

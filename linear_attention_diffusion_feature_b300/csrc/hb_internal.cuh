@@ -104,6 +104,11 @@ cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int
                                             const void* W, float* S_pool, float* Z_pool,
                                             int num_slots, int accumulate, unsigned* status,
                                             cudaStream_t st);
+// commit of the requests with mask[b] != 0 (rows [b*L, b*L + L) of k, v)
+cudaError_t launch_commit_masked_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                         const int32_t* mask, const void* k, const void* v,
+                                         const void* W, float* S_pool, float* Z_pool,
+                                         int num_slots, unsigned* status, cudaStream_t st);
 cudaError_t launch_state_zero(const Shape& s, int batch, const int32_t* slot_idx, float* S_pool,
                               float* Z_pool, int num_slots, unsigned* status, cudaStream_t st);
 cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_cache,

@@ -133,6 +133,30 @@ def hb_block_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logi
     return o
 
 
+def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits,
+                           commit, o=None, stream=None) -> torch.Tensor:
+    """hb_block_attend, then hb_commit_block of the same block for the requests
+    with commit[b] != 0, in one pass over the state."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(commit, "commit", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_commit(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                                      _ptr(v), _ptr(S_pool), _ptr(Z_pool), num_slots, _ptr(W),
+                                      _ptr(gate_logits), _ptr(commit), _ptr(o), _stream(stream)),
+           "hb_block_attend_commit")
+    return o
+
+
 def hb_commit_block(cfg: Config, slot_idx, k, v, W, S_pool, Z_pool, stream=None) -> None:
     """S += sum_t phi(k_t) v_t^T, Z += sum_t phi(k_t) for each listed slot."""
     B = slot_idx.shape[0]

@@ -1,0 +1,151 @@
+"""hb_block_attend_commit (GPU): the output uses the state as it was before
+the call, and the committing requests' states then hold the oracle's commit
+of the same block; other slots are untouched. Also checked against the two
+separate calls (hb_block_attend, then hb_commit_block on the subset)."""
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_diffusion_feature_b300 as hb
+import oracle.block_hybrid as ob
+from linear_attention_diffusion_feature_b300 import inputs
+from tests.parity import (TOL_OUT_BF16, TOL_OUT_FP32, TOL_STATE, assert_status_ok, f64, new_pool,
+                          out_err, slots, unit_err)
+
+pytestmark = pytest.mark.gpu
+
+MERGES = {"shared_norm": hb.MERGE_SHARED_NORM, "convex": hb.MERGE_CONVEX}
+
+
+def _case(dt, d=128, f=64, L=32, H=16):
+    prefix = [64, 96, 0, 32, 128, 160]
+    commit = [1, 0, 1, 1, 0, 0]
+    slot_of = [3, 0, 5, 1, 4, 2]
+    B = len(prefix)
+    W = inputs.draw(61, (H, d, f), dt, std=d ** -0.5)
+    gate = inputs.draw(62, (H,), torch.float32)
+    q, k, v = (inputs.draw(63 + i, (B, L, H, d), dt) for i in range(3))
+    states = []
+    for b, n in enumerate(prefix):
+        pk = inputs.draw(70 + 2 * b, (n, H, d), dt)
+        pv = inputs.draw(71 + 2 * b, (n, H, d), dt)
+        states.append(ob.prefill(f64(pk), f64(pv), f64(W)))
+    return dict(W=W, gate=gate, q=q, k=k, v=v, states=states, commit=commit, slot_of=slot_of,
+                B=B, H=H, d=d, f=f, L=L)
+
+
+def _pool(c, cfg, dev, num_slots=7):
+    S, Z = new_pool(cfg, num_slots, dev)
+    fill = inputs.draw(80, S.shape, torch.float32)  # slots no request names
+    S.copy_(fill.to(dev))
+    Z.copy_(fill[..., 0].abs().to(dev))
+    for b, sl in enumerate(c["slot_of"]):
+        S[sl] = torch.as_tensor(c["states"][b][0], dtype=torch.float32, device=dev)
+        Z[sl] = torch.as_tensor(c["states"][b][1], dtype=torch.float32, device=dev)
+    return S, Z
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_attend_commit_matches_oracle(cuda_device, merge, dt):
+    c = _case(dt)
+    cfg = hb.Config(c["H"], c["d"], c["f"], c["L"],
+                    dtype=hb.DTYPE_BF16 if dt == torch.bfloat16 else hb.DTYPE_FP32,
+                    merge=MERGES[merge])
+    S, Z = _pool(c, cfg, cuda_device)
+    S0, Z0 = S.clone(), Z.clone()
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    o = hb.hb_block_attend_commit(cfg, slots(c["slot_of"], cuda_device), dev(c["q"]), dev(c["k"]),
+                                  dev(c["v"]), S, Z, dev(c["W"]), dev(c["gate"]),
+                                  slots(c["commit"], cuda_device))
+    assert_status_ok()
+    tol = TOL_OUT_BF16 if dt == torch.bfloat16 else TOL_OUT_FP32
+    W64 = f64(c["W"])
+    for b, sl in enumerate(c["slot_of"]):
+        S_old, Z_old = c["states"][b]
+        ref = ob.attend(f64(c["q"][b]), f64(c["k"][b]), f64(c["v"][b]), S_old, Z_old, W64,
+                        f64(c["gate"]), MERGES[merge])
+        assert out_err(f64(o[b]), ref) <= tol, b
+        if c["commit"][b]:
+            S_new, Z_new = ob.commit(S_old, Z_old, f64(c["k"][b]), f64(c["v"][b]), W64)
+        else:
+            S_new, Z_new = f64(S0[sl]), f64(Z0[sl])
+        assert unit_err(f64(S[sl]), S_new, 1) <= TOL_STATE, b
+        assert unit_err(f64(Z[sl]), Z_new, 1) <= TOL_STATE, b
+    assert torch.equal(S[6], S0[6]) and torch.equal(Z[6], Z0[6])
+
+
+def test_attend_commit_equals_two_calls_at_full_size(cuda_device):
+    """64 requests, 16 committing (the continuous-batching step): the output
+    is the same bits as hb_block_attend's, the states match hb_commit_block's."""
+    w = inputs.continuous_batching(seed=7, device=cuda_device, B=64, n_commit=16)
+    t = w.tensors
+    cfg = hb.Config(16, 128, 64, 32)
+    sl = torch.arange(64, dtype=torch.int32, device=cuda_device)
+    S, Z = new_pool(cfg, 64, cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S, Z)
+    S2, Z2 = S.clone(), Z.clone()
+    mask = torch.zeros(64, dtype=torch.int32, device=cuda_device)
+    mask[t["commit_idx"]] = 1
+    o1 = hb.hb_block_attend_commit(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"], mask)
+    o2 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S2, Z2, t["W"], t["gate"])
+    ci = t["commit_idx"]
+    hb.hb_commit_block(cfg, sl[ci].contiguous(), t["k"][ci].contiguous(), t["v"][ci].contiguous(),
+                       t["W"], S2, Z2)
+    assert_status_ok()
+    assert torch.equal(o1, o2)
+    assert unit_err(f64(S), f64(S2), 2) <= TOL_STATE
+    assert unit_err(f64(Z), f64(Z2), 2) <= TOL_STATE
+    untouched = torch.ones(64, dtype=torch.bool, device=cuda_device)
+    untouched[ci] = False
+    assert torch.equal(S[untouched], S2[untouched])
+
+
+@pytest.mark.parametrize("pattern", ["none", "all"])
+def test_attend_commit_mask_extremes(cuda_device, pattern):
+    c = _case(torch.bfloat16)
+    c["commit"] = [0] * c["B"] if pattern == "none" else [1] * c["B"]
+    cfg = hb.Config(c["H"], c["d"], c["f"], c["L"])
+    S, Z = _pool(c, cfg, cuda_device)
+    S0 = S.clone()
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    hb.hb_block_attend_commit(cfg, slots(c["slot_of"], cuda_device), dev(c["q"]), dev(c["k"]),
+                              dev(c["v"]), S, Z, dev(c["W"]), dev(c["gate"]),
+                              slots(c["commit"], cuda_device))
+    assert_status_ok()
+    W64 = f64(c["W"])
+    for b, sl in enumerate(c["slot_of"]):
+        if pattern == "none":
+            assert torch.equal(S[sl], S0[sl])
+        else:
+            S_new, _ = ob.commit(*c["states"][b], f64(c["k"][b]), f64(c["v"][b]), W64)
+            assert unit_err(f64(S[sl]), S_new, 1) <= TOL_STATE
+
+
+def test_attend_commit_bad_slot_is_skipped_and_flagged(cuda_device):
+    c = _case(torch.bfloat16)
+    cfg = hb.Config(c["H"], c["d"], c["f"], c["L"])
+    S, Z = _pool(c, cfg, cuda_device)
+    S0 = S.clone()
+    bad = list(c["slot_of"])
+    bad[2] = 99  # a committing request with a slot outside the pool
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    o = torch.full_like(dev(c["q"]), 7.0)
+    hb.hb_block_attend_commit(cfg, slots(bad, cuda_device), dev(c["q"]), dev(c["k"]), dev(c["v"]),
+                              S, Z, dev(c["W"]), dev(c["gate"]), slots(c["commit"], cuda_device),
+                              o=o)
+    st = hb.hb_get_device_status()
+    assert st == 5  # HB_ERR_DEVICE_BOUNDS
+    assert bool((o[2] == 7.0).all())  # no output for the skipped request
+    W64 = f64(c["W"])
+    for b, sl in enumerate(c["slot_of"]):
+        if b == 2:
+            continue
+        if c["commit"][b]:
+            S_new, _ = ob.commit(*c["states"][b], f64(c["k"][b]), f64(c["v"][b]), W64)
+            assert unit_err(f64(S[sl]), S_new, 1) <= TOL_STATE
+        else:
+            assert torch.equal(S[sl], S0[sl])
+    assert torch.equal(S[5], S0[5])  # the skipped request's real slot
