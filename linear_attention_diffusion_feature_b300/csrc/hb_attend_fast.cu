@@ -45,7 +45,9 @@ using namespace ptx;
 constexpr int kD = 128, kFH = 64, kF = 128, kL = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarp = kConsumerWarps;    // warp 8
+constexpr int kCoefWarp = kConsumerWarps + 1;    // warp 9: per-row merge coefficients
+constexpr int kThreads = kConsumers + 64;
 
 // Stage layout (bytes from the stage base; the base is 1024-aligned).
 constexpr int kOffS = 0;                    // 4 x [128 F-rows][32 fp32], SW128
@@ -70,9 +72,9 @@ constexpr int kOffPhiKLo = kOffW + 8192;
 constexpr int kOffZ = 2 * kStageStride;     // 2 x [128] fp32 (per stage)
 constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, min of u(k): 5 x [32][4]
 constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
-constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients: 3 x [32]
-constexpr int kOffBar = kOffFin + 3 * 128;
-constexpr int kOffMeta = kOffBar + 6 * 8;   // per stage: flags, slot
+constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x 3 x [32]
+constexpr int kOffBar = kOffFin + 2 * 3 * 128;
+constexpr int kOffMeta = kOffBar + 10 * 8;  // per stage: flags, slot
 constexpr int kSmemUsed = kOffMeta + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* head_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* s_full = head_full + 2;
   uint64_t* empty = head_full + 4;
+  uint64_t* sums_ready = head_full + 6;  // consumers -> coefficient warp
+  uint64_t* fin_ready = head_full + 8;   // coefficient warp -> consumers
   int* meta = reinterpret_cast<int*>(smem + kOffMeta);
   float* pmax = reinterpret_cast<float*>(smem + kOffPart);  // [32][4]
   float* pmin = pmax + 128;                                 // [32][4]
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* pmaxk = smax + 128;                                // [32][4]
   float* pmink = pmaxk + 128;                               // [32][4]
   float* zpart = reinterpret_cast<float*>(smem + kOffZPart);  // [2][128]
-  float* fin = reinterpret_cast<float*>(smem + kOffFin);    // cU, cP, cM: [3][32]
+  float* fin_all = reinterpret_cast<float*>(smem + kOffFin);  // [stage][cU, cP, cM][32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = batch * H;
@@ -135,13 +139,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&head_full[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], kConsumerWarps + 1);  // + the coefficient warp
+      mbar_init(&sums_ready[s], kConsumerWarps);
+      mbar_init(&fin_ready[s], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == kCoefWarp) {
+    // ------------------------------------------------- merge coefficients
+    // Lane R computes row R of the unit's merge, o = cU U + cP num+ + cM num-
+    // (U = sum_j e^{s_ij - m} v_j; num+- the contractions of the unnormalised
+    // halves of phi(q) with S), from the row sums the consumers leave in the
+    // stage, while the consumers run the state contraction.
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const int s = i & 1, n = i >> 1;
+      const float gl = gate[u % H];
+      if (!mbar_wait(&sums_ready[s], n & 1)) {
+        if (lane == 0) atomicOr(status, kStatusTimeout);
+        break;
+      }
+      if (meta[s] & kUnitValid) {
+        const float* sums = reinterpret_cast<const float*>(smem + s * kStageStride + kOffSums);
+        float* fin = fin_all + s * 96;
+        const int R = lane;
+        const float4 a = *reinterpret_cast<const float4*>(sums + (kSumP * 32 + R) * 4);
+        const float4 c = *reinterpret_cast<const float4*>(sums + (kSumM * 32 + R) * 4);
+        const float4 d = *reinterpret_cast<const float4*>(sums + (kDenP * 32 + R) * 4);
+        const float4 e = *reinterpret_cast<const float4*>(sums + (kDenM * 32 + R) * 4);
+        const float4 f = *reinterpret_cast<const float4*>(sums + (kSumS * 32 + R) * 4);
+        const float4 m4 = *reinterpret_cast<const float4*>(smax + R * 4);
+        // (approximate reciprocals and exponentials: ~1e-7 relative, far
+        // below what a bf16 output can show)
+        const float sp = (a.x + a.y) + (a.z + a.w), sm = (c.x + c.y) + (c.z + c.w);
+        const float ps = (f.x + f.y) + (f.z + f.w);
+        const float isp = rcp_approx(sp), ism = rcp_approx(sm);
+        const float den = ((d.x + d.y) + (d.z + d.w)) * isp + ((e.x + e.y) + (e.z + e.w)) * ism;
+        const float m2 = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));  // row max, base 2
+        float cU, cN;
+        if (merge == HB_MERGE_SHARED_NORM) {
+          // (w e^m U + num) / (w e^m P + den) with log w = log sigmoid(alpha),
+          // rescaled by e^{-lam} or e^{lam} (lam = log w + m) so nothing overflows
+          const float lam2 = log_sigmoid(gl) * kLog2e + m2;  // lam in base 2
+          if (lam2 >= 0.f) {
+            const float r = ex2_approx(-lam2);
+            cU = rcp_approx(fmaf(r, den, ps));
+            cN = r * cU;
+          } else {
+            const float r = ex2_approx(lam2);
+            cN = rcp_approx(fmaf(r, ps, den));
+            cU = r * cN;
+          }
+        } else {
+          const float w = sigmoid(gl);
+          if (den > 0.f) {
+            cU = w * rcp_approx(ps);
+            cN = (1.f - w) * rcp_approx(den);
+          } else {  // nothing committed: the linear branch is dropped
+            cU = rcp_approx(ps);
+            cN = 0.f;
+          }
+        }
+        fin[R] = cU;
+        fin[32 + R] = cN * isp;
+        fin[64 + R] = cN * ism;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&fin_ready[s]);
+        mbar_arrive(&empty[s]);  // the row sums in the stage have been read
+      }
+    }
+    return;
+  }
+
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; lane 0 issues the copies. A unit's q, k,
     // v and W_h do not depend on its state slot, so they are issued before
@@ -252,11 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // to the next named barrier, which also votes, and all warps leave
   // together (a warp left behind at a named barrier would never return).
   int i = 0;
-  bool aborted = false;
+  bool aborted = false, late_fail = false;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
     const int s = i & 1, n = i >> 1;
-    // the gate is read before the wait so its latency hides behind it
-    const float gl = gate[u % H];
     const bool head_ok = mbar_wait(&head_full[s], n & 1);
     uint8_t* st = smem + s * kStageStride;
     const uint32_t sS = smem_u32(st + kOffS);
@@ -369,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // q and k are no longer read after this barrier
-    if (named_bar_any(1, kConsumers, !head_ok)) {
+    if (named_bar_any(1, kConsumers, !head_ok || late_fail)) {
       if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
       aborted = true;
       break;
@@ -483,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       st_shared_u32(sP + R0 * kPitchP + key * 2, pack_bf16(p[0], p[1]));
       st_shared_u32(sP + R1 * kPitchP + key * 2, pack_bf16(p[2], p[3]));
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sums_ready[s]);  // row sums are in the stage
     named_bar_sync(1, kConsumers);
 
     // ---- committing unit: phi(k) = e / sum as bf16 hi + lo (phi = hi + lo to
@@ -536,53 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           zpart[mt * 128 + kFH + c + 1] = colm[1];
         }
       }
-    }
-
-    // ---- per-row merge coefficients (lanes 0-3 of warp w: rows 4w .. 4w+3),
-    //      o = cU U + cP num+ + cM num-, with U = sum_j e^{s_ij - m} v_j,
-    //      num+- the contractions of the unnormalised halves with S
-    if (lane < 4) {
-      const int R = 4 * warp + lane;
-      const float4 a = *reinterpret_cast<const float4*>(sums + (kSumP * 32 + R) * 4);
-      const float4 c = *reinterpret_cast<const float4*>(sums + (kSumM * 32 + R) * 4);
-      const float4 d = *reinterpret_cast<const float4*>(sums + (kDenP * 32 + R) * 4);
-      const float4 e = *reinterpret_cast<const float4*>(sums + (kDenM * 32 + R) * 4);
-      const float4 f = *reinterpret_cast<const float4*>(sums + (kSumS * 32 + R) * 4);
-      const float4 m4 = *reinterpret_cast<const float4*>(smax + R * 4);
-      // (approximate reciprocals and exponentials: ~1e-7 relative, far
-      // below what a bf16 output can show)
-      const float sp = (a.x + a.y) + (a.z + a.w), sm = (c.x + c.y) + (c.z + c.w);
-      const float ps = (f.x + f.y) + (f.z + f.w);
-      const float isp = rcp_approx(sp), ism = rcp_approx(sm);
-      const float den = ((d.x + d.y) + (d.z + d.w)) * isp + ((e.x + e.y) + (e.z + e.w)) * ism;
-      const float m2 = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));  // row max, base 2
-      float cU, cN;
-      if (merge == HB_MERGE_SHARED_NORM) {
-        // (w e^m U + num) / (w e^m P + den) with log w = log sigmoid(alpha),
-        // rescaled by e^{-lam} or e^{lam} (lam = log w + m) so nothing overflows
-        const float lam2 = log_sigmoid(gl) * kLog2e + m2;  // lam in base 2
-        if (lam2 >= 0.f) {
-          const float r = ex2_approx(-lam2);
-          cU = rcp_approx(fmaf(r, den, ps));
-          cN = r * cU;
-        } else {
-          const float r = ex2_approx(lam2);
-          cN = rcp_approx(fmaf(r, ps, den));
-          cU = r * cN;
-        }
-      } else {
-        const float w = sigmoid(gl);
-        if (den > 0.f) {
-          cU = w * rcp_approx(ps);
-          cN = (1.f - w) * rcp_approx(den);
-        } else {  // nothing committed: the linear branch is dropped
-          cU = rcp_approx(ps);
-          cN = 0.f;
-        }
-      }
-      fin[R] = cU;
-      fin[32 + R] = cN * isp;
-      fin[64 + R] = cN * ism;
     }
 
     // ---- phase D: num+- = e+- S and U = P V for columns 16w .. 16w + 15
@@ -641,13 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // committing unit keeps it until its new S has been stored)
     __syncwarp();
     if (lane == 0 && !cm) mbar_arrive(&empty[s]);
-    // every row's coefficients are in fin after this barrier
-    if (named_bar_any(1, kConsumers, !s_ok)) {
-      if (threadIdx.x == 0) atomicOr(status, kStatusTimeout);
-      aborted = true;
-      break;
+    if (!s_ok) {
+      late_fail = true;  // voted on at the next unit's first barrier
+      if (lane == 0) atomicOr(status, kStatusTimeout);
     }
-    if (!valid) continue;
+    if (!(valid & kUnitValid)) continue;
+    if (!mbar_wait(&fin_ready[s], n & 1)) {
+      late_fail = true;
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+    }
+    const float* fin = fin_all + s * 96;
 
     // ---- merge and store o: thread holds columns c0 + 4t .. c0 + 4t + 3
 #pragma unroll
@@ -674,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      state is written over the old one in the stage and stored by TMA.
     //      Warp w produces F rows 16w .. 16w + 15, all 128 columns.
     if (cm) {
+      named_bar_sync(1, kConsumers);  // zpart of both row tiles is complete
       float acc[16][4];
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
