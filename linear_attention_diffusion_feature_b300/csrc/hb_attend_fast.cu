@@ -83,6 +83,7 @@ enum { kSumP = 0, kSumM, kDenP, kDenM, kSumS, kSumPK, kSumMK };
 enum : int { kUnitValid = 1, kUnitCommit = 2 };  // meta flags of a stage
 
 struct Maps {
+  const uint8_t* qkv[3];  // q, k, v base addresses (L2 prefetch of whole token rows)
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
@@ -251,12 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t unit = (size_t)slot * H + h;
       prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
       prefetch_l2(Z_pool + unit * kF, kF * 4);
+      // the request's block of q, k, v is one contiguous range of L rows of
+      // all heads; the CTAs working on its heads at the same time each
+      // prefetch a 1/H slice of it, so DRAM reads it as one long run
+      const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
+      const size_t off = (size_t)b * kL * H * kD * 2 + (size_t)h * slice;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        prefetch_l2_3d(&maps.q, 64 * j, h, b * kL);
-        prefetch_l2_3d(&maps.k, 64 * j, h, b * kL);
-        prefetch_l2_3d(&maps.v, 64 * j, h, b * kL);
-      }
+      for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
     };
     int slot_next = -1, commit_next = 0;
     for (int i = 0; i < n_local; ++i) {
@@ -784,6 +786,9 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st) {
   Maps maps;
+  maps.qkv[0] = static_cast<const uint8_t*>(q);
+  maps.qkv[1] = static_cast<const uint8_t*>(k);
+  maps.qkv[2] = static_cast<const uint8_t*>(v);
   {
     const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
     const uint64_t strides[1] = {kD * 4};

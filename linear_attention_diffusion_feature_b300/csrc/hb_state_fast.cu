@@ -79,6 +79,8 @@ struct Maps {
 
 struct Args {
   int H, num_slots, RB, splits, accumulate;
+  const uint8_t* k_bytes;  // k, v base addresses (L2 prefetch of whole token rows)
+  const uint8_t* v_bytes;
   int64_t total_rows, max_len;
   const int32_t* slot_idx;
   const int64_t* cu;  // nullptr: request b owns rows [b*RB, b*RB + RB)
@@ -183,7 +185,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bar[kWFull], 16384);
       tma_load_2d(smem + kOffW, &maps.W, 0, h * kD, &bar[kWFull]);
       // k of chunk c is loaded as soon as U = K W_h of chunk c - 2 is done
-      // (it is not needed after that); chunk c + 3 is prefetched into L2
+      // (it is not needed after that). Chunks c + 2 and c + 3 are prefetched
+      // into L2 as whole token rows: the H CTAs of a request each prefetch
+      // a contiguous 1/H slice of the chunk's rows of all heads, so DRAM
+      // sees long contiguous reads instead of 128-byte pieces at the row
+      // stride, and every head's TMA load then hits L2.
+      const int64_t row_bytes = (int64_t)a.H * kD * 2;
+      const int64_t slice = (int64_t)RB * kD * 2;  // = chunk bytes / H
+      auto l2_rows = [&](int c) {
+        if (c >= n_my) return;
+        const int64_t r0 = row0 + (c_begin + c) * RB;
+        const int64_t r1 = r0 + RB < row0 + cnt ? r0 + RB : row0 + cnt;
+        const int64_t lo = r0 * row_bytes + h * slice;
+        const int64_t hi_lim = r1 * row_bytes;
+        const int64_t hi = lo + slice < hi_lim ? lo + slice : hi_lim;
+        if (hi <= lo) return;
+        prefetch_l2(a.k_bytes + lo, (uint32_t)(hi - lo));
+        prefetch_l2(a.v_bytes + lo, (uint32_t)(hi - lo));
+      };
+      l2_rows(0);
+      l2_rows(1);
+      l2_rows(2);
       for (int c = 0; c < n_my; ++c) {
         const int s = c & 1, use = c >> 1;
         if (use > 0 && !mbar_wait(&bar[kKEmpty0 + s], (use - 1) & 1)) {
@@ -191,11 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int row = (int)(row0 + (c_begin + c) * RB);
-        if (c + 3 < n_my) {
-          const int row3 = (int)(row0 + (c_begin + c + 3) * RB);
-          prefetch_l2_3d(&maps.k, 0, h, row3);
-          prefetch_l2_3d(&maps.k, 64, h, row3);
-        }
+        l2_rows(c + 3);
         mbar_arrive_expect_tx(&bar[kKFull0 + s], 2 * RB * 128);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -214,11 +232,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int row = (int)(row0 + (c_begin + c) * RB);
-        if (c + 3 < n_my) {
-          const int row3 = (int)(row0 + (c_begin + c + 3) * RB);
-          prefetch_l2_3d(&maps.v, 0, h, row3);
-          prefetch_l2_3d(&maps.v, 64, h, row3);
-        }
         mbar_arrive_expect_tx(&bar[kVFull0 + s], 2 * RB * 128);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -341,16 +354,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = fmaxf(mx, xmax[q * 128 + tok]);
         mn = fminf(mn, xmin[q * 128 + tok]);
       }
-      // e^{u - max} and e^{min - u} as one FMA and one ex2 each
-      float ep[16], em[16], sp = 0.f, sm = 0.f;
-      const float op = -mx * kLog2e, om = mn * kLog2e;
+      // e^{u - max} as one packed FMA and one ex2 each. The other half uses
+      // e^{min - u} = C / e^{u - max} with C = e^{min - max}: a reciprocal on
+      // the FMA pipe instead of a second ex2, which halves the work of the
+      // special-function unit. That identity needs e^{u - max} to stay a
+      // normal float, so tokens whose u spans more than 60 use ex2 directly.
+      float ep[16], em[16];
+      float2 spp = make_float2(0.f, 0.f), smp = make_float2(0.f, 0.f);
+      {
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        const float2 op = make_float2(-mx * kLog2e, -mx * kLog2e);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        ep[j] = ex2_approx(fmaf(u[j], kLog2e, op));
-        em[j] = ex2_approx(fmaf(-u[j], kLog2e, om));
-        sp += ep[j];
-        sm += em[j];
+        for (int j = 0; j < 16; j += 2) {
+          const float2 x = fma2(make_float2(u[j], u[j + 1]), l2e, op);
+          ep[j] = ex2_approx(x.x);
+          ep[j + 1] = ex2_approx(x.y);
+          spp = add2(spp, make_float2(ep[j], ep[j + 1]));
+        }
+        if (mx - mn <= 60.f) {
+          const float C = ex2_approx((mn - mx) * kLog2e);
+          const float2 C2 = make_float2(C, C);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const float2 r = mul2(C2, rcp2_newton(make_float2(ep[j], ep[j + 1])));
+            em[j] = r.x;
+            em[j + 1] = r.y;
+            smp = add2(smp, r);
+          }
+        } else {
+          const float om = mn * kLog2e;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) em[j] = ex2_approx(fmaf(-u[j], kLog2e, om));
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) smp = add2(smp, make_float2(em[j], em[j + 1]));
+        }
       }
+      float sp = spp.x + spp.y, sm = smp.x + smp.y;
       xsp[sub * 128 + tok] = sp;
       xsm[sub * 128 + tok] = sm;
       named_bar_sync(hbar, 256);
@@ -364,19 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const float* e = half ? em : ep;
-          const float inv = half ? im : ip;
+          const float2 inv = half ? make_float2(im, im) : make_float2(ip, ip);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-              const float p0 = e[8 * q + 2 * p] * inv, p1 = e[8 * q + 2 * p + 1] * inv;
-              zacc[16 * half + 8 * q + 2 * p] += p0;
-              zacc[16 * half + 8 * q + 2 * p + 1] += p1;
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+              const int j = 8 * q + 2 * p;
+              const float2 pv = mul2(make_float2(e[j], e[j + 1]), inv);
+              const float2 z = add2(make_float2(zacc[16 * half + j], zacc[16 * half + j + 1]), pv);
+              zacc[16 * half + j] = z.x;
+              zacc[16 * half + j + 1] = z.y;
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(pv.x, pv.y);
               const float2 hf = __bfloat1622float2(hi);
               hw[p] = *reinterpret_cast<const uint32_t*>(&hi);
-              lw[p] = pack_bf16(p0 - hf.x, p1 - hf.y);
+              const float2 lo = add2(pv, make_float2(-hf.x, -hf.y));
+              lw[p] = pack_bf16(lo.x, lo.y);
             }
             const int chunk = 2 * sub + q;
             const uint32_t off = half * 16384 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
@@ -565,6 +607,8 @@ cudaError_t launch_tc(const Shape& s, int batch, const int32_t* slot_idx, const 
   }
   Args a;
   a.H = s.H;
+  a.k_bytes = static_cast<const uint8_t*>(k);
+  a.v_bytes = static_cast<const uint8_t*>(v);
   a.num_slots = num_slots;
   a.RB = RB;
   a.splits = splits;
