@@ -74,8 +74,9 @@ constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, 
 constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
 constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x 3 x [32]
 constexpr int kOffBar = kOffFin + 2 * 3 * 128;
-constexpr int kOffMeta = kOffBar + 10 * 8;  // per stage: flags, slot
-constexpr int kSmemUsed = kOffMeta + 16;
+constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot
+constexpr int kOffTmemSlot = kOffMeta + 16;
+constexpr int kSmemUsed = kOffTmemSlot + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
@@ -124,6 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = head_full + 4;
   uint64_t* sums_ready = head_full + 6;  // consumers -> coefficient warp
   uint64_t* fin_ready = head_full + 8;   // coefficient warp -> consumers
+  uint64_t* ds_full = head_full + 10;    // committing units: the tensor cores' dS is in TMEM
+  uint64_t* s_updated = head_full + 11;  // committing units: new S, Z are in the stage
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   int* meta = reinterpret_cast<int*>(smem + kOffMeta);
   float* pmax = reinterpret_cast<float*>(smem + kOffPart);  // [32][4]
   float* pmin = pmax + 128;                                 // [32][4]
@@ -144,9 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sums_ready[s], kConsumerWarps);
       mbar_init(&fin_ready[s], 1);
     }
+    mbar_init(ds_full, 1);
+    mbar_init(&s_updated[0], kConsumerWarps);
+    mbar_init(&s_updated[1], kConsumerWarps);
     fence_mbar_init();
   }
+  // committing variant: 128 TMEM columns hold dS = phi(k)^T V [128 F][128 d]
+  if (kCommit && warp == 0) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = kCommit ? *tmem_slot : 0u;
 
   if (warp == kCoefWarp) {
     // ------------------------------------------------- merge coefficients
@@ -155,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // halves of phi(q) with S), from the row sums the consumers leave in the
     // stage, while the consumers run the state contraction.
     int i = 0;
+    uint32_t su_phase[2] = {0u, 0u};  // parity of s_updated per stage
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const int s = i & 1, n = i >> 1;
       const float gl = gate[u % H];
@@ -208,8 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         fin[64 + R] = cN * ism;
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&fin_ready[s]);
+      if (lane == 0) mbar_arrive(&fin_ready[s]);
+      if (kCommit && (meta[s] & kUnitCommit)) {
+        // the consumers have written the new S and Z into the stage: store
+        // them (TMA), and hand the stage back on their behalf once the store
+        // has read it
+        const bool ok = mbar_wait(&s_updated[s], su_phase[s]);
+        su_phase[s] ^= 1u;
+        if (lane == 0) {
+          if (ok) {
+            const int uslot = meta[2 + s];
+            const int h = u % H;
+            const int row = (uslot * H + h) * kF;
+            uint8_t* st = smem + s * kStageStride;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+              tma_store_2d(&maps.S, 32 * bx, row, st + kOffS + bx * 16384);
+            bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, smem + kOffZ + s * 512, kF * 4);
+            bulk_commit();
+            bulk_wait_read();
+          } else {
+            atomicOr(status, kStatusTimeout);
+          }
+          mbar_arrive_cnt(&empty[s], kConsumerWarps + 1);
+        }
+      } else if (lane == 0) {
         mbar_arrive(&empty[s]);  // the row sums in the stage have been read
       }
     }
@@ -329,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // together (a warp left behind at a named barrier would never return).
   int i = 0;
   bool aborted = false, late_fail = false;
+  uint32_t cm_phase = 0;  // parity of ds_full for the next committing unit
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
     const int s = i & 1, n = i >> 1;
     const bool head_ok = mbar_wait(&head_full[s], n & 1);
@@ -612,6 +649,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           zpart[mt * 128 + kFH + c + 1] = colm[1];
         }
       }
+      // dS = phi(k)^T V on the tensor cores (M = F = 128, N = d = 128,
+      // K = 32 tokens, phi(k) as hi and lo; both operands MN-major in shared
+      // memory), running while this unit's state contraction and merge go on
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, kConsumers);
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        constexpr uint32_t idS = umma_idesc_bf16(128, kD, 1, 1);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint64_t aHi = umma_desc_sw128(sKHi + ks * 2048, 4096, 1024);
+          const uint64_t aLo = umma_desc_sw128(sKLo + ks * 2048, 4096, 1024);
+          const uint64_t bV = umma_desc_sw128(sV + ks * 2048, 4096, 1024);
+          umma_bf16(tbase, aHi, bV, idS, ks > 0 ? 1u : 0u);
+          umma_bf16(tbase, aLo, bV, idS, 1u);
+        }
+        umma_commit(ds_full);
+      }
     }
 
     // ---- phase D: num+- = e+- S and U = P V for columns 16w .. 16w + 15
@@ -706,57 +762,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      state is written over the old one in the stage and stored by TMA.
     //      Warp w produces F rows 16w .. 16w + 15, all 128 columns.
     if (cm) {
-      named_bar_sync(1, kConsumers);  // zpart of both row tiles is complete
-      float acc[16][4];
+      // dS rows F = 32 (w % 4) + lane (this warp's TMEM lane quarter),
+      // columns 64 (w / 4) .. 64 (w / 4) + 63, added to the staged old S
+      const bool ds_ok = mbar_wait(ds_full, cm_phase);
+      cm_phase ^= 1u;
+      if (!ds_ok) {
+        late_fail = true;
+        if (lane == 0) atomicOr(status, kStatusTimeout);
+      }
+      tc_fence_after();
+      const int F = 32 * (warp & 3) + lane;
+      const int n0 = 64 * (warp >> 2);
+      const uint32_t lane_bits = (uint32_t)(32 * (warp & 3)) << 16;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-      const uint32_t sKHi = smem_u32(st + kOffPhiKHi), sKLo = smem_u32(st + kOffPhiKLo);
-      const int mi = lane >> 3;
+      for (int part = 0; part < 2; ++part) {
+        float r[32];
+        tmem_ld32(tbase + lane_bits + n0 + 32 * part, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        // phi(k)^T fragments: rows F, columns tokens (transposed loads of [tok][F])
-        uint32_t ah[4], al[4];
-        {
-          const int tokr = 16 * kk + (mi >> 1) * 8 + (lane & 7);
-          const int ch = 2 * warp + (mi & 1);
-          const uint32_t off = (ch >> 3) * 4096 + sw128(tokr, ch & 7);
-          ldsm_x4_t(sKHi + off, ah[0], ah[1], ah[2], ah[3]);
-          ldsm_x4_t(sKLo + off, al[0], al[1], al[2], al[3]);
-        }
-#pragma unroll
-        for (int jp = 0; jp < 8; ++jp) {
-          uint32_t vb[4];
-          const int krow = 16 * kk + (mi & 1) * 8 + (lane & 7);
-          const int dch = 2 * jp + (mi >> 1);
-          ldsm_x4_t(sV + (dch >> 3) * 4096 + sw128(krow, dch & 7), vb[0], vb[1], vb[2], vb[3]);
-          mma_bf16(acc[2 * jp], ah, vb[0], vb[1]);
-          mma_bf16(acc[2 * jp], al, vb[0], vb[1]);
-          mma_bf16(acc[2 * jp + 1], ah, vb[2], vb[3]);
-          mma_bf16(acc[2 * jp + 1], al, vb[2], vb[3]);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const uint32_t a = sS + s_off(F, n0 + 32 * part + 4 * q4);
+          const float4 old = ld_shared_v4f(a);
+          st_shared_v4(a, __float_as_uint(old.x + r[4 * q4]), __float_as_uint(old.y + r[4 * q4 + 1]),
+                       __float_as_uint(old.z + r[4 * q4 + 2]),
+                       __float_as_uint(old.w + r[4 * q4 + 3]));
         }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const uint32_t a = sS + s_off(16 * warp + g + 8 * hr, 8 * j + 2 * t);
-          const float2 old = ld_shared_v2f(a);
-          st_shared_v2f(a, old.x + acc[j][2 * hr], old.y + acc[j][2 * hr + 1]);
-        }
+      tc_fence_before();
       if (threadIdx.x < kF) sZ[threadIdx.x] += zpart[threadIdx.x] + zpart[128 + threadIdx.x];
+      // the coefficient warp stores the new state and releases the stage
       fence_proxy_async_smem();
-      named_bar_sync(1, kConsumers);
-      if (threadIdx.x == 0) {
-        const int uslot = meta[2 + s];
-        const int row = (uslot * H + h) * kF;
-#pragma unroll
-        for (int bx = 0; bx < 4; ++bx) tma_store_2d(&maps.S, 32 * bx, row, st + kOffS + bx * 16384);
-        bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, sZ, kF * 4);
-        bulk_commit();
-        bulk_wait_read();  // the stage may be refilled only after this
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) mbar_arrive(&s_updated[s]);
     }
   }
   if (aborted && threadIdx.x == 0) {
@@ -765,6 +802,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = i; j <= i + 1 && blockIdx.x + j * gridDim.x < units; ++j) {
       mbar_wait(&head_full[j & 1], (j >> 1) & 1);
       mbar_wait(&s_full[j & 1], (j >> 1) & 1);
+    }
+  }
+  if (kCommit) {
+    // every consumer is past its last TMEM read (all leave the loop together)
+    tc_fence_before();
+    named_bar_sync(1, kConsumers);
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tbase, 128);
     }
   }
 }
