@@ -9,12 +9,18 @@
 //
 // The step is bound by the HBM read of S (64 KiB fp32 per request and head,
 // 2/3 of the bytes), so the kernel is a persistent streaming pipeline:
-//   * one CTA per SM, 9 warps: warp 8 is the producer, warps 0-7 compute;
+//   * one CTA per SM, 10 warps: warp 8 is the producer, warp 9 turns the
+//     row sums into merge coefficients (and, in the committing variant,
+//     stores updated states), warps 0-7 compute;
 //   * a two-stage shared-memory ring; each stage holds one (request, head)
 //     unit in two parts with their own mbarriers: the head (q, k, v as two
 //     4 KiB SWIZZLE_128B boxes each, W_h 16 KiB, Z 512 B) and S (four 16 KiB
 //     SWIZZLE_128B boxes); the feature map and block softmax run on the head
 //     while S is still arriving;
+//   * in the committing variant, units of committing requests come first in
+//     the grid-wide order, so that every CTA gets one or two of them;
+//   * launched with programmatic stream serialization: barrier set-up and
+//     TMEM allocation overlap the previous kernel's tail;
 //   * the producer reads slot indices ahead, prefetches the tiles of the
 //     units two steps ahead into L2, and issues unit i+1's loads while the
 //     consumers compute unit i; consumers release a stage through a third
@@ -74,8 +80,8 @@ constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, 
 constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
 constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x 3 x [32]
 constexpr int kOffBar = kOffFin + 2 * 3 * 128;
-constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot
-constexpr int kOffTmemSlot = kOffMeta + 16;
+constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head
+constexpr int kOffTmemSlot = kOffMeta + 32;
 constexpr int kSmemUsed = kOffTmemSlot + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
@@ -159,6 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = kCommit ? *tmem_slot : 0u;
+  // the set-up above overlaps the previous kernel's tail; global memory is
+  // touched only from here on
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kCoefWarp) {
     // ------------------------------------------------- merge coefficients
@@ -170,11 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t su_phase[2] = {0u, 0u};  // parity of s_updated per stage
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const int s = i & 1, n = i >> 1;
-      const float gl = gate[u % H];
       if (!mbar_wait(&sums_ready[s], n & 1)) {
         if (lane == 0) atomicOr(status, kStatusTimeout);
         break;
       }
+      const int h = meta[6 + s];
+      const float gl = gate[h];
       if (meta[s] & kUnitValid) {
         const float* sums = reinterpret_cast<const float*>(smem + s * kStageStride + kOffSums);
         float* fin = fin_all + s * 96;
@@ -231,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if (ok) {
             const int uslot = meta[2 + s];
-            const int h = u % H;
             const int row = (uslot * H + h) * kF;
             uint8_t* st = smem + s * kStageStride;
 #pragma unroll
@@ -255,10 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; lane 0 issues the copies. A unit's q, k,
-    // v and W_h do not depend on its state slot, so they are issued before
-    // the slot index is known. Slot indices are read 32 units at a time
-    // (lane j holds the slot of local unit 32w + j), and each unit's tiles
-    // are prefetched into L2 two units before their TMA load is issued.
+    // v and W_h do not depend on its state slot, so the first unit's are
+    // issued before its slot index is read; later units' slots are read
+    // three units ahead, and each unit's tiles are prefetched into L2 two
+    // units before their TMA load is issued.
     if (lane == 0) {
       prefetch_tmap(&maps.S);
       prefetch_tmap(&maps.q);
@@ -268,35 +278,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int first = blockIdx.x, stride = gridDim.x;
     const int n_local = first < units ? (units - first + stride - 1) / stride : 0;
-    int win = -1, win_slot = -1, win_commit = 0;
-    auto slot_of = [&](int i) -> int {  // warp-uniform i, called in increasing order
-      if ((i >> 5) != win) {
-        win = i >> 5;
-        const int uu = first + (32 * win + lane) * stride;
-        win_slot = uu < units ? slot_idx[uu / H] : -1;
-        win_commit = (kCommit && uu < units) ? commit_mask[uu / H] : 0;
+    // Unit schedule. Position p = first + i * stride of the grid-wide order
+    // is this CTA's i-th unit. Committing requests are heavier (their state
+    // is also updated and stored), so in the committing variant their units
+    // take the first positions, which spreads them evenly over the CTAs;
+    // then come the other requests', each group in request order, heads
+    // innermost. Each flag value has a cursor over the mask, 32 requests
+    // at a time.
+    int cur_win[2] = {0, 0}, cur_before[2] = {0, 0};
+    uint32_t cur_bits[2] = {0u, 0u};
+    auto window_bits = [&](int w, int want) -> uint32_t {
+      const int j = 32 * w + lane;
+      const bool hit = j < batch && ((commit_mask[j] != 0 ? 1 : 0) == want);
+      return __ballot_sync(0xffffffffu, hit);
+    };
+    int n_commit = 0;  // committing requests
+    if (kCommit) {
+      for (int j = lane; j < batch; j += 32) {
+        const int f = commit_mask[j] != 0 ? 1 : 0;
+        n_commit += f;
+        if (j < 32) {  // the cursors' first window
+          cur_bits[1] = f;
+          cur_bits[0] = 1 - f;
+        }
       }
-      return __shfl_sync(0xffffffffu, win_slot, i & 31);
+      cur_bits[1] = __ballot_sync(0xffffffffu, cur_bits[1] != 0u);
+      cur_bits[0] = __ballot_sync(0xffffffffu, cur_bits[0] != 0u);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) n_commit += __shfl_xor_sync(0xffffffffu, n_commit, o2);
+    }
+    const int commit_units = n_commit * H;
+    // r-th (0-based, r increasing from call to call) request whose commit
+    // flag is `want`; -1 if the mask no longer holds that many (it changed
+    // while this kernel ran)
+    auto nth_request = [&](int want, int r) -> int {
+      for (;;) {
+        const int cnt = __popc(cur_bits[want]);
+        if (cur_before[want] + cnt > r) {
+          uint32_t bits = cur_bits[want];
+          for (int t = r - cur_before[want]; t > 0; --t) bits &= bits - 1u;
+          return 32 * cur_win[want] + __ffs(bits) - 1;
+        }
+        cur_before[want] += cnt;
+        if (32 * ++cur_win[want] >= batch) return -1;
+        cur_bits[want] = window_bits(cur_win[want], want);
+      }
     };
-    auto commit_of = [&](int i) -> int {  // after slot_of(i), same window
-      return __shfl_sync(0xffffffffu, win_commit, i & 31);
+    struct Unit {
+      int b, h, slot, commit;
     };
-    auto l2_prefetch = [&](int i, int slot) {
-      const int uu = first + i * stride;
-      const int b = uu / H, h = uu - b * H;
-      if (lane != 0 || slot < 0 || slot >= num_slots) return;
-      const size_t unit = (size_t)slot * H + h;
+    auto unit_at = [&](int i) -> Unit {  // warp-uniform; i increasing between calls
+      Unit un;
+      const int p = first + i * stride;
+      int r;
+      if (p < commit_units) {
+        r = p / H;
+        un.h = p - r * H;
+        un.b = nth_request(1, r);
+        un.commit = 1;
+      } else {
+        r = (p - commit_units) / H;
+        un.h = p - commit_units - r * H;
+        un.b = kCommit ? nth_request(0, r) : r;
+        un.commit = 0;
+      }
+      un.slot = -1;  // not read yet
+      if (un.b < 0) {  // flagged through the slot; nothing is written for it
+        un.b = 0;
+        un.slot = -2;
+      }
+      return un;
+    };
+    auto with_slot = [&](Unit un) -> Unit {
+      if (un.slot == -1) un.slot = slot_idx[un.b];
+      return un;
+    };
+    auto l2_prefetch = [&](const Unit& un) {
+      if (lane != 0 || un.slot < 0 || un.slot >= num_slots) return;
+      const size_t unit = (size_t)un.slot * H + un.h;
       prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
       prefetch_l2(Z_pool + unit * kF, kF * 4);
       // the request's block of q, k, v is one contiguous range of L rows of
       // all heads; the CTAs working on its heads at the same time each
       // prefetch a 1/H slice of it, so DRAM reads it as one long run
       const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
-      const size_t off = (size_t)b * kL * H * kD * 2 + (size_t)h * slice;
+      const size_t off = (size_t)un.b * kL * H * kD * 2 + (size_t)un.h * slice;
 #pragma unroll
       for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
     };
-    int slot_next = -1, commit_next = 0;
+    // units i, i + 1 and i + 2 (i + 2 is prefetched into L2 at step i); the
+    // first unit's slot is read after its head loads have been issued
+    Unit cur{}, nxt{}, nn{};
+    if (n_local > 0) cur = unit_at(0);
     for (int i = 0; i < n_local; ++i) {
       const int s = i & 1, n = i >> 1;
       bool ok = true;
@@ -305,8 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) atomicOr(status, kStatusTimeout);
         break;
       }
-      const int u = first + i * stride;
-      const int b = u / H, h = u - b * H;
+      const int b = cur.b, h = cur.h;
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
         mbar_expect_tx(&head_full[s], kHeadBytes);
@@ -318,16 +390,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
       }
-      const int slot = i == 0 ? slot_of(0) : slot_next;
-      const int commit = i == 0 ? commit_of(0) : commit_next;
+      if (i == 0) cur = with_slot(cur);
       if (lane == 0) {
+        const int slot = cur.slot;
+        meta[4 + s] = b;
+        meta[6 + s] = h;
         if (slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
           mbar_arrive(&head_full[s]);
           mbar_arrive(&s_full[s]);
         } else {
-          meta[s] = kUnitValid | (commit != 0 ? kUnitCommit : 0);
+          meta[s] = kUnitValid | (cur.commit != 0 ? kUnitCommit : 0);
           meta[2 + s] = slot;
           mbar_expect_tx(&head_full[s], 512);
           bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
@@ -340,12 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
         }
       }
-      if (i + 1 < n_local) {
-        slot_next = slot_of(i + 1);
-        commit_next = commit_of(i + 1);
+      if (i == 0) {
+        if (n_local > 1) nxt = with_slot(unit_at(1));
+        if (n_local > 2) nn = with_slot(unit_at(2));
+        if (n_local > 1) l2_prefetch(nxt);
       }
-      if (i == 0 && n_local > 1) l2_prefetch(1, slot_next);
-      if (i + 2 < n_local) l2_prefetch(i + 2, slot_of(i + 2));
+      if (i + 2 < n_local) l2_prefetch(nn);
+      cur = nxt;
+      nxt = nn;
+      if (i + 3 < n_local) nn = with_slot(unit_at(i + 3));
     }
     return;
   }
@@ -379,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sP = smem_u32(st + kOffP);
     float* sums = reinterpret_cast<float*>(st + kOffSums);  // [7][32][4]
     float* sZ = reinterpret_cast<float*>(smem + kOffZ + s * 512);
-    const int b = u / H, h = u - b * H;
+    const int b = meta[4 + s], h = meta[6 + s];
     const int R0 = 16 * mt + g, R1 = R0 + 8;
     // stage flags, valid once the head has landed (the producer writes them
     // before it arrives on head_full)
@@ -874,10 +951,10 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   }
   const int units = batch * s.H;
   const int grid = units < g_num_sms ? units : g_num_sms;
-  kernel<<<grid, kThreads, kSmemBytes, st>>>(
-      maps, batch, s.H, num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
-      const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o), status);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, maps, batch, s.H,
+                    num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
+                    const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o),
+                    status);
 }
 
 }  // namespace hb

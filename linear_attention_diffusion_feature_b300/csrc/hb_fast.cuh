@@ -3,12 +3,33 @@
 // predicates. Every other shape or dtype goes to the generic kernels.
 #pragma once
 
+#include <utility>
+
 #include "hb_internal.cuh"
 
 namespace hb {
 
 inline bool production_shape(const Shape& s) {
   return s.dtype == HB_DTYPE_BF16 && s.d == 128 && s.f == 64 && s.L == 32;
+}
+
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel in the stream finishes, and the kernel
+// itself calls grid_dep_wait() before its first global memory access.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 bool fast_feature_map_ok(const Shape& s);

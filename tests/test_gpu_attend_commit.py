@@ -149,3 +149,38 @@ def test_attend_commit_bad_slot_is_skipped_and_flagged(cuda_device):
         else:
             assert torch.equal(S[sl], S0[sl])
     assert torch.equal(S[5], S0[5])  # the skipped request's real slot
+
+
+@pytest.mark.parametrize("pattern", ["every_third", "last_only", "first_window_none"])
+def test_attend_commit_schedules_any_mask(cuda_device, pattern):
+    """The kernel orders committing requests' units first; with 100 requests
+    (four 32-request windows of the mask) and permuted slots, any mask gives
+    the two separate calls' result."""
+    B, H = 100, 16
+    cfg = hb.Config(H, 128, 64, 32)
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (inputs.draw(90 + i, (B, 32, H, 128), torch.bfloat16).to(cuda_device)
+               for i in range(3))
+    W = inputs.draw(93, (H, 128, 64), torch.bfloat16, std=128 ** -0.5).to(cuda_device)
+    gate = inputs.draw(94, (H,), torch.float32).to(cuda_device)
+    perm = torch.randperm(B, generator=g).to(torch.int32).to(cuda_device)
+    flags = {"every_third": [b % 3 == 0 for b in range(B)],
+             "last_only": [b == B - 1 for b in range(B)],
+             "first_window_none": [b >= 32 and b % 2 == 1 for b in range(B)]}[pattern]
+    mask = torch.tensor(flags, dtype=torch.int32, device=cuda_device)
+    S, Z = new_pool(cfg, B, cuda_device)
+    S.copy_(inputs.draw(95, S.shape, torch.float32).to(cuda_device) * 1e-2)
+    Z.copy_(inputs.draw(96, Z.shape, torch.float32).abs().to(cuda_device) + 1.0)
+    S2, Z2 = S.clone(), Z.clone()
+    o1 = hb.hb_block_attend_commit(cfg, perm, q, k, v, S, Z, W, gate, mask)
+    o2 = hb.hb_block_attend(cfg, perm, q, k, v, S2, Z2, W, gate)
+    ci = torch.nonzero(mask).flatten()
+    hb.hb_commit_block(cfg, perm[ci].contiguous(), k[ci].contiguous(), v[ci].contiguous(), W,
+                       S2, Z2)
+    assert_status_ok()
+    assert torch.equal(o1, o2)
+    assert unit_err(f64(S), f64(S2), 2) <= TOL_STATE
+    assert unit_err(f64(Z), f64(Z2), 2) <= TOL_STATE
+    untouched = torch.ones(B, dtype=torch.bool, device=cuda_device)
+    untouched[perm[ci].long()] = False
+    assert torch.equal(S[untouched], S2[untouched])
