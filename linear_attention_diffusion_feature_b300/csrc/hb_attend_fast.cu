@@ -50,6 +50,9 @@ using namespace ptx;
 
 constexpr int kD = 128, kFH = 64, kF = 128, kL = 32;
 constexpr int kConsumerWarps = 8;
+// q, k, v and W of a step are prefetched into L2 ahead of the loads when
+// together they take at most this many bytes
+constexpr size_t kPrefetchBudget = size_t(48) << 20;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;    // warp 8
 constexpr int kCoefWarp = kConsumerWarps + 1;    // warp 9: per-row merge coefficients
@@ -82,7 +85,10 @@ constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x
 constexpr int kOffBar = kOffFin + 2 * 3 * 128;
 constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head
 constexpr int kOffTmemSlot = kOffMeta + 32;
-constexpr int kSmemUsed = kOffTmemSlot + 16;
+// committing variant: the commit mask as one bit per request, 32 per word
+constexpr int kMaskWords = 1024;  // batches up to 32768 are scheduled commit-first
+constexpr int kOffMaskBits = kOffTmemSlot + 16;
+constexpr int kSmemUsed = kOffMaskBits + 4 * kMaskWords;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
@@ -91,6 +97,7 @@ enum : int { kUnitValid = 1, kUnitCommit = 2 };  // meta flags of a stage
 
 struct Maps {
   const uint8_t* qkv[3];  // q, k, v base addresses (L2 prefetch of whole token rows)
+  const uint8_t* w;       // W base address
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
@@ -165,8 +172,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = kCommit ? *tmem_slot : 0u;
-  // the set-up above overlaps the previous kernel's tail; global memory is
-  // touched only from here on
+  // The set-up above overlaps the previous kernel's tail, and so does an L2
+  // prefetch of the step's q, k, v and W when together they take a modest
+  // part of L2: each CTA prefetches a 1/grid share. A prefetch reads nothing
+  // into the SM, and L2 is where the previous kernel's writes land, so this
+  // is safe before the wait. Every load and store of global memory comes
+  // after grid_dep_wait().
+  if (warp == kProducerWarp && lane == 0) {
+    const size_t qkv_bytes = (size_t)batch * kL * H * kD * 2;
+    const size_t w_bytes = (size_t)H * kD * kFH * 2;
+    if (3 * qkv_bytes + w_bytes <= kPrefetchBudget) {
+      const uint8_t* base[4] = {maps.qkv[0], maps.qkv[1], maps.qkv[2], maps.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const size_t bytes = j < 3 ? qkv_bytes : w_bytes;
+        // 16-byte aligned share of this CTA, issued in pieces of <= 32 KiB
+        const size_t share = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+        size_t lo = (size_t)blockIdx.x * share;
+        const size_t hi = lo + share < bytes ? lo + share : bytes;
+        for (; lo < hi; lo += 32768) {
+          const size_t n = (hi - lo < 32768 ? hi - lo : 32768) & ~size_t(15);
+          if (n > 0) prefetch_l2(base[j] + lo, (uint32_t)n);
+        }
+      }
+    }
+  }
   grid_dep_wait();
   grid_dep_launch();
 
@@ -283,102 +313,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     // is also updated and stored), so in the committing variant their units
     // take the first positions, which spreads them evenly over the CTAs;
     // then come the other requests', each group in request order, heads
-    // innermost. Each flag value has a cursor over the mask, 32 requests
-    // at a time.
-    int cur_win[2] = {0, 0}, cur_before[2] = {0, 0};
-    uint32_t cur_bits[2] = {0u, 0u};
-    auto window_bits = [&](int w, int want) -> uint32_t {
-      const int j = 32 * w + lane;
-      const bool hit = j < batch && ((commit_mask[j] != 0 ? 1 : 0) == want);
-      return __ballot_sync(0xffffffffu, hit);
-    };
+    // innermost. The mask is kept as bits in shared memory.
+    uint32_t* mask_bits = reinterpret_cast<uint32_t*>(smem + kOffMaskBits);
+    const int mask_words = (batch + 31) >> 5;
+    const bool commit_first = kCommit && mask_words <= kMaskWords;
     int n_commit = 0;  // committing requests
-    if (kCommit) {
-      for (int j = lane; j < batch; j += 32) {
-        const int f = commit_mask[j] != 0 ? 1 : 0;
-        n_commit += f;
-        if (j < 32) {  // the cursors' first window
-          cur_bits[1] = f;
-          cur_bits[0] = 1 - f;
-        }
+    if (commit_first) {
+      for (int w = 0; w < mask_words; ++w) {
+        const int j = 32 * w + lane;
+        const uint32_t bits = __ballot_sync(0xffffffffu, j < batch && commit_mask[j] != 0);
+        if (lane == 0) mask_bits[w] = bits;
+        n_commit += __popc(bits);
       }
-      cur_bits[1] = __ballot_sync(0xffffffffu, cur_bits[1] != 0u);
-      cur_bits[0] = __ballot_sync(0xffffffffu, cur_bits[0] != 0u);
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) n_commit += __shfl_xor_sync(0xffffffffu, n_commit, o2);
+      __syncwarp();
     }
     const int commit_units = n_commit * H;
-    // r-th (0-based, r increasing from call to call) request whose commit
-    // flag is `want`; -1 if the mask no longer holds that many (it changed
-    // while this kernel ran)
+    // Lane j describes local unit 32 W + j of window W. Its request comes
+    // from a per-lane cursor over the mask bits for each flag value (a
+    // lane's units have increasing positions, so the cursors only move
+    // forward); -1 if the mask no longer holds that many (it changed while
+    // this kernel ran).
+    int cw[2] = {0, 0}, cbefore[2] = {0, 0};
     auto nth_request = [&](int want, int r) -> int {
       for (;;) {
-        const int cnt = __popc(cur_bits[want]);
-        if (cur_before[want] + cnt > r) {
-          uint32_t bits = cur_bits[want];
-          for (int t = r - cur_before[want]; t > 0; --t) bits &= bits - 1u;
-          return 32 * cur_win[want] + __ffs(bits) - 1;
+        if (cw[want] >= mask_words) return -1;
+        const int w = cw[want];
+        uint32_t bits = mask_bits[w];
+        if (!want) {
+          const int left = batch - 32 * w;
+          bits = ~bits & (left >= 32 ? 0xffffffffu : (1u << left) - 1u);
         }
-        cur_before[want] += cnt;
-        if (32 * ++cur_win[want] >= batch) return -1;
-        cur_bits[want] = window_bits(cur_win[want], want);
+        const int cnt = __popc(bits);
+        if (cbefore[want] + cnt > r) {
+          for (int t = r - cbefore[want]; t > 0; --t) bits &= bits - 1u;
+          return 32 * w + __ffs(bits) - 1;
+        }
+        cbefore[want] += cnt;
+        ++cw[want];
       }
     };
-    struct Unit {
-      int b, h, slot, commit;
+    struct Window {
+      int b, h, flags;  // flags: kUnitCommit, or -1 for a request the mask lost
+      int slot;
     };
-    auto unit_at = [&](int i) -> Unit {  // warp-uniform; i increasing between calls
-      Unit un;
+    // fills this lane's entry of window W and issues its slot load
+    auto fill_window = [&](int W) -> Window {
+      Window wd{0, 0, 0, -1};
+      const int i = 32 * W + lane;
+      if (i >= n_local) return wd;
       const int p = first + i * stride;
       int r;
       if (p < commit_units) {
         r = p / H;
-        un.h = p - r * H;
-        un.b = nth_request(1, r);
-        un.commit = 1;
+        wd.h = p - r * H;
+        wd.b = nth_request(1, r);
+        wd.flags = kUnitCommit;
       } else {
         r = (p - commit_units) / H;
-        un.h = p - commit_units - r * H;
-        un.b = kCommit ? nth_request(0, r) : r;
-        un.commit = 0;
+        wd.h = p - commit_units - r * H;
+        wd.b = commit_first ? nth_request(0, r) : r;
+        wd.flags = (kCommit && !commit_first && commit_mask[wd.b] != 0) ? kUnitCommit : 0;
       }
-      un.slot = -1;  // not read yet
-      if (un.b < 0) {  // flagged through the slot; nothing is written for it
-        un.b = 0;
-        un.slot = -2;
+      if (wd.b < 0) {  // flagged through the slot; nothing is written for it
+        wd.b = 0;
+        wd.flags = -1;
+      } else {
+        wd.slot = slot_idx[wd.b];
       }
-      return un;
+      return wd;
     };
-    auto with_slot = [&](Unit un) -> Unit {
-      if (un.slot == -1) un.slot = slot_idx[un.b];
-      return un;
+    Window win_cur = fill_window(0), win_next = fill_window(1);
+    int win_base = 0;  // window index of win_cur
+    // fields of local unit i (warp-uniform, within the two windows held)
+    auto unit_b = [&](int i) {
+      return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.b : win_next.b, i & 31);
     };
-    auto l2_prefetch = [&](const Unit& un) {
-      if (lane != 0 || un.slot < 0 || un.slot >= num_slots) return;
-      const size_t unit = (size_t)un.slot * H + un.h;
-      prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
-      prefetch_l2(Z_pool + unit * kF, kF * 4);
-      // the request's block of q, k, v is one contiguous range of L rows of
-      // all heads; the CTAs working on its heads at the same time each
-      // prefetch a 1/H slice of it, so DRAM reads it as one long run
-      const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
-      const size_t off = (size_t)un.b * kL * H * kD * 2 + (size_t)un.h * slice;
-#pragma unroll
-      for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
+    auto unit_h = [&](int i) {
+      return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.h : win_next.h, i & 31);
     };
-    // units i, i + 1 and i + 2 (i + 2 is prefetched into L2 at step i); the
-    // first unit's slot is read after its head loads have been issued
-    Unit cur{}, nxt{}, nn{};
-    if (n_local > 0) cur = unit_at(0);
-    for (int i = 0; i < n_local; ++i) {
-      const int s = i & 1, n = i >> 1;
-      bool ok = true;
-      if (lane == 0 && n > 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-        if (lane == 0) atomicOr(status, kStatusTimeout);
-        break;
-      }
-      const int b = cur.b, h = cur.h;
+    auto unit_flags = [&](int i) {
+      return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.flags : win_next.flags,
+                         i & 31);
+    };
+    auto unit_slot = [&](int i) {
+      return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.slot : win_next.slot,
+                         i & 31);
+    };
+    auto issue_head = [&](int i) {
+      const int s = i & 1;
+      const int b = unit_b(i), h = unit_h(i);
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
         mbar_expect_tx(&head_full[s], kHeadBytes);
@@ -390,18 +413,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
       }
-      if (i == 0) cur = with_slot(cur);
+    };
+    auto issue_state = [&](int i) {
+      const int s = i & 1;
+      const int b = unit_b(i), h = unit_h(i);
+      const int flags = unit_flags(i), slot = unit_slot(i);
+      uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
-        const int slot = cur.slot;
         meta[4 + s] = b;
         meta[6 + s] = h;
-        if (slot < 0 || slot >= num_slots) {
+        if (flags < 0 || slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
           mbar_arrive(&head_full[s]);
           mbar_arrive(&s_full[s]);
         } else {
-          meta[s] = kUnitValid | (cur.commit != 0 ? kUnitCommit : 0);
+          meta[s] = kUnitValid | flags;
           meta[2 + s] = slot;
           mbar_expect_tx(&head_full[s], 512);
           bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
@@ -414,15 +441,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
         }
       }
-      if (i == 0) {
-        if (n_local > 1) nxt = with_slot(unit_at(1));
-        if (n_local > 2) nn = with_slot(unit_at(2));
-        if (n_local > 1) l2_prefetch(nxt);
+    };
+    auto l2_prefetch = [&](int i) {
+      const int b = unit_b(i), h = unit_h(i), slot = unit_slot(i);
+      if (lane != 0 || slot < 0 || slot >= num_slots) return;
+      const size_t unit = (size_t)slot * H + h;
+      prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
+      prefetch_l2(Z_pool + unit * kF, kF * 4);
+      // the request's block of q, k, v is one contiguous range of L rows of
+      // all heads; the CTAs working on its heads at the same time each
+      // prefetch a 1/H slice of it, so DRAM reads it as one long run
+      const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
+      const size_t off = (size_t)b * kL * H * kD * 2 + (size_t)h * slice;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
+    };
+    // Both stages are free at the start. Unit 0 goes out first and whole;
+    // unit 1's head follows, but its state only once unit 0's has landed,
+    // so that DRAM serves unit 0 first and its computation starts early.
+    // Later units are prefetched into L2 two units ahead of their TMA loads.
+    if (n_local > 0) {
+      issue_head(0);
+      issue_state(0);
+    }
+    if (n_local > 1) {
+      issue_head(1);
+      if (lane == 0) mbar_wait(&s_full[0], 0);  // a wait that runs out only delays
+      __syncwarp();
+      issue_state(1);
+    }
+    if (n_local > 2) l2_prefetch(2);
+    for (int i = 2; i < n_local; ++i) {
+      const int s = i & 1, n = i >> 1;
+      if ((i >> 5) != win_base) {  // move on to the next window
+        win_cur = win_next;
+        ++win_base;
+        win_next = fill_window(win_base + 1);
       }
-      if (i + 2 < n_local) l2_prefetch(nn);
-      cur = nxt;
-      nxt = nn;
-      if (i + 3 < n_local) nn = with_slot(unit_at(i + 3));
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        if (lane == 0) atomicOr(status, kStatusTimeout);
+        break;
+      }
+      issue_head(i);
+      issue_state(i);
+      if (i == 2 && i + 1 < n_local) l2_prefetch(i + 1);
+      if (i + 2 < n_local) l2_prefetch(i + 2);
     }
     return;
   }
@@ -840,7 +905,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      Warp w produces F rows 16w .. 16w + 15, all 128 columns.
     if (cm) {
       // dS rows F = 32 (w % 4) + lane (this warp's TMEM lane quarter),
-      // columns 64 (w / 4) .. 64 (w / 4) + 63, added to the staged old S
+      // columns 64 (w / 4) .. 64 (w / 4) + 63, added to the staged old S,
+      // once every warp's state contraction has finished reading it
+      named_bar_sync(1, kConsumers);
       const bool ds_ok = mbar_wait(ds_full, cm_phase);
       cm_phase ^= 1u;
       if (!ds_ok) {
@@ -912,6 +979,7 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   maps.qkv[0] = static_cast<const uint8_t*>(q);
   maps.qkv[1] = static_cast<const uint8_t*>(k);
   maps.qkv[2] = static_cast<const uint8_t*>(v);
+  maps.w = static_cast<const uint8_t*>(W);
   {
     const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
     const uint64_t strides[1] = {kD * 4};

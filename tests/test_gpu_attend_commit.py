@@ -184,3 +184,31 @@ def test_attend_commit_schedules_any_mask(cuda_device, pattern):
     untouched = torch.ones(B, dtype=torch.bool, device=cuda_device)
     untouched[perm[ci].long()] = False
     assert torch.equal(S[untouched], S2[untouched])
+
+
+def test_attend_commit_many_units_per_cta(cuda_device):
+    """700 requests: every CTA runs more than 64 units, so the kernel's unit
+    table moves through several 32-unit windows; the result is still that of
+    the two separate calls."""
+    B, H = 700, 16
+    cfg = hb.Config(H, 128, 64, 32)
+    g = torch.Generator().manual_seed(11)
+    q, k, v = (torch.randn((B, 32, H, 128), generator=g).to(torch.bfloat16).to(cuda_device)
+               for _ in range(3))
+    W = (torch.randn((H, 128, 64), generator=g) * 128 ** -0.5).to(torch.bfloat16).to(cuda_device)
+    gate = torch.randn((H,), generator=g).to(cuda_device)
+    perm = torch.randperm(B, generator=g).to(torch.int32).to(cuda_device)
+    mask = (torch.rand(B, generator=g) < 0.3).to(torch.int32).to(cuda_device)
+    S, Z = new_pool(cfg, B, cuda_device)
+    S.copy_(torch.randn(S.shape, generator=g).to(cuda_device) * 1e-2)
+    Z.copy_(torch.rand(Z.shape, generator=g).to(cuda_device) + 1.0)
+    S2, Z2 = S.clone(), Z.clone()
+    o1 = hb.hb_block_attend_commit(cfg, perm, q, k, v, S, Z, W, gate, mask)
+    o2 = hb.hb_block_attend(cfg, perm, q, k, v, S2, Z2, W, gate)
+    ci = torch.nonzero(mask).flatten()
+    hb.hb_commit_block(cfg, perm[ci].contiguous(), k[ci].contiguous(), v[ci].contiguous(), W,
+                       S2, Z2)
+    assert_status_ok()
+    assert torch.equal(o1, o2)
+    assert unit_err(f64(S), f64(S2), 2) <= TOL_STATE
+    assert unit_err(f64(Z), f64(Z2), 2) <= TOL_STATE
