@@ -167,7 +167,7 @@ def _traffic(kernel: str):
         return None
     from linear_attention_diffusion_feature_b300 import build
 
-    if rec.get("source_sha") != build.source_digest():
+    if rec.get("source_sha") != build.source_digest(rec.get("sources")):
         return None
     return rec.get("bytes_per_launch")
 
@@ -455,8 +455,9 @@ def run_prefill(args):
     med = _median(ms)
     tokens = nB * T
     nbytes = 2 * tokens * H * D * 2 + nB * H * (F * D + F) * 4 + H * D * FH * 2
-    # tensor work as issued: U = K W (2 d f), phi^T V and phi^T 1 with phi split hi + lo
-    flops = tokens * H * (2 * D * FH + 2 * 2 * F * D + 2 * 2 * F * 16)
+    # tensor work as issued: U = K W (2 d f) and phi^T V with phi split hi + lo
+    # (Z = sum of phi is summed on the CUDA cores)
+    flops = tokens * H * (2 * D * FH + 2 * 2 * F * D)
     peak, kind = _peaks()
     tpeak, tkind = _tensor_peak()
     achieved = nbytes / (med / 1e3) / 1e9

@@ -59,11 +59,16 @@ def _compile(nvcc: str, src: str, verbose: bool) -> str:
     return obj
 
 
-def source_digest() -> str:
-    """sha256 over the library's CUDA sources and headers (names and bytes)."""
+def source_digest(names=None) -> str:
+    """sha256 over the library's CUDA sources and headers (names and bytes);
+    with ``names``, over those files of the source folder only (a kernel's
+    own file and the headers it includes)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                   + glob.glob(os.path.join(INCLUDE, "*.h")))
+    if names is None:
+        files = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+                       + glob.glob(os.path.join(INCLUDE, "*.h")))
+    else:
+        files = [os.path.join(CSRC, n) for n in sorted(names)]
     for path in files:
         h.update(os.path.basename(path).encode())
         with open(path, "rb") as fh:
