@@ -223,6 +223,38 @@ def attend_bruteforce(q, k, v, k_prev, v_prev, W, gate,
     return o
 
 
+def prefill_attend(q, k, v, W, gate, L: int, merge: int = MERGE_SHARED_NORM, scale=None,
+                   S0=None, Z0=None):
+    """A prompt processed block by block with block-hybrid attention, so that
+    every prompt token gets its output ([GIST] "Methodology: Block-Hybrid
+    Attention / Architecture Design": exact softmax inside the active block,
+    linear attention over the committed blocks through S and Z, which change
+    only when a block is committed).
+
+    Reading taken: the prompt q/k/v [T, H, d] (T a multiple of L) is a
+    sequence of T / L blocks; block j is the active block, attending to the
+    state of blocks 0 .. j-1 (added to the initial state S0, Z0, zero when
+    omitted), and is then committed. The pages run this form when the layers
+    are trained against their softmax teacher ([GIST] "Retrofitting
+    Strategy", stage 1) and give no other prefill formula.
+
+    Returns (o [T, H, d], S [H, F, d], Z [H, F]) in float64.
+    """
+    q, k, v, W = (_f64(a) for a in (q, k, v, W))
+    T, H, d = q.shape
+    if T % L != 0:
+        raise ValueError("prompt length must be a multiple of the block length")
+    f = W.shape[2]
+    S = np.zeros((H, 2 * f, d)) if S0 is None else _f64(S0).copy()
+    Z = np.zeros((H, 2 * f)) if Z0 is None else _f64(Z0).copy()
+    o = np.empty((T, H, d))
+    for j0 in range(0, T, L):
+        blk = slice(j0, j0 + L)
+        o[blk] = attend(q[blk], k[blk], v[blk], S, Z, W, gate, merge, scale)
+        S, Z = commit(S, Z, k[blk], v[blk], W)
+    return o, S, Z
+
+
 def softmax_kv_attend(k_prefix, v_prefix, q, k, v, scale=None):
     """Full-prefix softmax attention of the active block over a KV cache, the
     cost the method removes ([ABS]: each denoising step attends to all

@@ -267,6 +267,64 @@ def check_softmax_kv_empty_prefix(ob):
     _close(o, _sdpa(p["q"], p["k"], p["v"]), rtol=1e-10)
 
 
+# ------------------------------------------------- prompt with outputs (N1)
+
+def _prompt_problem(seed, T=12, L=4, H=2, d=6, f=2, N0=5):
+    g = np.random.default_rng(seed)
+    return dict(
+        q=g.standard_normal((T, H, d)), k=g.standard_normal((T, H, d)),
+        v=g.standard_normal((T, H, d)), k0=g.standard_normal((N0, H, d)),
+        v0=g.standard_normal((N0, H, d)), W=g.standard_normal((H, d, f)) / np.sqrt(d),
+        gate=g.standard_normal(H), L=L)
+
+
+def check_prefill_attend_vs_bruteforce(ob):
+    """Block j of a prompt attends to exactly the tokens before it: each
+    block's output equals the state-free token-by-token formulation over
+    the earlier tokens (and an earlier context, when one is given), and the
+    final state equals the plain sum over every token, built here from
+    outer products of phi(k_t) and v_t."""
+    p = _prompt_problem(7)
+    L = p["L"]
+    for merge in (ob.MERGE_SHARED_NORM, ob.MERGE_CONVEX):
+        for with_context in (False, True):
+            if with_context:
+                S0, Z0 = ob.prefill(p["k0"], p["v0"], p["W"])
+                kc, vc = p["k0"], p["v0"]
+            else:
+                S0 = Z0 = None
+                kc, vc = p["k0"][:0], p["v0"][:0]
+            o, S, Z = ob.prefill_attend(p["q"], p["k"], p["v"], p["W"], p["gate"], L, merge,
+                                        S0=S0, Z0=Z0)
+            for j0 in range(0, p["q"].shape[0], L):
+                blk = slice(j0, j0 + L)
+                ref = ob.attend_bruteforce(p["q"][blk], p["k"][blk], p["v"][blk],
+                                           np.concatenate([kc, p["k"][:j0]]),
+                                           np.concatenate([vc, p["v"][:j0]]), p["W"], p["gate"],
+                                           merge)
+                _close(o[blk], ref, rtol=1e-10, atol=1e-12)
+            K = np.concatenate([kc, p["k"]])
+            V = np.concatenate([vc, p["v"]])
+            H = p["W"].shape[0]
+            for h in range(H):
+                S_ref = sum(np.outer(ob.feature_map(K[t, h], p["W"][h]), V[t, h])
+                            for t in range(K.shape[0]))
+                Z_ref = sum(ob.feature_map(K[t, h], p["W"][h]) for t in range(K.shape[0]))
+                _close(S[h], S_ref, rtol=1e-10, atol=1e-12)
+                _close(Z[h], Z_ref, rtol=1e-10, atol=1e-12)
+
+
+def check_prefill_attend_first_block_is_softmax(ob):
+    """With nothing committed before it, the first block of a prompt is plain
+    softmax attention within the block (SHARED_NORM, any gate): torch's fp64
+    scaled_dot_product_attention."""
+    p = _prompt_problem(8)
+    L = p["L"]
+    o, _, _ = ob.prefill_attend(p["q"], p["k"], p["v"], p["W"], p["gate"], L,
+                                ob.MERGE_SHARED_NORM)
+    _close(o[:L], _sdpa(p["q"][:L], p["k"][:L], p["v"][:L]), rtol=1e-10, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_feature_map_golden,
     check_feature_map_vs_scipy,
@@ -284,4 +342,6 @@ ALL_CHECKS = [
     check_convex_combination,
     check_softmax_kv_vs_sdpa,
     check_softmax_kv_empty_prefix,
+    check_prefill_attend_vs_bruteforce,
+    check_prefill_attend_first_block_is_softmax,
 ]

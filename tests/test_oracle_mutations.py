@@ -92,8 +92,31 @@ def _softmax_kv_no_block(k_prefix, v_prefix, q, k, v, scale=None):
     return _ORIG["softmax_kv_attend"](k_prefix[:-1], v_prefix[:-1], q, k_prefix[-1:], v_prefix[-1:], scale)
 
 
+def _prefill_attend_commit_first(q, k, v, W, gate, L, merge=ob.MERGE_SHARED_NORM, scale=None,
+                                 S0=None, Z0=None):
+    """Commits each block before it attends (the block sees itself twice)."""
+    q, k, v, W = (np.asarray(a, np.float64) for a in (q, k, v, W))
+    T, H, d = q.shape
+    f = W.shape[2]
+    S = np.zeros((H, 2 * f, d)) if S0 is None else np.asarray(S0, np.float64).copy()
+    Z = np.zeros((H, 2 * f)) if Z0 is None else np.asarray(Z0, np.float64).copy()
+    o = np.empty((T, H, d))
+    for j0 in range(0, T, L):
+        blk = slice(j0, j0 + L)
+        S, Z = ob.commit(S, Z, k[blk], v[blk], W)
+        o[blk] = ob.attend(q[blk], k[blk], v[blk], S, Z, W, gate, merge, scale)
+    return o, S, Z
+
+
+def _prefill_attend_ignores_context(q, k, v, W, gate, L, merge=ob.MERGE_SHARED_NORM, scale=None,
+                                    S0=None, Z0=None):
+    """Starts from an empty state even when an earlier context is given."""
+    return _ORIG["prefill_attend"](q, k, v, W, gate, L, merge, scale)
+
+
 _ORIG = {name: getattr(ob, name) for name in
-         ("commit", "sigmoid", "softmax_kv_attend", "feature_map", "_softmax_last", "_scale", "attend")}
+         ("commit", "sigmoid", "softmax_kv_attend", "feature_map", "_softmax_last", "_scale", "attend",
+          "prefill_attend")}
 
 MUTATIONS = {
     "phi halves swapped": {"feature_map": _fm_swapped_halves},
@@ -110,6 +133,8 @@ MUTATIONS = {
     "linear read uses phi(k) of the block": {"attend": _make_attend("phi_of_key")},
     "convex weights swapped": {"attend": _make_attend("convex_swapped")},
     "comparison drops block keys": {"softmax_kv_attend": _softmax_kv_no_block},
+    "prompt block committed before it attends": {"prefill_attend": _prefill_attend_commit_first},
+    "prompt ignores the earlier context": {"prefill_attend": _prefill_attend_ignores_context},
 }
 
 
