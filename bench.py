@@ -753,6 +753,64 @@ def run_psweep(args):
     }
 
 
+def run_prefill_attend(args):
+    """Prompt processing with outputs: 8 prompts x 8,192 tokens, 16 heads,
+    d=128, f=64 (the prompt-ingestion shape), every 32-token block attending
+    to the state of the blocks before it and then committed
+    (hb_prefill_attend, 256 launches of the attend-and-commit kernel)."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    nB, T = 8, 8192
+    cfg = hb.Config(H, D, FH, L)
+    g = inputs.prompt_ingestion(device=device, B=nB, T=T)
+    k = g.tensors["k"].view(nB, T, H, D)
+    v = g.tensors["v"].view(nB, T, H, D)
+    q = inputs.draw(41, (nB, T, H, D), torch.bfloat16, device=device)
+    W = g.tensors["W"]
+    gate = g.tensors["gate"]
+    S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
+    Z = torch.empty((nB, H, F), dtype=torch.float32, device=device)
+    sl = torch.arange(nB, dtype=torch.int32, device=device)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        hb.hb_prefill_attend(cfg, sl, q, k, v, S, Z, W, gate, o=o)
+
+    reps = max(3, min(args.steps, 20))
+    with ClockSampler(0) as clocks:
+        ms = _graph_ms(call, 1, reps, args.warmup, stream)
+    assert hb.hb_get_device_status() == 0
+    tokens = nB * T
+    # the formulation's minimum: read q, k, v, write o and the final state
+    nbytes = 4 * tokens * H * D * 2 + nB * H * (F * D + F) * 4 + H * D * FH * 2
+    # what this implementation moves: each block also reads and writes the
+    # request's state (most of it from L2, the 8 requests' states being 8 MB)
+    state_rw = (T // L) * nB * H * (F * D + F) * 4 * 2
+    peak, kind = _peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {
+        "metric": "prompt processing with outputs: prompt tokens/s", "value": tokens / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "hb_prefill_attend: 8 prompts x 8,192 tokens, 16 heads, d=128, "
+                               "f=64, L=32, from empty states",
+                   "timing": "one call (256 kernel launches) per CUDA graph, replayed",
+                   "l2": "q, k, v, o 1.07 GB > L2"},
+        "roofline": {"kernel": "hb_prefill_attend (k_attend_fast, block by block)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": kind,
+                     "algorithmic_bytes_per_call": nbytes,
+                     "state_bytes_moved_per_call": state_rw, "traffic": None},
+        "gpu_launches": reps * (1 + T // L),
+        "clocks": clocks.summary(),
+    }
+
+
 def cpu_baseline_prefill(max_seconds: float = 15.0, T: int = 256):
     """The oracle's prefill on one 256-token prompt of the same shape."""
     import numpy as np
@@ -868,7 +926,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map", "psweep"],
+    ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map", "psweep",
+                             "prefill_attend"],
                     default="step",
                     help="step: continuous-batching step (default); decode: single-layer "
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
@@ -887,7 +946,8 @@ def main(argv=None):
         if world > 1:
             ap.error("--workload other than step runs on one GPU")
         runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack,
-                  "feature_map": run_feature_map, "psweep": run_psweep}
+                  "feature_map": run_feature_map, "psweep": run_psweep,
+                  "prefill_attend": run_prefill_attend}
         print(json.dumps(runner[args.workload](args)), flush=True)
         return 0
     if world > 1:

@@ -163,6 +163,37 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
                                  hb_stream_t stream);
 
 /*
+ * hb_prefill_attend — a prompt processed block by block with block-hybrid
+ * attention, so that every prompt token also gets its output (gist.science
+ * technical summary, "Methodology: Block-Hybrid Attention / Architecture
+ * Design": exact softmax inside the active block, linear attention over the
+ * committed blocks through S and Z, which change only when a block is
+ * committed). The prompt is cut into seq_len / L blocks; block j is the
+ * active block against the state of blocks 0 .. j - 1 (plus the slot's
+ * existing state when accumulate = 1) and is then committed. This library's
+ * reading of prefill with outputs: the pages run this form when they train
+ * the layers against the softmax teacher; they give no separate prefill
+ * formula.
+ *   slot_idx     [batch] int32, device: request b's state slot (distinct)
+ *   q, k, v      [batch, seq_len, H, d] activation dtype: the prompts
+ *   seq_len      prompt length, a multiple of L (every prompt has it)
+ *   S_pool, Z_pool  the slots' states: zeroed first when accumulate = 0,
+ *                continued from when accumulate = 1; hold the whole
+ *                prompt's commit at the end
+ *   W, gate_logits as in hb_block_attend
+ *   o            [batch, seq_len, H, d] activation dtype, written
+ * Runs as seq_len / L kernel launches on `stream` (each an attend and commit
+ * of one block per request), graph-capturable. seq_len not a multiple of L
+ * returns HB_ERR_INVALID_ARG; a bad slot is flagged as in hb_block_attend.
+ */
+hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch,
+                            const int32_t* slot_idx, const void* q,
+                            const void* k, const void* v, int64_t seq_len,
+                            float* S_pool, float* Z_pool, int32_t num_slots,
+                            const void* W, const float* gate_logits,
+                            int32_t accumulate, void* o, hb_stream_t stream);
+
+/*
  * hb_commit_block — fold a finished block into the state (gist.science
  * technical summary, state-compression bullet: the states change only when a
  * block is committed; pith.science review, "What carries the argument":

@@ -18,6 +18,7 @@ from .hb import (  # noqa: F401
     hb_commit_block,
     hb_feature_map,
     hb_get_device_status,
+    hb_prefill_attend,
     hb_prefill_state,
     hb_prefill_state_noalloc,
     hb_prefill_workspace_size,

@@ -129,10 +129,10 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch, const int32_t* sl
   cudaError_t e = hb::status_word_ptr(&status);
   if (e != cudaSuccess) return HB_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots))
+  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, nullptr, o, status,
-                                                st));
+                                                st, s.L, 0, false));
   return hb::from_cuda(hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                  num_slots, W, gate_logits, o, status, st));
 }
@@ -154,10 +154,10 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int3
   unsigned* status = nullptr;
   if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots))
+  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, commit, o, status,
-                                                st));
+                                                st, s.L, 0, false));
   // other shapes: the attend pass reads every state, then the committing
   // requests fold their block in, in stream order
   cudaError_t e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots,
@@ -165,6 +165,48 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int3
   if (e != cudaSuccess) return HB_ERR_CUDA;
   return hb::from_cuda(hb::launch_commit_masked_generic(s, batch, slot_idx, commit, k, v, W,
                                                         S_pool, Z_pool, num_slots, status, st));
+}
+
+hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                            const void* q, const void* k, const void* v, int64_t seq_len,
+                            float* S_pool, float* Z_pool, int32_t num_slots, const void* W,
+                            const float* gate_logits, int32_t accumulate, void* o,
+                            hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0 || seq_len < 0) return HB_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return HB_ERR_INVALID_ARG;
+  if (seq_len % s.L != 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, S_pool, Z_pool, W, gate_logits})) != HB_OK) return r;
+  if (seq_len > 0 && (r = hb::check_ptrs({q, k, v, o})) != HB_OK) return r;
+  if ((int64_t)batch * seq_len >= ((int64_t)1 << 31)) return HB_ERR_UNSUPPORTED_SHAPE;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (accumulate == 0 &&
+      (e = hb::launch_state_zero(s, batch, slot_idx, S_pool, Z_pool, num_slots, status, st)) !=
+          cudaSuccess)
+    return HB_ERR_CUDA;
+  const bool fast = hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len);
+  for (int64_t row = 0; row < seq_len; row += s.L) {
+    if (fast) {
+      e = hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
+                                 gate_logits, nullptr, o, status, st, (int)seq_len, (int)row,
+                                 true);
+    } else {
+      e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
+                                    gate_logits, o, status, st, seq_len, row);
+      if (e == cudaSuccess)
+        e = hb::launch_commit_rows_generic(s, batch, slot_idx, k, v, seq_len, row, W, S_pool,
+                                           Z_pool, num_slots, status, st);
+    }
+    if (e != cudaSuccess) return hb::from_cuda(e);
+  }
+  return HB_OK;
 }
 
 hb_status hb_commit_block(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,

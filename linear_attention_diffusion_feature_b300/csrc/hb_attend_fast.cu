@@ -98,6 +98,11 @@ enum : int { kUnitValid = 1, kUnitCommit = 2 };  // meta flags of a stage
 struct Maps {
   const uint8_t* qkv[3];  // q, k, v base addresses (L2 prefetch of whole token rows)
   const uint8_t* w;       // W base address
+  // Request b's active block is rows b * rows_per_req + row_base .. + L - 1
+  // of q, k, v and o (rows_per_req = L, row_base = 0 for a decoding step;
+  // the prompt length and the block's offset for chunkwise prompt
+  // processing); commit_all: every request commits (commit_mask unused).
+  int rows_per_req, row_base, commit_all;
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // is safe before the wait. Every load and store of global memory comes
   // after grid_dep_wait().
   if (warp == kProducerWarp && lane == 0) {
-    const size_t qkv_bytes = (size_t)batch * kL * H * kD * 2;
+    const size_t qkv_bytes = (size_t)batch * maps.rows_per_req * H * kD * 2;
     const size_t w_bytes = (size_t)H * kD * kFH * 2;
     if (3 * qkv_bytes + w_bytes <= kPrefetchBudget) {
       const uint8_t* base[4] = {maps.qkv[0], maps.qkv[1], maps.qkv[2], maps.w};
@@ -316,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // innermost. The mask is kept as bits in shared memory.
     uint32_t* mask_bits = reinterpret_cast<uint32_t*>(smem + kOffMaskBits);
     const int mask_words = (batch + 31) >> 5;
-    const bool commit_first = kCommit && mask_words <= kMaskWords;
+    const bool all_commit = kCommit && maps.commit_all != 0;
+    const bool commit_first = kCommit && !all_commit && mask_words <= kMaskWords;
     int n_commit = 0;  // committing requests
     if (commit_first) {
       for (int w = 0; w < mask_words; ++w) {
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    const int commit_units = n_commit * H;
+    const int commit_units = all_commit ? units : n_commit * H;
     // Lane j describes local unit 32 W + j of window W. Its request comes
     // from a per-lane cursor over the mask bits for each flag value (a
     // lane's units have increasing positions, so the cursors only move
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p < commit_units) {
         r = p / H;
         wd.h = p - r * H;
-        wd.b = nth_request(1, r);
+        wd.b = all_commit ? r : nth_request(1, r);
         wd.flags = kUnitCommit;
       } else {
         r = (p - commit_units) / H;
@@ -407,9 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&head_full[s], kHeadBytes);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, b * kL, &head_full[s]);
-          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, b * kL, &head_full[s]);
-          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, b * kL, &head_full[s]);
+          const int row = b * maps.rows_per_req + maps.row_base;
+          tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, row, &head_full[s]);
+          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, row, &head_full[s]);
+          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, row, &head_full[s]);
         }
         tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
       }
@@ -452,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all heads; the CTAs working on its heads at the same time each
       // prefetch a 1/H slice of it, so DRAM reads it as one long run
       const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
-      const size_t off = (size_t)b * kL * H * kD * 2 + (size_t)h * slice;
+      const size_t off =
+          ((size_t)b * maps.rows_per_req + maps.row_base) * H * kD * 2 + (size_t)h * slice;
 #pragma unroll
       for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
     };
@@ -895,7 +903,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint2 pk;
         pk.x = pack_bf16(ov[0], ov[1]);
         pk.y = pack_bf16(ov[2], ov[3]);
-        *reinterpret_cast<uint2*>(o + ((size_t)(b * kL + R) * H + h) * kD + c0 + 4 * t) = pk;
+        const size_t orow = (size_t)b * maps.rows_per_req + maps.row_base + R;
+        *reinterpret_cast<uint2*>(o + (orow * H + h) * kD + c0 + 4 * t) = pk;
       }
     }
 
@@ -965,17 +974,21 @@ int g_num_sms = 0;
 
 bool fast_attend_ok(const Shape& s) { return production_shape(s); }
 
-bool attend_fast_fits(const Shape& s, int batch, int num_slots) {
+bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req) {
   return (int64_t)num_slots * s.H * kF < ((int64_t)1 << 31) &&
-         (int64_t)batch * kL < ((int64_t)1 << 31);
+         (int64_t)batch * rows_per_req < ((int64_t)1 << 31);
 }
 
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
-                               unsigned* status, cudaStream_t st) {
+                               unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
+                               bool commit_all) {
   Maps maps;
+  maps.rows_per_req = rows_per_req;
+  maps.row_base = row_base;
+  maps.commit_all = commit_all ? 1 : 0;
   maps.qkv[0] = static_cast<const uint8_t*>(q);
   maps.qkv[1] = static_cast<const uint8_t*>(k);
   maps.qkv[2] = static_cast<const uint8_t*>(v);
@@ -989,7 +1002,7 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * kL};
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * rows_per_req};
     const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
     const uint32_t box[3] = {64, 1, 32};
     const void* ptrs[3] = {q, k, v};
@@ -1007,7 +1020,7 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto* kernel = commit_mask ? k_attend_fast<true> : k_attend_fast<false>;
+  auto* kernel = (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   if (g_num_sms == 0) {

@@ -39,15 +39,18 @@ bool fast_softmax_kv_ok(const Shape& s);
 
 cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, const void* W,
                                     float* phi, unsigned* status, cudaStream_t st);
-// commit_mask == nullptr: attend only (S_pool and Z_pool are not written).
-// Otherwise request b with commit_mask[b] != 0 also folds its block's k, v
-// into its state slot after its output has used the old state.
-bool attend_fast_fits(const Shape& s, int batch, int num_slots);
+// commit_mask == nullptr and !commit_all: attend only (S_pool and Z_pool are
+// not written). Otherwise request b with commit_mask[b] != 0 (every request,
+// with commit_all) also folds its block's k, v into its state slot after its
+// output has used the old state. Request b's block is rows
+// b * rows_per_req + row_base .. + L - 1 of q, k, v and o.
+bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
-                               unsigned* status, cudaStream_t st);
+                               unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
+                               bool commit_all);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);

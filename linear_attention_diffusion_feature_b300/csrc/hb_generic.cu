@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) k_state_accumulate_generic(
     int H, int d, int f, int L, const int32_t* __restrict__ slot_idx,
     const int32_t* __restrict__ mask, const T* __restrict__ k,
     const T* __restrict__ v, int64_t total_tokens, const int64_t* __restrict__ cu_seqlens,
-    int64_t max_seqlen,
+    int64_t max_seqlen, int64_t row_stride, int64_t row_base,
     const T* __restrict__ W, float* __restrict__ S_pool, float* __restrict__ Z_pool,
     int num_slots, int accumulate, unsigned* status) {
   constexpr int CH = 16;
@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(kThreads) k_state_accumulate_generic(
   if (cu_seqlens) {
     row0 = cu_seqlens[b];
     cnt = cu_seqlens[b + 1] - row0;
-  } else {
-    row0 = (int64_t)b * L;
+  } else {  // block b is rows b * row_stride + row_base .. + L - 1
+    row0 = (int64_t)b * row_stride + row_base;
     cnt = L;
   }
   if (slot < 0 || slot >= num_slots || cnt < 0 || cnt > max_seqlen || row0 < 0 ||
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
     int H, int d, int f, int L, float scale, int merge, const int32_t* __restrict__ slot_idx,
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ S_pool, const float* __restrict__ Z_pool, int num_slots,
-    const T* __restrict__ W, const float* __restrict__ gate, T* __restrict__ o, unsigned* status) {
+    const T* __restrict__ W, const float* __restrict__ gate, T* __restrict__ o, unsigned* status,
+    int64_t row_stride, int64_t row_base) {
   const int F = 2 * f;
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int slot = slot_idx[b];
@@ -197,7 +198,8 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
   float* s_den = s_P + L;                     // phi(q)^T Z
 
   const size_t tok_stride = (size_t)H * d;
-  const size_t base = ((size_t)b * L * H + h) * d;
+  // request b's block: rows b * row_stride + row_base .. + L - 1
+  const size_t base = (((size_t)b * row_stride + row_base) * H + h) * d;
   for (int i = tid; i < L * d; i += kThreads) {
     const int t = i / d, a = i - t * d;
     const size_t g = base + t * tok_stride + a;
@@ -447,7 +449,9 @@ static cudaError_t state_accumulate_generic(const Shape& s, int batch, const int
                                             const int64_t* cu_seqlens, int64_t max_seqlen,
                                             const void* W, float* S_pool, float* Z_pool,
                                             int num_slots, int accumulate, unsigned* status,
-                                            cudaStream_t st) {
+                                            cudaStream_t st, int64_t row_stride = -1,
+                                            int64_t row_base = 0) {
+  if (row_stride < 0) row_stride = s.L;
   constexpr int CH = 16;
   const size_t smem =
       sizeof(float) * ((size_t)s.d * s.f + 2 * CH * s.d + CH * s.f + CH * s.F);
@@ -459,14 +463,14 @@ static cudaError_t state_accumulate_generic(const Shape& s, int batch, const int
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, mask, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, total_tokens, cu_seqlens, maxlen,
-                                     (const __nv_bfloat16*)W, S_pool, Z_pool, num_slots,
-                                     accumulate, status);
+                                     row_stride, row_base, (const __nv_bfloat16*)W, S_pool, Z_pool,
+                                     num_slots, accumulate, status);
   } else {
     auto* fn = k_state_accumulate_generic<float>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, slot_idx, mask, (const float*)k,
                                      (const float*)v, total_tokens, cu_seqlens, maxlen,
-                                     (const float*)W,
+                                     row_stride, row_base, (const float*)W,
                                      S_pool, Z_pool, num_slots, accumulate, status);
   }
   return cudaGetLastError();
@@ -491,10 +495,22 @@ cudaError_t launch_commit_masked_generic(const Shape& s, int batch, const int32_
                                   s.L, W, S_pool, Z_pool, num_slots, 1, status, st);
 }
 
+cudaError_t launch_commit_rows_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                       const void* k, const void* v, int64_t rows_per_req,
+                                       int64_t row_base, const void* W, float* S_pool,
+                                       float* Z_pool, int num_slots, unsigned* status,
+                                       cudaStream_t st) {
+  return state_accumulate_generic(s, batch, slot_idx, nullptr, k, v, (int64_t)batch * rows_per_req,
+                                  nullptr, s.L, W, S_pool, Z_pool, num_slots, 1, status, st,
+                                  rows_per_req, row_base);
+}
+
 cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot_idx,
                                   const void* q, const void* k, const void* v, const float* S_pool,
                                   const float* Z_pool, int num_slots, const void* W,
-                                  const float* gate, void* o, unsigned* status, cudaStream_t st) {
+                                  const float* gate, void* o, unsigned* status, cudaStream_t st,
+                                  int64_t rows_per_req, int64_t row_base) {
+  if (rows_per_req < 0) rows_per_req = s.L;
   const int scr_ld = s.L > s.f ? s.L : s.f;
   const size_t smem = sizeof(float) * ((size_t)3 * s.L * s.d + s.d * s.f + s.L * s.F +
                                        s.L * scr_ld + s.F + 3 * s.L);
@@ -506,13 +522,15 @@ cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, s.scale, s.merge, slot_idx,
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, S_pool, Z_pool, num_slots,
-                                     (const __nv_bfloat16*)W, gate, (__nv_bfloat16*)o, status);
+                                     (const __nv_bfloat16*)W, gate, (__nv_bfloat16*)o, status,
+                                     rows_per_req, row_base);
   } else {
     auto* fn = k_attend_generic<float>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, s.scale, s.merge, slot_idx,
                                      (const float*)q, (const float*)k, (const float*)v, S_pool,
-                                     Z_pool, num_slots, (const float*)W, gate, (float*)o, status);
+                                     Z_pool, num_slots, (const float*)W, gate, (float*)o, status,
+                                     rows_per_req, row_base);
   }
   return cudaGetLastError();
 }

@@ -93,10 +93,13 @@ __device__ __forceinline__ float merge_out(int merge, float U, float P, float m,
 // tensor-core kernels are not built for.
 cudaError_t launch_feature_map_generic(const Shape& s, int64_t n, const void* x, const void* W,
                                        float* phi, cudaStream_t st);
+// Request b's block is rows b * rows_per_req + row_base .. + L - 1 of q, k, v
+// and o (rows_per_req < 0 means L).
 cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot_idx,
                                   const void* q, const void* k, const void* v, const float* S_pool,
                                   const float* Z_pool, int num_slots, const void* W,
-                                  const float* gate, void* o, unsigned* status, cudaStream_t st);
+                                  const float* gate, void* o, unsigned* status, cudaStream_t st,
+                                  int64_t rows_per_req = -1, int64_t row_base = 0);
 // commit (cu_seqlens == nullptr: request b owns rows [b*L, b*L+L)) and prefill.
 cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int32_t* slot_idx,
                                             const void* k, const void* v, int64_t total_tokens,
@@ -109,6 +112,12 @@ cudaError_t launch_commit_masked_generic(const Shape& s, int batch, const int32_
                                          const int32_t* mask, const void* k, const void* v,
                                          const void* W, float* S_pool, float* Z_pool,
                                          int num_slots, unsigned* status, cudaStream_t st);
+// commit of every request's block at rows b * rows_per_req + row_base .. + L - 1
+cudaError_t launch_commit_rows_generic(const Shape& s, int batch, const int32_t* slot_idx,
+                                       const void* k, const void* v, int64_t rows_per_req,
+                                       int64_t row_base, const void* W, float* S_pool,
+                                       float* Z_pool, int num_slots, unsigned* status,
+                                       cudaStream_t st);
 cudaError_t launch_state_zero(const Shape& s, int batch, const int32_t* slot_idx, float* S_pool,
                               float* Z_pool, int num_slots, unsigned* status, cudaStream_t st);
 cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_cache,

@@ -157,6 +157,33 @@ def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, ga
     return o
 
 
+def hb_prefill_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits,
+                      accumulate: bool = False, o=None, stream=None) -> torch.Tensor:
+    """Prompts q/k/v [B, T, H, d] (T a multiple of L) processed block by
+    block: block j attends against the state of blocks 0 .. j-1 (plus the
+    slot's state when accumulate), then is committed. Returns o [B, T, H, d];
+    the slots end up holding the whole prompt's state."""
+    B = slot_idx.shape[0]
+    H, d, f = cfg.num_heads, cfg.head_dim, cfg.feat_half
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    T = q.shape[1] if q.dim() == 4 else -1
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, T, H, d))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, T, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_prefill_attend(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                                 _ptr(v), T, _ptr(S_pool), _ptr(Z_pool), num_slots, _ptr(W),
+                                 _ptr(gate_logits), 1 if accumulate else 0, _ptr(o),
+                                 _stream(stream)),
+           "hb_prefill_attend")
+    return o
+
+
 def hb_commit_block(cfg: Config, slot_idx, k, v, W, S_pool, Z_pool, stream=None) -> None:
     """S += sum_t phi(k_t) v_t^T, Z += sum_t phi(k_t) for each listed slot."""
     B = slot_idx.shape[0]

@@ -126,6 +126,26 @@ def test_prefill_checks(lib):
                                     A, need - 16, None) == 7
 
 
+def test_prefill_attend_checks(lib):
+    c = _cfg()
+    # args: cfg, batch, slot_idx, q, k, v, seq_len, S, Z, num_slots, W, gate, accumulate, o, stream
+    # prompt length not a multiple of the block length (32)
+    assert lib.hb_prefill_attend(ctypes.byref(c), 1, A, A, A, A, 33, A, A, 1, A, A, 0, A,
+                                 None) == 1
+    assert lib.hb_prefill_attend(ctypes.byref(c), 1, A, A, A, A, -32, A, A, 1, A, A, 0, A,
+                                 None) == 1
+    # bad accumulate flag, missing q, misaligned o
+    assert lib.hb_prefill_attend(ctypes.byref(c), 1, A, A, A, A, 64, A, A, 1, A, A, 2, A,
+                                 None) == 1
+    assert lib.hb_prefill_attend(ctypes.byref(c), 1, A, None, A, A, 64, A, A, 1, A, A, 0, A,
+                                 None) == 1
+    assert lib.hb_prefill_attend(ctypes.byref(c), 1, A, A, A, A, 64, A, A, 1, A, A, 0, M,
+                                 None) == 3
+    # batch 0 is a no-op
+    assert lib.hb_prefill_attend(ctypes.byref(c), 0, None, None, None, None, 64, None, None, 0,
+                                 None, None, 0, None, None) == 0
+
+
 def test_softmax_kv_checks(lib):
     c = _cfg()
     assert lib.hb_softmax_kv_attend(ctypes.byref(c), 1, A, A, 8, None, 8, A, A, A, A, None, 0,
