@@ -182,9 +182,11 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
  *                prompt's commit at the end
  *   W, gate_logits as in hb_block_attend
  *   o            [batch, seq_len, H, d] activation dtype, written
- * Runs as seq_len / L kernel launches on `stream` (each an attend and commit
- * of one block per request), graph-capturable. seq_len not a multiple of L
- * returns HB_ERR_INVALID_ARG; a bad slot is flagged as in hb_block_attend.
+ * Asynchronous on `stream` and graph-capturable (a state reset when
+ * accumulate = 0, then one launch in which each (request, head) walks its
+ * blocks in order with the state kept on chip; other shapes take one attend
+ * and one commit launch per block). seq_len not a multiple of L returns
+ * HB_ERR_INVALID_ARG; a bad slot is flagged as in hb_block_attend.
  */
 hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch,
                             const int32_t* slot_idx, const void* q,

@@ -191,19 +191,20 @@ hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch, const int32_t* 
       (e = hb::launch_state_zero(s, batch, slot_idx, S_pool, Z_pool, num_slots, status, st)) !=
           cudaSuccess)
     return HB_ERR_CUDA;
-  const bool fast = hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len);
+  if (seq_len == 0) return HB_OK;
+  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len))
+    // one CTA per (request, head) walks the prompt's blocks with the state
+    // kept on chip
+    return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
+                                                num_slots, W, gate_logits, nullptr, o, status,
+                                                st, (int)seq_len, 0, true, true));
+  // other shapes: an attend and a commit launch per block, in stream order
   for (int64_t row = 0; row < seq_len; row += s.L) {
-    if (fast) {
-      e = hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
-                                 gate_logits, nullptr, o, status, st, (int)seq_len, (int)row,
-                                 true);
-    } else {
-      e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
-                                    gate_logits, o, status, st, seq_len, row);
-      if (e == cudaSuccess)
-        e = hb::launch_commit_rows_generic(s, batch, slot_idx, k, v, seq_len, row, W, S_pool,
-                                           Z_pool, num_slots, status, st);
-    }
+    e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
+                                  gate_logits, o, status, st, seq_len, row);
+    if (e == cudaSuccess)
+      e = hb::launch_commit_rows_generic(s, batch, slot_idx, k, v, seq_len, row, W, S_pool,
+                                         Z_pool, num_slots, status, st);
     if (e != cudaSuccess) return hb::from_cuda(e);
   }
   return HB_OK;

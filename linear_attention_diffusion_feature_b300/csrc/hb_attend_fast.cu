@@ -93,7 +93,7 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
 enum { kSumP = 0, kSumM, kDenP, kDenM, kSumS, kSumPK, kSumMK };
-enum : int { kUnitValid = 1, kUnitCommit = 2 };  // meta flags of a stage
+enum : int { kUnitValid = 1, kUnitCommit = 2, kUnitLast = 4 };  // meta flags of a stage
 
 struct Maps {
   const uint8_t* qkv[3];  // q, k, v base addresses (L2 prefetch of whole token rows)
@@ -125,10 +125,16 @@ __device__ __forceinline__ uint32_t v_off(int key, int n) {
                     (n & 7) * 2);
 }
 
+// kSeq = true (with kCommit): one CTA per (request, head) runs the blocks of
+// a prompt in order (rows j L .. j L + L - 1 of rows_per_req), each block
+// attending to the state left by the blocks before it and then committed.
+// The state is loaded once into the first stage's S and Z buffers, updated
+// there in place after every block, and stored after the last one; only q,
+// k, v and W_h go through the two-stage ring.
 // kCommit = false: attend only (commit_mask is ignored; S_pool and Z_pool are
 // not written). kCommit = true: requests with commit_mask[b] != 0 also fold
 // their block into the state after their output has been formed.
-template <bool kCommit>
+template <bool kCommit, bool kSeq = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
                   int merge, const int32_t* __restrict__ slot_idx,
@@ -204,6 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dep_wait();
   grid_dep_launch();
+  // units of this CTA: every gridDim.x-th (request, head) unit, or in the
+  // sequential mode the blocks of its (request, head)
+  const int n_units_cta =
+      kSeq ? maps.rows_per_req / kL
+           : ((int)blockIdx.x < units ? (units - (int)blockIdx.x + (int)gridDim.x - 1) /
+                                            (int)gridDim.x
+                                      : 0);
 
   if (warp == kCoefWarp) {
     // ------------------------------------------------- merge coefficients
@@ -211,9 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (U = sum_j e^{s_ij - m} v_j; num+- the contractions of the unnormalised
     // halves of phi(q) with S), from the row sums the consumers leave in the
     // stage, while the consumers run the state contraction.
-    int i = 0;
     uint32_t su_phase[2] = {0u, 0u};  // parity of s_updated per stage
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+    for (int i = 0; i < n_units_cta; ++i) {
       const int s = i & 1, n = i >> 1;
       if (!mbar_wait(&sums_ready[s], n & 1)) {
         if (lane == 0) atomicOr(status, kStatusTimeout);
@@ -268,7 +280,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&fin_ready[s]);
-      if (kCommit && (meta[s] & kUnitCommit)) {
+      if (kSeq) {
+        // the prompt's last block: store the state once the consumers have
+        // updated it; every block: the row sums have been read
+        if (meta[s] & kUnitLast) {
+          const bool ok = mbar_wait(&s_updated[s], su_phase[s]);
+          su_phase[s] ^= 1u;
+          if (lane == 0) {
+            if (ok) {
+              const int uslot = meta[2 + s];
+              const int row = (uslot * H + h) * kF;
+#pragma unroll
+              for (int bx = 0; bx < 4; ++bx)
+                tma_store_2d(&maps.S, 32 * bx, row, smem + kOffS + bx * 16384);
+              bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, smem + kOffZ, kF * 4);
+              bulk_commit();
+              bulk_wait_read();
+            } else {
+              atomicOr(status, kStatusTimeout);
+            }
+          }
+        }
+        if (lane == 0) mbar_arrive(&empty[s]);
+      } else if (kCommit && (meta[s] & kUnitCommit)) {
         // the consumers have written the new S and Z into the stage: store
         // them (TMA), and hand the stage back on their behalf once the store
         // has read it
@@ -312,7 +346,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.W);
     }
     const int first = blockIdx.x, stride = gridDim.x;
-    const int n_local = first < units ? (units - first + stride - 1) / stride : 0;
+    const int n_local = n_units_cta;
+    if (kSeq) {
+      // this CTA's (request, head); its blocks in order, the state with the
+      // first one only
+      const int b = (int)blockIdx.x / H, h = (int)blockIdx.x - b * H;
+      const int slot = slot_idx[b];
+      const bool bad = slot < 0 || slot >= num_slots;
+      if (lane == 0 && bad) atomicOr(status, kStatusBounds);
+      const size_t slice = (size_t)kL * kD * 2;
+      for (int i = 0; i < n_local; ++i) {
+        const int s = i & 1, n = i >> 1;
+        bool ok = true;
+        if (lane == 0 && n > 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          if (lane == 0) atomicOr(status, kStatusTimeout);
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* st = smem + s * kStageStride;
+          const int row = b * maps.rows_per_req + i * kL;
+          mbar_expect_tx(&head_full[s], kHeadBytes);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, row, &head_full[s]);
+            tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, row, &head_full[s]);
+            tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, row, &head_full[s]);
+          }
+          tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
+          meta[4 + s] = b;
+          meta[6 + s] = h;
+          if (bad) {
+            meta[s] = 0;
+            mbar_arrive(&head_full[s]);
+            mbar_arrive(&s_full[s]);
+          } else {
+            meta[s] = kUnitValid | kUnitCommit | (i == n_local - 1 ? kUnitLast : 0);
+            meta[2 + s] = slot;
+            if (i == 0) {
+              mbar_expect_tx(&head_full[s], 512);
+              bulk_load(smem + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &head_full[s]);
+              mbar_arrive(&head_full[s]);
+              mbar_arrive_expect_tx(&s_full[s], kSBytes);
+              const int srow = (slot * H + h) * kF;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(smem + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
+            } else {
+              mbar_arrive(&head_full[s]);
+              mbar_arrive(&s_full[s]);
+            }
+          }
+          if (i + 2 < n_local) {
+            // the block two ahead: its rows of all heads are contiguous, so
+            // the CTAs of this request each prefetch a 1/H slice of them
+            const size_t off = ((size_t)b * maps.rows_per_req + (size_t)(i + 2) * kL) * H * kD * 2 +
+                               (size_t)h * slice;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
+          }
+        }
+        __syncwarp();
+      }
+      return;
+    }
     // Unit schedule. Position p = first + i * stride of the grid-wide order
     // is this CTA's i-th unit. Committing requests are heavier (their state
     // is also updated and stored), so in the committing variant their units
@@ -516,11 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int i = 0;
   bool aborted = false, late_fail = false;
   uint32_t cm_phase = 0;  // parity of ds_full for the next committing unit
-  for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+  for (; i < n_units_cta; ++i) {
     const int s = i & 1, n = i >> 1;
     const bool head_ok = mbar_wait(&head_full[s], n & 1);
     uint8_t* st = smem + s * kStageStride;
-    const uint32_t sS = smem_u32(st + kOffS);
+    // the sequential mode keeps one state, in the first stage's buffers
+    const uint32_t sS = smem_u32(kSeq ? smem + kOffS : st + kOffS);
     const uint32_t sQ = smem_u32(st + kOffQ);
     const uint32_t sK = smem_u32(st + kOffK);
     const uint32_t sV = smem_u32(st + kOffV);
@@ -528,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sPhi = smem_u32(st + kOffPhi);
     const uint32_t sP = smem_u32(st + kOffP);
     float* sums = reinterpret_cast<float*>(st + kOffSums);  // [7][32][4]
-    float* sZ = reinterpret_cast<float*>(smem + kOffZ + s * 512);
+    float* sZ = reinterpret_cast<float*>(smem + kOffZ + (kSeq ? 0 : s * 512));
     const int b = meta[4 + s], h = meta[6 + s];
     const int R0 = 16 * mt + g, R1 = R0 + 8;
     // stage flags, valid once the head has landed (the producer writes them
@@ -874,8 +972,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the stage is no longer read: hand it back to the producer (a
     // committing unit keeps it until its new S has been stored)
+    if (kSeq && cm) {
+      // the stage's V and phi(k) are read by the dS MMA; once it is done,
+      // the stage (q, k, v, W_h) is free: the state lives elsewhere
+      const bool ds_ok = mbar_wait(ds_full, cm_phase);
+      cm_phase ^= 1u;
+      if (!ds_ok) {
+        late_fail = true;
+        if (lane == 0) atomicOr(status, kStatusTimeout);
+      }
+    }
     __syncwarp();
-    if (lane == 0 && !cm) mbar_arrive(&empty[s]);
+    if (lane == 0 && (kSeq || !cm)) mbar_arrive(&empty[s]);
     if (!s_ok) {
       late_fail = true;  // voted on at the next unit's first barrier
       if (lane == 0) atomicOr(status, kStatusTimeout);
@@ -903,7 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint2 pk;
         pk.x = pack_bf16(ov[0], ov[1]);
         pk.y = pack_bf16(ov[2], ov[3]);
-        const size_t orow = (size_t)b * maps.rows_per_req + maps.row_base + R;
+        const size_t orow =
+            (size_t)b * maps.rows_per_req + (kSeq ? i * kL : maps.row_base) + R;
         *reinterpret_cast<uint2*>(o + (orow * H + h) * kD + c0 + 4 * t) = pk;
       }
     }
@@ -917,11 +1026,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns 64 (w / 4) .. 64 (w / 4) + 63, added to the staged old S,
       // once every warp's state contraction has finished reading it
       named_bar_sync(1, kConsumers);
-      const bool ds_ok = mbar_wait(ds_full, cm_phase);
-      cm_phase ^= 1u;
-      if (!ds_ok) {
-        late_fail = true;
-        if (lane == 0) atomicOr(status, kStatusTimeout);
+      if (!kSeq) {
+        const bool ds_ok = mbar_wait(ds_full, cm_phase);
+        cm_phase ^= 1u;
+        if (!ds_ok) {
+          late_fail = true;
+          if (lane == 0) atomicOr(status, kStatusTimeout);
+        }
       }
       tc_fence_after();
       const int F = 32 * (warp & 3) + lane;
@@ -944,15 +1055,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       if (threadIdx.x < kF) sZ[threadIdx.x] += zpart[threadIdx.x] + zpart[128 + threadIdx.x];
       // the coefficient warp stores the new state and releases the stage
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_updated[s]);
+      // (sequential mode: stores it after the prompt's last block)
+      if (!kSeq || (flags & kUnitLast)) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_updated[s]);
+      }
     }
   }
   if (aborted && threadIdx.x == 0) {
     // let the copies of this unit and the next, if issued, land before the
     // CTA exits (each wait is bounded too)
-    for (int j = i; j <= i + 1 && blockIdx.x + j * gridDim.x < units; ++j) {
+    for (int j = i; j <= i + 1 && j < n_units_cta; ++j) {
       mbar_wait(&head_full[j & 1], (j >> 1) & 1);
       mbar_wait(&s_full[j & 1], (j >> 1) & 1);
     }
@@ -984,7 +1098,7 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all) {
+                               bool commit_all, bool sequential) {
   Maps maps;
   maps.rows_per_req = rows_per_req;
   maps.row_base = row_base;
@@ -1020,7 +1134,8 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto* kernel = (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
+  auto* kernel = sequential ? k_attend_fast<true, true>
+                 : (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   if (g_num_sms == 0) {
@@ -1031,7 +1146,9 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
     g_num_sms = n;
   }
   const int units = batch * s.H;
-  const int grid = units < g_num_sms ? units : g_num_sms;
+  // persistent grid over the units, or one CTA per (request, head) walking
+  // its prompt's blocks in order
+  const int grid = sequential ? units : (units < g_num_sms ? units : g_num_sms);
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, maps, batch, s.H,
                     num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
                     const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o),

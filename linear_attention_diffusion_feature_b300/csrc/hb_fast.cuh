@@ -43,14 +43,17 @@ cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, co
 // not written). Otherwise request b with commit_mask[b] != 0 (every request,
 // with commit_all) also folds its block's k, v into its state slot after its
 // output has used the old state. Request b's block is rows
-// b * rows_per_req + row_base .. + L - 1 of q, k, v and o.
+// b * rows_per_req + row_base .. + L - 1 of q, k, v and o. sequential: one
+// CTA per (request, head) runs all rows_per_req / L blocks of the request in
+// order (each attends to the state left by the ones before, then commits;
+// row_base and commit_mask unused).
 bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all);
+                               bool commit_all, bool sequential = false);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);
