@@ -803,7 +803,8 @@ def run_prefill_attend(args):
         "roofline": {"kernel": "hb_prefill_attend (k_attend_fast, sequential mode)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": kind,
-                     "algorithmic_bytes_per_call": nbytes, "traffic": None},
+                     "algorithmic_bytes_per_call": nbytes,
+                     "traffic": _traffic("hb_prefill_attend")},
         "gpu_launches": reps * 2,
         "clocks": clocks.summary(),
     }
