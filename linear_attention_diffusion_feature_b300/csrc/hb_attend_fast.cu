@@ -422,11 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool commit_first = kCommit && !all_commit && mask_words <= kMaskWords;
     int n_commit = 0;  // committing requests
     if (commit_first) {
-      for (int w = 0; w < mask_words; ++w) {
-        const int j = 32 * w + lane;
-        const uint32_t bits = __ballot_sync(0xffffffffu, j < batch && commit_mask[j] != 0);
-        if (lane == 0) mask_bits[w] = bits;
-        n_commit += __popc(bits);
+      // eight words per round, their loads issued back to back, so the scan
+      // costs one memory round trip for batches up to 256
+      for (int w0 = 0; w0 < mask_words; w0 += 8) {
+        int f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 32 * (w0 + j) + lane;
+          f[j] = (w0 + j < mask_words && r < batch) ? commit_mask[r] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t bits = __ballot_sync(0xffffffffu, f[j] != 0);
+          if (lane == 0 && w0 + j < mask_words) mask_bits[w0 + j] = bits;
+          n_commit += __popc(bits);
+        }
       }
       __syncwarp();
     }
@@ -857,8 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int R = hr ? R1 : R0;
         const float4 a = *reinterpret_cast<const float4*>(sums + (kSumPK * 32 + R) * 4);
         const float4 c = *reinterpret_cast<const float4*>(sums + (kSumMK * 32 + R) * 4);
-        ip[hr] = 1.f / ((a.x + a.y) + (a.z + a.w));
-        im[hr] = 1.f / ((c.x + c.y) + (c.z + c.w));
+        ip[hr] = rcp_approx((a.x + a.y) + (a.z + a.w));  // ~1e-7 relative
+        im[hr] = rcp_approx((c.x + c.y) + (c.z + c.w));
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
