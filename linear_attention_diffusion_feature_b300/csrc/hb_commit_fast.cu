@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     named_bar_sync(1, 128);
     sp = xsp[tok] + xsp[32 + tok] + xsp[64 + tok] + xsp[96 + tok];
     sm = xsm[tok] + xsm[32 + tok] + xsm[64 + tok] + xsm[96 + tok];
-    const float ip = 1.f / sp, im = 1.f / sm;
+    const float ip = rcp_approx(sp), im = rcp_approx(sm);  // sums >= 1 (max term e^0)
     // phi columns 16q..16q+15 of each half: two 16-byte chunks per atom row
     const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
 #pragma unroll

@@ -395,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(hbar, 256);
       sp = (xsp[tok] + xsp[128 + tok]) + (xsp[256 + tok] + xsp[384 + tok]);
       sm = (xsm[tok] + xsm[128 + tok]) + (xsm[256 + tok] + xsm[384 + tok]);
-      const float ip = live ? 1.f / sp : 0.f, im = live ? 1.f / sm : 0.f;
+      // (sp, sm >= 1: each sum holds its row maximum term e^0)
+      const float ip = live ? rcp_approx(sp) : 0.f, im = live ? rcp_approx(sm) : 0.f;
       if (ok && c >= 1) ok = mbar_wait(&bar[kPhiEmptyA + half_id], (c - 1) & 1);
       if (used) {
         // phi columns 16 sub .. 16 sub + 15 of each half: two 16-byte chunks
