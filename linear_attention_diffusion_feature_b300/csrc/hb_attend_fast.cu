@@ -22,9 +22,10 @@
 //   * launched with programmatic stream serialization: barrier set-up and
 //     TMEM allocation overlap the previous kernel's tail;
 //   * the producer reads slot indices ahead, prefetches the tiles of the
-//     units two steps ahead into L2, and issues unit i+1's loads while the
-//     consumers compute unit i; consumers release a stage through a third
-//     mbarrier as soon as S and V have been read;
+//     next unit into L2 (deeper prefetch measured slower: it lengthens the
+//     DRAM queue the TMA loads wait in), and issues unit i+1's loads while
+//     the consumers compute unit i; consumers release a stage through a
+//     third mbarrier as soon as S and V have been read;
 //   * once q and k have been used their bytes hold the unit's feature map,
 //     block probabilities and row sums;
 //   * all four contractions (qW, qk^T, phi(q)S, PV) run on bf16 mma.sync with
@@ -335,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; lane 0 issues the copies. A unit's q, k,
     // v and W_h do not depend on its state slot, so the first unit's are
-    // issued before its slot index is read; later units' slots are read
-    // three units ahead, and each unit's tiles are prefetched into L2 two
-    // units before their TMA load is issued.
+    // issued before its slot index is read; the slots of later units are
+    // read 32 at a time, a window ahead, and each unit's tiles are
+    // prefetched into L2 one unit before their TMA load is issued.
     if (lane == 0) {
       prefetch_tmap(&maps.S);
       prefetch_tmap(&maps.q);
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Both stages are free at the start. Unit 0 goes out first and whole;
     // unit 1's head follows, but its state only once unit 0's has landed,
     // so that DRAM serves unit 0 first and its computation starts early.
-    // Later units are prefetched into L2 two units ahead of their TMA loads.
+    // Later units are prefetched into L2 one unit ahead of their TMA loads.
     if (n_local > 0) {
       issue_head(0);
       issue_state(0);
@@ -601,8 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issue_head(i);
       issue_state(i);
-      if (i == 2 && i + 1 < n_local) l2_prefetch(i + 1);
-      if (i + 2 < n_local) l2_prefetch(i + 2);
+      if (i + 1 < n_local) l2_prefetch(i + 1);
     }
     return;
   }
