@@ -74,6 +74,22 @@ hb_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HB_OK : HB_ERR_CU
 
 }  // namespace
 
+cudaError_t current_sm_count(int* n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::map<int, int> counts;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& c = counts[dev];
+  if (c == 0 &&
+      (e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+    c = 0;
+    return e;
+  }
+  *n = c;
+  return cudaSuccess;
+}
+
 cudaError_t ensure_smem_attr(const void* fn, int bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
   int dev = 0;

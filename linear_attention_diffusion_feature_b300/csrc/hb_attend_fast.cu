@@ -1092,8 +1092,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int g_num_sms = 0;
-
 }  // namespace
 
 bool fast_attend_ok(const Shape& s) { return production_shape(s); }
@@ -1148,17 +1146,12 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                  : (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (g_num_sms == 0) {
-    int dev = 0, n = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-    g_num_sms = n;
-  }
+  int num_sms = 0;
+  if ((e = current_sm_count(&num_sms)) != cudaSuccess) return e;
   const int units = batch * s.H;
   // persistent grid over the units, or one CTA per (request, head) walking
   // its prompt's blocks in order
-  const int grid = sequential ? units : (units < g_num_sms ? units : g_num_sms);
+  const int grid = sequential ? units : (units < num_sms ? units : num_sms);
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, maps, batch, s.H,
                     num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
                     const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o),

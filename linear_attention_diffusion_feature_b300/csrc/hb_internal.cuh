@@ -130,5 +130,7 @@ cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_c
 // device to at least `bytes` (remembered per kernel and device, so the
 // runtime is asked only when the value has to grow).
 cudaError_t ensure_smem_attr(const void* fn, int bytes);
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t current_sm_count(int* n);
 
 }  // namespace hb

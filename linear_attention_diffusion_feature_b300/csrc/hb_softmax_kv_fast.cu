@@ -361,16 +361,8 @@ __global__ void __launch_bounds__(256) k_softmax_kv_combine(const __grid_constan
 }
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      return 148;
-  }
-  return n;
+  int n = 0;
+  return current_sm_count(&n) == cudaSuccess && n > 0 ? n : 148;
 }
 
 // Splits per (request, head): about one wave of two CTAs per SM, at most one
