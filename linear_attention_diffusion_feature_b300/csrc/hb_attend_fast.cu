@@ -18,9 +18,17 @@
 //     SWIZZLE_128B boxes); the feature map and block softmax run on the head
 //     while S is still arriving;
 //   * in the committing variant, units of committing requests come first in
-//     the grid-wide order, so that every CTA gets one or two of them;
-//   * launched with programmatic stream serialization: barrier set-up and
-//     TMEM allocation overlap the previous kernel's tail;
+//     the grid-wide order, so that every CTA gets one or two of them; such a
+//     unit also forms phi(k) as bf16 hi + lo, runs dS = phi(k)^T V on
+//     tcgen05 into TMEM during its state contraction, adds dS into the
+//     staged S once every warp has read it, and the coefficient warp
+//     TMA-stores the new S and Z;
+//   * in the sequential mode (prompts with outputs) one CTA per
+//     (request, head) walks the blocks of its prompt in order, the state
+//     kept in the first stage's buffers and stored after the last block;
+//   * launched with programmatic stream serialization: barrier set-up, TMEM
+//     allocation and an L2 prefetch of the step's q, k, v and W overlap the
+//     previous kernel's tail;
 //   * the producer reads slot indices ahead, prefetches the tiles of the
 //     next unit into L2 (deeper prefetch measured slower: it lengthens the
 //     DRAM queue the TMA loads wait in), and issues unit i+1's loads while
