@@ -13,7 +13,9 @@ from .block_hybrid import (  # noqa: F401
     attend_bruteforce,
     commit,
     feature_map,
+    gather_pages,
     prefill,
     sigmoid,
     softmax_kv_attend,
+    softmax_kv_attend_paged,
 )

@@ -276,3 +276,30 @@ def softmax_kv_attend(k_prefix, v_prefix, q, k, v, scale=None):
         p = _softmax_last(s)
         o[:, h, :] = p @ V[:, h, :]
     return o
+
+
+def gather_pages(pages, page_ids, P):
+    """The first P tokens of one request from a paged cache, in token order.
+
+    A paged cache stores a request's tokens in fixed-size pages drawn from a
+    shared pool (PagedAttention, Kwon et al., SOSP 2023); [GIST] "Key
+    Contributions", implementation bullet: the method's serving kernel keeps
+    the fixed-size state next to such paged KV caches. Token t of the request
+    sits in slot t mod p of page page_ids[t // p], where p is the page size.
+    pages [num_pages, p, H, d]; page_ids lists the request's pages in order.
+    Slots past token P - 1 are never read.
+    """
+    pages = _f64(pages)
+    p = pages.shape[1]
+    rows = [pages[int(page_ids[t // p]), t % p] for t in range(int(P))]
+    if not rows:
+        return np.zeros((0,) + pages.shape[2:])
+    return np.stack(rows)
+
+
+def softmax_kv_attend_paged(k_pages, v_pages, page_ids, P, q, k, v, scale=None):
+    """softmax_kv_attend over a paged KV cache: the request's P cached keys
+    and values are gathered from their pages (gather_pages), then the
+    comparison softmax is applied to them and the active block unchanged."""
+    return softmax_kv_attend(gather_pages(k_pages, page_ids, P),
+                             gather_pages(v_pages, page_ids, P), q, k, v, scale)

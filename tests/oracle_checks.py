@@ -267,6 +267,49 @@ def check_softmax_kv_empty_prefix(ob):
     _close(o, _sdpa(p["q"], p["k"], p["v"]), rtol=1e-10)
 
 
+
+def _paged_problem(seed, P=11, p=4, n_junk=3):
+    """A request's P cached tokens cut into pages of p slots, the pages put at
+    shuffled positions of a pool that also holds unused pages. Unused pages
+    and the slots past token P - 1 hold NaN, so reading any of them shows."""
+    g = np.random.default_rng(seed)
+    prob = _rand_problem(seed, N=P)
+    H, d = prob["q"].shape[1:]
+    n_pages = -(-P // p)
+    order = g.permutation(n_pages + n_junk)
+    page_ids = order[:n_pages]
+    k_pages = np.full((n_pages + n_junk, p, H, d), np.nan)
+    v_pages = np.full((n_pages + n_junk, p, H, d), np.nan)
+    for t in range(P):
+        k_pages[page_ids[t // p], t % p] = prob["k_prev"][t]
+        v_pages[page_ids[t // p], t % p] = prob["v_prev"][t]
+    return prob, k_pages, v_pages, page_ids
+
+
+def check_paged_gather_layout(ob):
+    """Token t of a request is slot t mod p of its (t // p)-th page: the
+    gather puts the scattered tokens back in order, exactly."""
+    prob, k_pages, v_pages, page_ids = _paged_problem(16)
+    P = prob["k_prev"].shape[0]
+    np.testing.assert_array_equal(ob.gather_pages(k_pages, page_ids, P), prob["k_prev"])
+    np.testing.assert_array_equal(ob.gather_pages(v_pages, page_ids, P), prob["v_prev"])
+    assert ob.gather_pages(k_pages, page_ids, 0).shape == (0,) + k_pages.shape[2:]
+
+
+def check_paged_softmax_kv_vs_sdpa(ob):
+    """Over a shuffled page pool with NaN in every unused slot, the paged
+    comparison equals torch's fp64 scaled_dot_product_attention over the
+    request's tokens in order followed by its block; with an empty prefix it
+    is attention within the block alone."""
+    for P, p in ((11, 4), (8, 4), (1, 3), (0, 4)):
+        prob, k_pages, v_pages, page_ids = _paged_problem(17 + P, P=P, p=p)
+        o = ob.softmax_kv_attend_paged(k_pages, v_pages, page_ids, P, prob["q"], prob["k"],
+                                       prob["v"])
+        ref = _sdpa(prob["q"], np.concatenate([prob["k_prev"], prob["k"]]),
+                    np.concatenate([prob["v_prev"], prob["v"]]))
+        _close(o, ref, rtol=1e-10)
+
+
 # ------------------------------------------------- prompt with outputs (N1)
 
 def _prompt_problem(seed, T=12, L=4, H=2, d=6, f=2, N0=5):
@@ -342,6 +385,8 @@ ALL_CHECKS = [
     check_convex_combination,
     check_softmax_kv_vs_sdpa,
     check_softmax_kv_empty_prefix,
+    check_paged_gather_layout,
+    check_paged_softmax_kv_vs_sdpa,
     check_prefill_attend_vs_bruteforce,
     check_prefill_attend_first_block_is_softmax,
 ]

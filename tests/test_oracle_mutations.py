@@ -114,9 +114,29 @@ def _prefill_attend_ignores_context(q, k, v, W, gate, L, merge=ob.MERGE_SHARED_N
     return _ORIG["prefill_attend"](q, k, v, W, gate, L, merge, scale)
 
 
+
+def _gather_pool_order(pages, page_ids, P):
+    """Reads pages in pool order instead of through the page table."""
+    return _ORIG["gather_pages"](pages, np.arange(np.asarray(pages).shape[0]), P)
+
+
+def _gather_page_slot_swapped(pages, page_ids, P):
+    """Swaps the roles of page index and slot: page t mod p, slot t // p."""
+    pages = np.asarray(pages, np.float64)
+    p = pages.shape[1]
+    rows = [pages[int(page_ids[t % p]), t // p] for t in range(int(P))]
+    return np.stack(rows) if rows else np.zeros((0,) + pages.shape[2:])
+
+
+def _gather_whole_pages(pages, page_ids, P):
+    """Reads every slot of the request's pages, past token P - 1 too."""
+    p = np.asarray(pages).shape[1]
+    return _ORIG["gather_pages"](pages, page_ids, -(-int(P) // p) * p)
+
+
 _ORIG = {name: getattr(ob, name) for name in
          ("commit", "sigmoid", "softmax_kv_attend", "feature_map", "_softmax_last", "_scale", "attend",
-          "prefill_attend")}
+          "prefill_attend", "gather_pages")}
 
 MUTATIONS = {
     "phi halves swapped": {"feature_map": _fm_swapped_halves},
@@ -135,6 +155,9 @@ MUTATIONS = {
     "comparison drops block keys": {"softmax_kv_attend": _softmax_kv_no_block},
     "prompt block committed before it attends": {"prefill_attend": _prefill_attend_commit_first},
     "prompt ignores the earlier context": {"prefill_attend": _prefill_attend_ignores_context},
+    "paged gather ignores the page table": {"gather_pages": _gather_pool_order},
+    "paged gather swaps page and slot": {"gather_pages": _gather_page_slot_swapped},
+    "paged gather reads whole pages": {"gather_pages": _gather_whole_pages},
 }
 
 
