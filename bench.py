@@ -682,8 +682,9 @@ def run_psweep(args):
     """One linearized layer, B in {1, 64}, prefix P = 1,024 .. 32,768 tokens:
     hb_block_attend (reads the fixed-size state, whatever P) against
     hb_softmax_kv_attend over the same prefix kept as a KV cache (reads all
-    of it). This is the shape of the pages' comparison over generation
-    lengths."""
+    of it), packed per request and, through hb_softmax_kv_attend_paged, in
+    32-token pages scattered over a shared pool. This is the shape of the
+    pages' comparison over generation lengths."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
@@ -694,8 +695,8 @@ def run_psweep(args):
     peak, kind = _peaks()
     sweep = []
     reps = max(3, min(args.steps, 100))
-    for nB in (1, 64):
-        for P in (1024, 2048, 4096, 8192, 16384, 32768):
+    for nB in args.psweep_batches:
+        for P in args.psweep_prefixes:
             w = inputs.stack_layer(0, nB, device=device, P=P)
             t = w.tensors
             S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
@@ -708,6 +709,8 @@ def run_psweep(args):
             ws = torch.empty(max(hb.hb_softmax_kv_workspace_size(cfg, nB, P), 16),
                              dtype=torch.uint8, device=device)
             o = torch.empty_like(t["q"])
+            kp, vp, table, plen = inputs.paged_cache(P, t["prefix_k"], t["prefix_v"], [P] * nB,
+                                                     32)
 
             def hybrid():
                 hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"], o=o)
@@ -716,31 +719,38 @@ def run_psweep(args):
                 hb.hb_softmax_kv_attend(cfg, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P,
                                         t["q"], t["k"], t["v"], o=o, workspace=ws)
 
+            def softmax_paged():
+                hb.hb_softmax_kv_attend_paged(cfg, kp, vp, table, plen, P, t["q"], t["k"],
+                                              t["v"], o=o, workspace=ws)
+
             h_ms = _graph_ms(hybrid, 10, reps, args.warmup, stream)
             s_ms = _graph_ms(softmax, 2, max(3, reps // 4), args.warmup, stream)
+            sp_ms = _graph_ms(softmax_paged, 2, max(3, reps // 4), args.warmup, stream)
             assert hb.hb_get_device_status() == 0
             hb_bytes = nB * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W
             sm_bytes = nB * ((P + L) * H * D * 2 * 2 + 2 * L * H * D * 2)
             sweep.append({
                 "batch": nB, "prefix": P, "hybrid_ms": h_ms, "softmax_kv_ms": s_ms,
-                "speedup": s_ms / h_ms,
+                "speedup": s_ms / h_ms, "softmax_kv_paged_ms": sp_ms,
+                "paged_over_packed": sp_ms / s_ms,
                 "hybrid_gbs": hb_bytes / (h_ms / 1e3) / 1e9,
                 "softmax_kv_gbs": sm_bytes / (s_ms / 1e3) / 1e9,
                 "hybrid_frac": hb_bytes / (h_ms / 1e3) / 1e9 / peak,
                 "softmax_kv_frac": sm_bytes / (s_ms / 1e3) / 1e9 / peak,
             })
-            del w, t, S, Z, ws, pws, o
+            del w, t, S, Z, ws, pws, o, kp, vp, table, plen
             torch.cuda.empty_cache()
-    top = [r for r in sweep if r["batch"] == 64][-1]
+    top = sweep[-1]
     return {
         "metric": "prefix-length sweep: active-block tokens/s, hybrid vs softmax over KV cache",
-        "value": 64 * L / (top["hybrid_ms"] / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "value": top["batch"] * L / (top["hybrid_ms"] / 1e3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": top["hybrid_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "one linearized layer x 16 heads, d=128, f=64, L=32; B in {1, 64}; "
-                               "prefix P = 1,024 .. 32,768 tokens",
+        "config": {"workload": "one linearized layer x 16 heads, d=128, f=64, L=32; "
+                               f"B in {args.psweep_batches}; prefix P in {args.psweep_prefixes}",
                    "timing": "10 (hybrid) or 2 (softmax) calls per CUDA graph, graph replayed",
+                   "paged": "softmax over 32-token pages at seeded positions of one pool",
                    "l2": "back-to-back calls on one layer: the hybrid's bytes (1.8 MB at B=1, "
                          "101 MB at B=64) and the softmax caches below ~100 MB stay partly in "
                          "the 126 MB L2 between calls; the step and stack workloads rotate "
@@ -962,6 +972,9 @@ def main(argv=None):
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
                          "softmax over a KV cache; feature_map: standalone phi")
     ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
+    ap.add_argument("--psweep-batches", type=int, nargs="+", default=[1, 64])
+    ap.add_argument("--psweep-prefixes", type=int, nargs="+",
+                    default=[1024, 2048, 4096, 8192, 16384, 32768])
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

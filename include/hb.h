@@ -312,6 +312,41 @@ size_t hb_softmax_kv_workspace_size(const hb_config* cfg, int32_t batch,
                                     int64_t max_prefix);
 
 /*
+ * hb_softmax_kv_attend_paged — hb_softmax_kv_attend over a paged KV cache
+ * (PagedAttention, Kwon et al., SOSP 2023; gist.science technical summary,
+ * "Key Contributions", implementation bullet: the method's serving kernel
+ * keeps the fixed-size state next to paged KV caches). Comparison path only;
+ * the same output as the packed call on the same tokens.
+ *   k_pages, v_pages [num_pages, page_tokens, H, d] activation dtype, a pool
+ *                    shared by all requests (NULL allowed when num_pages == 0)
+ *   page_table       [batch, max_pages] int32, device: row b lists request b's
+ *                    pages in token order; cached token t of request b is
+ *                    row t % page_tokens of page page_table[b][t / page_tokens].
+ *                    Only the first ceil(P_b / page_tokens) entries of a row
+ *                    are read (NULL allowed when max_pages == 0)
+ *   prefix_len       [batch] int32, device: P_b, the request's cached tokens.
+ *                    Slots of its last page past token P_b - 1 are never
+ *                    read into a sum and may hold anything, NaN included
+ *   max_prefix       host upper bound on any P_b (sizes the grid), < 2^31
+ *   q, k, v          [batch, L, H, d]; o [batch, L, H, d] written
+ *   workspace        device scratch of hb_softmax_kv_workspace_size(cfg,
+ *                    batch, max_prefix) bytes suffices
+ * A request with P_b < 0, P_b > max_prefix, more than max_pages pages, or a
+ * page id outside [0, num_pages) among the pages it reads gets no output
+ * written and is flagged as HB_ERR_DEVICE_BOUNDS; no page outside the pool
+ * is ever read. bf16 with d = 128, L = 32 and page_tokens a multiple of 32
+ * takes the TMA kernel; every other case a plain kernel.
+ */
+hb_status hb_softmax_kv_attend_paged(const hb_config* cfg, int32_t batch,
+                                     const void* k_pages, const void* v_pages,
+                                     int64_t num_pages, int32_t page_tokens,
+                                     const int32_t* page_table, int32_t max_pages,
+                                     const int32_t* prefix_len, int64_t max_prefix,
+                                     const void* q, const void* k, const void* v,
+                                     void* o, void* workspace,
+                                     size_t workspace_bytes, hb_stream_t stream);
+
+/*
  * hb_get_device_status — synchronise `stream`, then read and clear the
  * current device's status word. Returns HB_OK when no device-side fault was
  * recorded since the last call, else HB_ERR_DEVICE_BOUNDS or HB_ERR_TIMEOUT

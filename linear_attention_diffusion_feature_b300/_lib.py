@@ -68,6 +68,10 @@ SIGNATURES = {
                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                        c_void_p]),
     "hb_softmax_kv_workspace_size": (c_size_t, [_P, c_int32, c_int64]),
+    "hb_softmax_kv_attend_paged": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_int64, c_int32,
+                                             c_void_p, c_int32, c_void_p, c_int64, c_void_p,
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                             c_void_p]),
     "hb_get_device_status": (c_int32, [c_void_p]),
     "hb_status_string": (ctypes.c_char_p, [c_int32]),
 }

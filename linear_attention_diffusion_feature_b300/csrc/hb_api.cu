@@ -9,6 +9,7 @@
 
 #include "hb_fast.cuh"
 #include "hb_internal.cuh"
+#include "hb_paged.cuh"
 
 namespace hb {
 
@@ -338,6 +339,44 @@ hb_status hb_softmax_kv_attend(const hb_config* cfg, int32_t batch, const void* 
   return hb::from_cuda(hb::launch_softmax_kv_generic(s, batch, k_cache, v_cache, total_prefix,
                                                      cu_prefix,
                                                      max_prefix, q, k, v, o, status, st));
+}
+
+hb_status hb_softmax_kv_attend_paged(const hb_config* cfg, int32_t batch, const void* k_pages,
+                                     const void* v_pages, int64_t num_pages, int32_t page_tokens,
+                                     const int32_t* page_table, int32_t max_pages,
+                                     const int32_t* prefix_len, int64_t max_prefix, const void* q,
+                                     const void* k, const void* v, void* o, void* workspace,
+                                     size_t workspace_bytes, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || max_prefix < 0 || max_prefix > INT32_MAX || num_pages < 0 ||
+      page_tokens <= 0 || max_pages < 0)
+    return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({prefix_len, q, k, v, o})) != HB_OK) return r;
+  if (max_pages > 0 && (r = hb::check_ptrs({page_table})) != HB_OK) return r;
+  if (num_pages > 0 && (r = hb::check_ptrs({k_pages, v_pages})) != HB_OK) return r;
+  const size_t need =
+      hb::softmax_kv_paged_fast_fits(s, batch, num_pages, page_tokens, max_pages)
+          ? hb::softmax_kv_fast_workspace_bytes(s, batch, max_prefix)
+          : 0;
+  if (need > 0) {
+    if (workspace_bytes < need) return HB_ERR_WORKSPACE;
+    if ((r = hb::check_ptrs({workspace})) != HB_OK) return r;
+  }
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  hb::PagedKV pg;
+  pg.table = page_table;
+  pg.plen = prefix_len;
+  pg.max_pages = max_pages;
+  pg.page_tokens = page_tokens;
+  pg.num_pages = num_pages;
+  return hb::from_cuda(hb::launch_softmax_kv_paged(s, batch, k_pages, v_pages, pg, max_prefix, q,
+                                                   k, v, o, workspace, status,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 hb_status hb_get_device_status(hb_stream_t stream) {

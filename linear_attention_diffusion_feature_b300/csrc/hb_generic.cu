@@ -12,6 +12,7 @@
 #include <float.h>
 
 #include "hb_internal.cuh"
+#include "hb_paged.cuh"
 
 namespace hb {
 namespace {
@@ -291,17 +292,37 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
 
 // ---------------------------------------------------- softmax over KV cache
 // grid (batch, H), block 256. Flash-style online softmax over the request's
-// prefix keys followed by its block keys, in chunks of KC keys.
+// prefix keys followed by its block keys, in chunks of KC keys. The cache is
+// packed per request (cu_prefix) or paged (pg.table set): cached token t of
+// request b is then row t % page_tokens of page table[b][t / page_tokens].
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_softmax_kv_generic(
     int H, int d, int L, float scale, const T* __restrict__ k_cache, const T* __restrict__ v_cache,
     int64_t total_prefix, const int64_t* __restrict__ cu_prefix, int64_t max_prefix, const T* __restrict__ q,
-    const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ o, unsigned* status) {
+    const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ o, unsigned* status,
+    PagedKV pg) {
   constexpr int KC = 64;
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int64_t p0 = cu_prefix[b];
-  const int64_t P = cu_prefix[b + 1] - p0;
-  if (P < 0 || P > max_prefix || p0 < 0 || p0 + P > total_prefix) {
+  int64_t p0, P;
+  bool bad;
+  if (pg.table) {
+    p0 = 0;
+    P = pg.plen[b];
+    bad = P < 0 || P > max_prefix || (P + pg.page_tokens - 1) / pg.page_tokens > pg.max_pages;
+  } else {
+    p0 = cu_prefix[b];
+    P = cu_prefix[b + 1] - p0;
+    bad = P < 0 || P > max_prefix || p0 < 0 || p0 + P > total_prefix;
+  }
+  if (!bad && pg.table) {
+    // every page the request's tokens occupy must lie in the pool
+    int out = 0;
+    const int32_t* row = pg.table + (size_t)b * pg.max_pages;
+    for (int64_t j = tid; j < (P + pg.page_tokens - 1) / pg.page_tokens; j += blockDim.x)
+      out |= row[j] < 0 || row[j] >= pg.num_pages;
+    bad = __syncthreads_or(out) != 0;
+  }
+  if (bad) {
     if (tid == 0) atomicOr(status, kStatusBounds);
     return;
   }
@@ -339,7 +360,10 @@ __global__ void __launch_bounds__(kThreads) k_softmax_kv_generic(
       const int64_t key = c0 + t;
       float kk, vv;
       if (key < P) {
-        const size_t g = ((size_t)(p0 + key) * H + h) * d + a;
+        const int64_t r = pg.table ? (int64_t)pg.table[(size_t)b * pg.max_pages + key / pg.page_tokens] *
+                                             pg.page_tokens + key % pg.page_tokens
+                                   : p0 + key;
+        const size_t g = ((size_t)r * H + h) * d + a;
         kk = to_f32(k_cache[g]);
         vv = to_f32(v_cache[g]);
       } else {
@@ -535,11 +559,26 @@ cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot
   return cudaGetLastError();
 }
 
+static cudaError_t softmax_kv_generic(const Shape& s, int batch, const void* k_cache,
+                                      const void* v_cache, int64_t total_prefix,
+                                      const int64_t* cu_prefix, int64_t max_prefix, const void* q,
+                                      const void* k, const void* v, void* o, unsigned* status,
+                                      cudaStream_t st, const PagedKV& pg);
+
 cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_cache,
                                       const void* v_cache, int64_t total_prefix,
                                       const int64_t* cu_prefix,
                                       int64_t max_prefix, const void* q, const void* k,
                                       const void* v, void* o, unsigned* status, cudaStream_t st) {
+  return softmax_kv_generic(s, batch, k_cache, v_cache, total_prefix, cu_prefix, max_prefix, q, k,
+                            v, o, status, st, PagedKV{});
+}
+
+static cudaError_t softmax_kv_generic(const Shape& s, int batch, const void* k_cache,
+                                      const void* v_cache, int64_t total_prefix,
+                                      const int64_t* cu_prefix, int64_t max_prefix, const void* q,
+                                      const void* k, const void* v, void* o, unsigned* status,
+                                      cudaStream_t st, const PagedKV& pg) {
   constexpr int KC = 64;
   const size_t smem = sizeof(float) * ((size_t)s.L * s.d + 2 * KC * s.d + s.L * KC + 3 * s.L);
   const dim3 grid(batch, s.H);
@@ -551,16 +590,25 @@ cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_c
                                      (const __nv_bfloat16*)v_cache, total_prefix, cu_prefix,
                                      max_prefix,
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
-                                     (const __nv_bfloat16*)v, (__nv_bfloat16*)o, status);
+                                     (const __nv_bfloat16*)v, (__nv_bfloat16*)o, status, pg);
   } else {
     auto* fn = k_softmax_kv_generic<float>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.L, s.scale, (const float*)k_cache,
                                      (const float*)v_cache, total_prefix, cu_prefix, max_prefix,
                                      (const float*)q, (const float*)k, (const float*)v,
-                                     (float*)o, status);
+                                     (float*)o, status, pg);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_kv_paged_generic(const Shape& s, int batch, const void* k_pages,
+                                            const void* v_pages, const PagedKV& pg,
+                                            int64_t max_prefix, const void* q, const void* k,
+                                            const void* v, void* o, unsigned* status,
+                                            cudaStream_t st) {
+  return softmax_kv_generic(s, batch, k_pages, v_pages, 0, nullptr, max_prefix, q, k, v, o,
+                            status, st, pg);
 }
 
 cudaError_t launch_state_zero(const Shape& s, int batch, const int32_t* slot_idx, float* S_pool,

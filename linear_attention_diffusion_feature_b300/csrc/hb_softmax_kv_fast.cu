@@ -21,10 +21,22 @@
 //   * the two key halves merge in shared memory at the end; a CTA that holds
 //     the whole key range writes o, otherwise it writes (m, l, O) partials
 //     that k_softmax_kv_combine merges in split order.
+//
+// Paged cache (kPaged): the cached tokens live in pages of page_tokens rows
+// of a shared pool (PagedAttention, Kwon et al., SOSP 2023; gist.science
+// technical summary, "Key Contributions", implementation bullet: the serving
+// kernel keeps the state next to paged KV caches). Token t of request b is
+// row t mod page_tokens of page page_table[b][t / page_tokens]. With
+// page_tokens a multiple of 32, each 64-key tile is two 32-row TMA boxes,
+// each inside one page. Every page id a CTA needs is checked before the first
+// load, and the V rows of a tile past the request's last token are zeroed in
+// registers, so unused slots of a page are never read into a sum (they may
+// hold anything, NaN included).
 #include <float.h>
 #include <math.h>
 
 #include "hb_fast.cuh"
+#include "hb_paged.cuh"
 #include "hb_ptx.cuh"
 
 namespace hb {
@@ -45,10 +57,14 @@ constexpr int kStageBytes = 32768;
 constexpr int kOffV = 16384;                  // V within a stage
 constexpr int kOffBar = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBar + 128 + 1024;
+// Paged: the page ids of a CTA's key range, read once when they are checked.
+constexpr int kPageCache = 1024;
+constexpr int kOffPages = kOffBar + 128;
+constexpr int kSmemBytesPaged = kOffPages + 4 * kPageCache + 1024;
 constexpr int kPartFloats = kL * kD + 2 * kL;  // O [32][128], m [32], l [32]
 
 struct Maps {
-  CUtensorMap kc;  // [total_prefix][H][d], box {64, 1, 64}
+  CUtensorMap kc;  // [total_prefix][H][d], box {64, 1, 64}; paged: [pages * page_tokens][H][d], box {64, 1, 32}
   CUtensorMap vc;
   CUtensorMap q;   // [B*L][H][d], box {64, 1, 32}
   CUtensorMap k;
@@ -63,18 +79,51 @@ struct Args {
   __nv_bfloat16* o;
   float* ws;
   unsigned* status;
+  // paged cache only
+  const int32_t* page_table;  // [batch][max_pages]
+  const int32_t* plen;        // [batch] cached tokens per request
+  int max_pages, page_tokens;
+  int64_t num_pages;
 };
 
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+template <bool kPaged>
 __device__ __forceinline__ bool prefix_range(const Args& a, int b, int64_t* p0, int64_t* P) {
-  *p0 = a.cu[b];
-  *P = a.cu[b + 1] - *p0;
-  return *P >= 0 && *P <= a.max_prefix && *p0 >= 0 && *p0 + *P <= a.total_prefix;
+  if constexpr (kPaged) {
+    *p0 = 0;
+    *P = a.plen[b];
+    return *P >= 0 && *P <= a.max_prefix &&
+           (*P + a.page_tokens - 1) / a.page_tokens <= a.max_pages;
+  } else {
+    *p0 = a.cu[b];
+    *P = a.cu[b + 1] - *p0;
+    return *P >= 0 && *P <= a.max_prefix && *p0 >= 0 && *p0 + *P <= a.total_prefix;
+  }
 }
 
+// True on every thread of the block when each page holding cached tokens
+// [tok_lo, tok_hi) of request b lies in the pool. All threads must call it.
+// With `cache` set, the id of the range's j-th page is also kept in
+// cache[j] for j < kPageCache (visible to the whole block on return).
+__device__ __forceinline__ bool pages_in_pool(const Args& a, int b, int64_t tok_lo,
+                                              int64_t tok_hi, int32_t* cache = nullptr) {
+  int bad = 0;
+  if (tok_lo < tok_hi) {
+    const int64_t first = tok_lo / a.page_tokens, last = (tok_hi - 1) / a.page_tokens;
+    const int32_t* row = a.page_table + (size_t)b * a.max_pages;
+    for (int64_t j = first + threadIdx.x; j <= last; j += blockDim.x) {
+      const int32_t id = row[j];
+      bad |= id < 0 || id >= a.num_pages;
+      if (cache && j - first < kPageCache) cache[j - first] = id;
+    }
+  }
+  return !__syncthreads_or(bad);
+}
+
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2)
     k_softmax_kv_fast(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -87,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   int64_t p0, P;
-  if (!prefix_range(a, b, &p0, &P)) {
+  if (!prefix_range<kPaged>(a, b, &p0, &P)) {
     if (threadIdx.x == 0 && split == 0) atomicOr(a.status, kStatusBounds);
     return;
   }
@@ -96,6 +145,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int t_begin = (int)((int64_t)n_t * split / a.splits);
   const int t_end = (int)((int64_t)n_t * (split + 1) / a.splits);
   const int n_my = t_end - t_begin;
+  int32_t* s_pages = reinterpret_cast<int32_t*>(smem + kOffPages);  // paged only
+  int64_t first_page = 0;
+  if constexpr (kPaged) {
+    const int64_t lo = min((int64_t)t_begin * kKT, P), hi = min((int64_t)t_end * kKT, P);
+    first_page = lo / a.page_tokens;
+    if (!pages_in_pool(a, b, lo, hi, s_pages)) {
+      if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(qbar, 1);
@@ -118,6 +177,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(qbar, 2 * 4096);
       tma_load_3d(smem + kOffQ, &maps.q, 0, h, b * kL, qbar);
       tma_load_3d(smem + kOffQ + 4096, &maps.q, 64, h, b * kL, qbar);
+      // paged: page (relative to first_page) and row within it of the next
+      // 32-token piece, advanced without a division per piece
+      int pg_rel = 0, pg_off = 0;
+      if (kPaged && t_begin < n_pre) {
+        const int64_t tok = (int64_t)t_begin * kKT;
+        pg_rel = (int)(tok / a.page_tokens - first_page);
+        pg_off = (int)(tok % a.page_tokens);
+      }
       for (int i = 0; i < n_my; ++i) {
         const int s = i % kStages, n = i / kStages;
         if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
@@ -126,7 +193,29 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const int t = t_begin + i;
         uint8_t* st = smem + kOffStage + s * kStageBytes;
-        if (t < n_pre) {
+        if (t < n_pre && kPaged) {
+          // one 32-row box per page piece; the second half only when the
+          // request has a token there
+          const int64_t tok0 = (int64_t)t * kKT;
+          const int halves = P - tok0 > 32 ? 2 : 1;
+          mbar_arrive_expect_tx(&full[s], halves * 4 * 4096);
+          for (int c = 0; c < halves; ++c) {
+            const int32_t page = pg_rel < kPageCache
+                                     ? s_pages[pg_rel]
+                                     : a.page_table[(size_t)b * a.max_pages + first_page + pg_rel];
+            const int row = page * a.page_tokens + pg_off;
+            pg_off += 32;
+            if (pg_off == a.page_tokens) {
+              pg_off = 0;
+              ++pg_rel;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              tma_load_3d(st + j * 8192 + c * 4096, &maps.kc, 64 * j, h, row, &full[s]);
+              tma_load_3d(st + kOffV + j * 8192 + c * 4096, &maps.vc, 64 * j, h, row, &full[s]);
+            }
+          }
+        } else if (t < n_pre) {
           const int row = (int)(p0 + (int64_t)t * kKT);
           mbar_arrive_expect_tx(&full[s], 4 * 8192);
 #pragma unroll
@@ -248,11 +337,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         pa[3] = pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
         const int mtx = lane >> 3;
         const int vrow = key0 + 16 * ks + (mtx & 1) * 8 + (lane & 7);
+        // Paged: this lane's V operand holds keys kb, kb + 1 (first register
+        // of each pair) and kb + 8, kb + 9 (second); rows past the request's
+        // last token are zeroed so that a page's unused slots never enter
+        // the sum, whatever they hold.
+        uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+        if constexpr (kPaged) {
+          const int kb = key0 + 16 * ks + 2 * t4;
+          mk0 = (kb < valid ? 0x0000ffffu : 0u) | (kb + 1 < valid ? 0xffff0000u : 0u);
+          mk1 = (kb + 8 < valid ? 0x0000ffffu : 0u) | (kb + 9 < valid ? 0xffff0000u : 0u);
+        }
 #pragma unroll
         for (int np = 0; np < 8; ++np) {
           uint32_t v0, v1, v2, v3;
           const int dch = 2 * np + (mtx >> 1);
           ldsm_x4_t(sV + (dch >> 3) * 8192 + sw128(vrow, dch & 7), v0, v1, v2, v3);
+          if constexpr (kPaged) {
+            v0 &= mk0;
+            v1 &= mk1;
+            v2 &= mk0;
+            v3 &= mk1;
+          }
           mma_bf16(oacc[2 * np], pa, v0, v1);
           mma_bf16(oacc[2 * np + 1], pa, v2, v3);
         }
@@ -325,11 +430,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// Merges the split partials of each (request, head) in split order.
+// Merges the split partials of each (request, head) in split order. A
+// request that k_softmax_kv_fast flagged gets no output.
+template <bool kPaged>
 __global__ void __launch_bounds__(256) k_softmax_kv_combine(const __grid_constant__ Args a) {
   const int h = blockIdx.x, b = blockIdx.y;
   int64_t p0, P;
-  if (!prefix_range(a, b, &p0, &P)) return;  // flagged by k_softmax_kv_fast
+  if (!prefix_range<kPaged>(a, b, &p0, &P)) return;
+  if constexpr (kPaged) {
+    if (!pages_in_pool(a, b, 0, P)) return;
+  }
   __shared__ float wgt[kMaxSplits][kL];
   __shared__ float inv[kL];
   const float* base = a.ws + (size_t)(b * a.H + h) * a.splits * kPartFloats;
@@ -365,12 +475,13 @@ int num_sms() {
   return current_sm_count(&n) == cudaSuccess && n > 0 ? n : 148;
 }
 
-// Splits per (request, head): about one wave of two CTAs per SM, at most one
-// split per 64-key tile.
+// Splits per (request, head): at most one wave of two CTAs per SM (rounded
+// down, so that no CTA waits for a second wave), at most one split per
+// 64-key tile.
 int kv_splits(int batch, int H, int64_t max_prefix) {
   const int64_t units = (int64_t)batch * H;
   const int64_t tiles = (max_prefix + kKT - 1) / kKT + 1;
-  int64_t s = (2 * (int64_t)num_sms() + units - 1) / (units > 0 ? units : 1);
+  int64_t s = 2 * (int64_t)num_sms() / (units > 0 ? units : 1);
   if (s > tiles) s = tiles;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : (int)s;
@@ -379,6 +490,60 @@ int kv_splits(int batch, int H, int64_t max_prefix) {
 bool fast_kv_fits(int batch, int64_t total_prefix) {
   return batch <= 65535 && total_prefix < ((int64_t)1 << 31) &&
          (int64_t)batch * kL < ((int64_t)1 << 31);
+}
+
+// q, k, v of the active blocks: [batch * L][H][d], box {64, 1, 32}.
+bool encode_block_maps(Maps* m, const Shape& s, int batch, const void* q, const void* k,
+                       const void* v) {
+  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * kL};
+  const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
+  const uint32_t box[3] = {64, 1, 32};
+  const void* ptrs[3] = {q, k, v};
+  CUtensorMap* dst[3] = {&m->q, &m->k, &m->v};
+  for (int j = 0; j < 3; ++j)
+    if (!encode_tmap(dst[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[j], dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  return true;
+}
+
+// Cached keys and values: `rows` rows of [H][d], boxes of `box_rows` rows.
+bool encode_cache_maps(Maps* m, const Shape& s, const void* kc, const void* vc, uint64_t rows,
+                       uint32_t box_rows) {
+  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, rows};
+  const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
+  const uint32_t box[3] = {64, 1, box_rows};
+  return encode_tmap(&m->kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kc, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_tmap(&m->vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vc, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool kPaged>
+cudaError_t run(const Maps& maps, const Args& a, int H, int batch, cudaStream_t st) {
+  const int smem = kPaged ? kSmemBytesPaged : kSmemBytes;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_softmax_kv_fast<kPaged>), smem);
+  if (e != cudaSuccess) return e;
+  k_softmax_kv_fast<kPaged><<<dim3(a.splits, H, batch), kThreads, smem, st>>>(maps, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.splits > 1) {
+    k_softmax_kv_combine<kPaged><<<dim3(H, batch), 256, 0, st>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+Args common_args(const Shape& s, int batch, int64_t max_prefix, void* o, void* workspace,
+                 unsigned* status) {
+  Args a{};
+  a.H = s.H;
+  a.splits = kv_splits(batch, s.H, max_prefix);
+  a.max_prefix = max_prefix;
+  a.scale_log2 = s.scale * kLog2e;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.ws = static_cast<float*>(workspace);
+  a.status = status;
+  return a;
 }
 
 }  // namespace
@@ -399,50 +564,50 @@ cudaError_t launch_softmax_kv_fast(const Shape& s, int batch, const void* k_cach
     return launch_softmax_kv_generic(s, batch, k_cache, v_cache, total_prefix, cu_prefix,
                                      max_prefix, q, k, v, o, status, st);
   Maps maps;
-  {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * kL};
-    const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
-    const uint32_t box[3] = {64, 1, 32};
-    const void* ptrs[3] = {q, k, v};
-    CUtensorMap* dst[3] = {&maps.q, &maps.k, &maps.v};
-    for (int j = 0; j < 3; ++j)
-      if (!encode_tmap(dst[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[j], dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-  }
-  {
-    // With no cached rows at all no prefix tile is ever loaded; the block
-    // tensors then stand in so that the maps stay encodable.
-    const bool none = total_prefix == 0;
-    const uint64_t rows = none ? (uint64_t)batch * kL : (uint64_t)total_prefix;
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, rows};
-    const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
-    const uint32_t box[3] = {64, 1, kKT};
-    if (!encode_tmap(&maps.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, none ? k : k_cache, dims,
-                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap(&maps.vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, none ? v : v_cache, dims,
-                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  Args a;
-  a.H = s.H;
-  a.splits = kv_splits(batch, s.H, max_prefix);
+  // With no cached rows at all no prefix tile is ever loaded; the block
+  // tensors then stand in so that the maps stay encodable.
+  const bool none = total_prefix == 0;
+  if (!encode_block_maps(&maps, s, batch, q, k, v) ||
+      !encode_cache_maps(&maps, s, none ? k : k_cache, none ? v : v_cache,
+                         none ? (uint64_t)batch * kL : (uint64_t)total_prefix, kKT))
+    return cudaErrorInvalidValue;
+  Args a = common_args(s, batch, max_prefix, o, workspace, status);
   a.total_prefix = total_prefix;
-  a.max_prefix = max_prefix;
-  a.scale_log2 = s.scale * kLog2e;
   a.cu = cu_prefix;
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.ws = static_cast<float*>(workspace);
-  a.status = status;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_softmax_kv_fast), kSmemBytes);
-  if (e != cudaSuccess) return e;
-  k_softmax_kv_fast<<<dim3(a.splits, s.H, batch), kThreads, kSmemBytes, st>>>(maps, a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.splits > 1) {
-    k_softmax_kv_combine<<<dim3(s.H, batch), 256, 0, st>>>(a);
-    e = cudaGetLastError();
-  }
-  return e;
+  return run<false>(maps, a, s.H, batch, st);
+}
+
+bool softmax_kv_paged_fast_fits(const Shape& s, int batch, int64_t num_pages, int page_tokens,
+                                int max_pages) {
+  return production_shape(s) && page_tokens > 0 && page_tokens % 32 == 0 && batch <= 65535 &&
+         num_pages >= 0 && num_pages * (int64_t)page_tokens < ((int64_t)1 << 31) &&
+         (int64_t)batch * max_pages < ((int64_t)1 << 31) &&
+         (int64_t)batch * kL < ((int64_t)1 << 31);
+}
+
+cudaError_t launch_softmax_kv_paged(const Shape& s, int batch, const void* k_pages,
+                                    const void* v_pages, const PagedKV& pg, int64_t max_prefix,
+                                    const void* q, const void* k, const void* v, void* o,
+                                    void* workspace, unsigned* status, cudaStream_t st) {
+  if (!softmax_kv_paged_fast_fits(s, batch, pg.num_pages, pg.page_tokens, pg.max_pages))
+    return launch_softmax_kv_paged_generic(s, batch, k_pages, v_pages, pg, max_prefix, q, k, v,
+                                           o, status, st);
+  Maps maps;
+  // An empty pool is never read (every request with a cached token is
+  // flagged); the block tensors then stand in for it.
+  const bool none = pg.num_pages == 0;
+  if (!encode_block_maps(&maps, s, batch, q, k, v) ||
+      !encode_cache_maps(&maps, s, none ? k : k_pages, none ? v : v_pages,
+                         none ? (uint64_t)batch * kL : (uint64_t)(pg.num_pages * pg.page_tokens),
+                         32))
+    return cudaErrorInvalidValue;
+  Args a = common_args(s, batch, max_prefix, o, workspace, status);
+  a.page_table = pg.table;
+  a.plen = pg.plen;
+  a.max_pages = pg.max_pages;
+  a.page_tokens = pg.page_tokens;
+  a.num_pages = pg.num_pages;
+  return run<true>(maps, a, s.H, batch, st);
 }
 
 }  // namespace hb

@@ -293,6 +293,39 @@ def hb_softmax_kv_attend(cfg: Config, k_cache, v_cache, cu_prefix, max_prefix: i
     return o
 
 
+def hb_softmax_kv_attend_paged(cfg: Config, k_pages, v_pages, page_table, prefix_len,
+                               max_prefix: int, q, k, v, o=None, workspace=None,
+                               stream=None) -> torch.Tensor:
+    """Comparison path over a paged KV cache: k_pages/v_pages [num_pages,
+    page_tokens, H, d] shared by all requests, page_table [B, max_pages] int32
+    (request b's pages in token order), prefix_len [B] int32 cached tokens."""
+    B = q.shape[0]
+    H, d, L = cfg.num_heads, cfg.head_dim, cfg.block_len
+    num_pages, page_tokens = k_pages.shape[0], k_pages.shape[1]
+    _check(k_pages, "k_pages", cfg.torch_dtype, (num_pages, page_tokens, H, d))
+    _check(v_pages, "v_pages", cfg.torch_dtype, (num_pages, page_tokens, H, d))
+    max_pages = page_table.shape[1] if page_table.dim() == 2 else -1
+    _check(page_table, "page_table", torch.int32, (B, max_pages))
+    _check(prefix_len, "prefix_len", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    need = hb_softmax_kv_workspace_size(cfg, B, max_prefix)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _raise(lib.hb_softmax_kv_attend_paged(
+        ctypes.byref(cfg.c()), B, _ptr(k_pages) if num_pages else None,
+        _ptr(v_pages) if num_pages else None, num_pages, page_tokens,
+        _ptr(page_table) if max_pages else None, max_pages, _ptr(prefix_len), max_prefix,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(workspace), ws_bytes, _stream(stream)),
+        "hb_softmax_kv_attend_paged")
+    return o
+
+
 def hb_get_device_status(stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device status code."""
     return int(_lib.load().hb_get_device_status(_stream(stream)))

@@ -154,3 +154,35 @@ def draw(seed: int, shape, dtype=torch.bfloat16, device="cpu", std: float = 1.0)
     """One seeded N(0, std^2) tensor, drawn in float32 and rounded to dtype
     (for ad-hoc shapes: ragged lengths, edge cases)."""
     return _normal(_gen(seed, device), tuple(shape), dtype, device, std=std)
+
+
+def paged_cache(seed: int, k_cache: torch.Tensor, v_cache: torch.Tensor, lens,
+                page_tokens: int, spare_pages: int = 3, fill: float = float("nan")):
+    """Lays a packed per-request cache ``[sum P, H, d]`` out as a paged cache:
+    each request's tokens go, ``page_tokens`` at a time, into pages at seeded
+    random positions of one pool, with ``spare_pages`` pages that no request
+    uses. Returns ``k_pages``, ``v_pages`` ``[num_pages, page_tokens, H, d]``,
+    ``page_table`` ``[B, max_pages]`` int32 (entries past a request's last
+    page are -1) and ``prefix_len`` ``[B]`` int32, on the cache's device.
+    Unused pages and the slots past a request's last token hold ``fill``."""
+    pt = int(page_tokens)
+    n_pages = [-(-int(P) // pt) for P in lens]
+    num_pages = sum(n_pages) + spare_pages
+    perm = torch.randperm(num_pages, generator=_gen(seed, "cpu")).tolist()
+    H, d = k_cache.shape[1:]
+    dev, dt = k_cache.device, k_cache.dtype
+    k_pages = torch.full((num_pages, pt, H, d), fill, dtype=dt, device=dev)
+    v_pages = torch.full((num_pages, pt, H, d), fill, dtype=dt, device=dev)
+    table = torch.full((len(lens), max(n_pages + [1])), -1, dtype=torch.int32)
+    rows, used = [], 0
+    for b, P in enumerate(lens):
+        table[b, :n_pages[b]] = torch.tensor(perm[used:used + n_pages[b]], dtype=torch.int32)
+        used += n_pages[b]
+        t = torch.arange(int(P))
+        rows.append(table[b, t // pt].long() * pt + t % pt)  # pool row of each token
+    if rows:
+        rows = torch.cat(rows).to(dev)
+        k_pages.view(num_pages * pt, H, d)[rows] = k_cache
+        v_pages.view(num_pages * pt, H, d)[rows] = v_cache
+    prefix_len = torch.tensor([int(P) for P in lens], dtype=torch.int32)
+    return k_pages, v_pages, table.to(dev), prefix_len.to(dev)

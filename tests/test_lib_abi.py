@@ -156,6 +156,29 @@ def test_softmax_kv_checks(lib):
                                     None) == 3
 
 
+def test_softmax_kv_paged_checks(lib):
+    c = _cfg()
+    # args: cfg, batch, k_pages, v_pages, num_pages, page_tokens, page_table, max_pages,
+    #       prefix_len, max_prefix, q, k, v, o, workspace, workspace_bytes, stream
+    def call(batch=1, num_pages=4, page_tokens=32, table=A, max_pages=2, plen=A,
+             max_prefix=64, q=A, kp=A):
+        return lib.hb_softmax_kv_attend_paged(ctypes.byref(c), batch, kp, kp, num_pages,
+                                              page_tokens, table, max_pages, plen, max_prefix,
+                                              q, A, A, A, None, 0, None)
+    assert call(batch=-1) == 1
+    assert call(page_tokens=0) == 1
+    assert call(num_pages=-1) == 1
+    assert call(max_pages=-1) == 1
+    assert call(max_prefix=-1) == 1
+    assert call(max_prefix=1 << 31) == 1          # prefix lengths are int32
+    assert call(plen=None) == 1
+    assert call(table=None) == 1                  # pages to look up but no table
+    assert call(kp=None) == 1                     # a non-empty pool needs its pointers
+    assert call(q=M) == 3
+    assert call(table=M) == 3
+    assert call(batch=0, table=None, plen=None, q=None, kp=None) == 0
+
+
 def test_feature_map_checks(lib):
     c = _cfg()
     assert lib.hb_feature_map(ctypes.byref(c), -1, A, A, A, None) == 1
