@@ -65,6 +65,11 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None
         raise TypeError(f"{name}: expected a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name}: must be a CUDA tensor, got {t.device}")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        # the library launches on the current device; a pointer into another
+        # GPU's memory would be dereferenced there
+        raise ValueError(f"{name}: lives on {t.device}, but the current device is cuda:{cur}")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
@@ -79,6 +84,9 @@ def _ptr(t):
 
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
+    cur = torch.cuda.current_device()
+    if s.device.index != cur:
+        raise ValueError(f"stream belongs to {s.device}, but the current device is cuda:{cur}")
     return ctypes.c_void_p(s.cuda_stream)
 
 

@@ -125,9 +125,11 @@ def test_continuous_batching_step(cuda_device, merge):
             assert torch.equal(S[slot], S_before[slot]) and torch.equal(Z[slot], Z_before[slot])
 
 
-@pytest.mark.parametrize("B", [1, 16])
+@pytest.mark.parametrize("B", [1, 16, 256])
 def test_stack_layer(cuda_device, B):
-    """One layer of the 6-layer stack shape (2,048-token prefixes)."""
+    """One layer of the 6-layer stack shape (2,048-token prefixes), up to the
+    largest batch the stack is timed at (256 requests), sampled at the first,
+    middle and last request."""
     w = inputs.stack_layer(2, B, device=cuda_device)
     cfg = config(w, hb.MERGE_SHARED_NORM)
     t = w.tensors

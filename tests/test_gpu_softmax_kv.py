@@ -33,7 +33,7 @@ def test_softmax_kv_ragged(cuda_device, dt):
         assert out_err(f64(o[b]), ref) <= tol, b
 
 
-@pytest.mark.parametrize("B", [1, 16, 32])
+@pytest.mark.parametrize("B", [1, 16, 32, 256])
 def test_softmax_kv_stack_layer(cuda_device, B):
     w = inputs.stack_layer(1, B, device=cuda_device)
     cfg = config(w)

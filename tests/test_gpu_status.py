@@ -92,3 +92,23 @@ def test_host_validation_raises(cuda_device):
     bad = hb.Config(2, 128, 64, 32, scale=-1.0)
     with pytest.raises(hb.HBError):
         hb.hb_block_attend(bad, slots([0], cuda_device), q, q, q, S, Z, W, gate)
+
+
+def test_tensors_on_another_device_are_refused(cuda_device, monkeypatch):
+    """The library launches on the current device, so the binding refuses a
+    tensor or a stream that lives on another one before anything is launched
+    (emulated on one GPU by reporting another current device)."""
+    cfg = hb.Config(2, 128, 64, 32)
+    S, Z = new_pool(cfg, 2, cuda_device)
+    q = inputs.draw(7, (1, 32, 2, 128), device=cuda_device)
+    W = inputs.draw(8, (2, 128, 64), device=cuda_device, std=128 ** -0.5)
+    gate = torch.zeros(2, device=cuda_device)
+    sl = slots([0], cuda_device)
+    o = torch.full_like(q, 7.0)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: cuda_device.index + 1)
+    with pytest.raises(ValueError, match="current device"):
+        hb.hb_block_attend(cfg, sl, q, q, q, S, Z, W, gate, o=o)
+    monkeypatch.undo()
+    torch.cuda.synchronize()
+    assert bool((o == 7.0).all())
+    assert hb.hb_get_device_status() == 0
