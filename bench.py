@@ -674,8 +674,22 @@ def run_stack(args):
                      "peak": peak, "unit": "GB/s", "frac": top["hybrid_frac"],
                      "peak_kind": kind, "traffic": None},
         "sweep": sweep,
+        "memory_per_request": _stack_memory(),
         "gpu_launches": N_LAYERS * args.steps,
     }
+
+
+def _stack_memory():
+    """What one request of the stack holds in device memory: the 6 layers'
+    states against the KV cache the same 6 layers would keep as softmax
+    layers (2,048 cached tokens and the active block, 32-token pages)."""
+    from linear_attention_diffusion_feature_b300 import capacity
+
+    tokens = 2048 + L
+    kv = capacity.kv_cache_bytes(tokens, N_LAYERS, H, D)
+    st = capacity.state_bytes(N_LAYERS, H, FH, D)
+    return {"tokens": tokens, "kv_cache_bytes": kv, "state_bytes": st, "ratio": kv / st,
+            "break_even_tokens": capacity.break_even_tokens(H, D, FH)}
 
 
 def run_psweep(args):
