@@ -187,7 +187,7 @@ def attend(q, k, v, S, Z, W, gate, merge: int = MERGE_SHARED_NORM, scale=None):
 
 
 def attend_bruteforce(q, k, v, k_prev, v_prev, W, gate,
-                      merge: int = MERGE_SHARED_NORM, scale=None):
+                      merge: int = MERGE_SHARED_NORM, scale=None, Wk=None):
     """Second, state-free formulation of ``attend`` used to cross-check it.
 
     By the kernel identity phi(q)^T (sum_t phi(k_t) v_t^T) =
@@ -195,8 +195,13 @@ def attend_bruteforce(q, k, v, k_prev, v_prev, W, gate,
     the committed tokens themselves with weights a_t = phi(q) . phi(k_t).
     This function evaluates that sum token by token and never forms S or Z.
     k_prev/v_prev [N, H, d] are all committed tokens (N may be 0).
+    With ``Wk`` given, the committed keys take that feature map and the
+    queries ``W`` (separate query and key maps; the pages speak of the
+    feature map matrices W of a layer without saying whether queries and
+    keys share one); by default one map serves both.
     """
     q, k, v, k_prev, v_prev, W = (_f64(a) for a in (q, k, v, k_prev, v_prev, W))
+    Wk = W if Wk is None else _f64(Wk)
     gate = _f64(gate)
     L, H, d = q.shape
     N = k_prev.shape[0]
@@ -207,7 +212,7 @@ def attend_bruteforce(q, k, v, k_prev, v_prev, W, gate,
         for i in range(L):
             phi_q = feature_map(q[i, h, :], W[h])
             blk_w = np.array([np.exp(sc * np.dot(q[i, h, :], k[j, h, :])) for j in range(L)])
-            lin_w = np.array([np.dot(phi_q, feature_map(k_prev[t, h, :], W[h])) for t in range(N)])
+            lin_w = np.array([np.dot(phi_q, feature_map(k_prev[t, h, :], Wk[h])) for t in range(N)])
             blk_num = sum(blk_w[j] * v[j, h, :] for j in range(L))
             blk_den = blk_w.sum()
             lin_num = sum((lin_w[t] * v_prev[t, h, :] for t in range(N)), np.zeros(d))

@@ -249,6 +249,25 @@ def check_convex_combination(ob):
         _close(o, np.broadcast_to(c, o.shape))
 
 
+
+def check_separate_query_key_maps(ob):
+    """A state built with a key map Wk and read with a query map Wq equals
+    the token-by-token sum with weights phi_Wq(q) . phi_Wk(k_t), both
+    merges; and it differs from using either map for both."""
+    p = _rand_problem(19, N=9)
+    g = np.random.default_rng(19)
+    Wk = g.standard_normal(p["W"].shape) / np.sqrt(p["W"].shape[1])
+    S, Z = ob.prefill(p["k_prev"], p["v_prev"], Wk)
+    for merge in (ob.MERGE_SHARED_NORM, ob.MERGE_CONVEX):
+        o = ob.attend(p["q"], p["k"], p["v"], S, Z, p["W"], p["gate"], merge)
+        ref = ob.attend_bruteforce(p["q"], p["k"], p["v"], p["k_prev"], p["v_prev"], p["W"],
+                                   p["gate"], merge, Wk=Wk)
+        _close(o, ref, rtol=1e-10, atol=1e-12)
+        same = ob.attend_bruteforce(p["q"], p["k"], p["v"], p["k_prev"], p["v_prev"], p["W"],
+                                    p["gate"], merge)
+        assert np.abs(o - same).max() > 1e-3
+
+
 # --------------------------------------------------- softmax-over-KV comparison
 
 def check_softmax_kv_vs_sdpa(ob):
@@ -383,6 +402,7 @@ ALL_CHECKS = [
     check_pure_linear_limits,
     check_block_permutation,
     check_convex_combination,
+    check_separate_query_key_maps,
     check_softmax_kv_vs_sdpa,
     check_softmax_kv_empty_prefix,
     check_paged_gather_layout,
