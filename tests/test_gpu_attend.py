@@ -159,3 +159,36 @@ def test_attend_deterministic(cuda_device):
     o1 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
     o2 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
     assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+def test_separate_query_and_key_feature_maps(cuda_device, merge):
+    """Separate feature maps for queries (Wq) and keys (Wk) through the
+    unfused calls: the state is built with Wk (hb_prefill_state, then
+    hb_commit_block of the active block) and read with Wq (hb_block_attend,
+    whose W only maps the queries). The oracle is the token-by-token sum with
+    weights phi_Wq(q) . phi_Wk(k_t)."""
+    B = 4
+    w = inputs.continuous_batching(device=cuda_device, B=B, lo=8, hi=16, n_commit=0)
+    cfg = config(w, MERGES[merge])
+    t = w.tensors
+    Wq = t["W"]
+    Wk = inputs.draw(77, tuple(Wq.shape), device=cuda_device, std=128 ** -0.5)
+    S, Z = new_pool(cfg, B, cuda_device)
+    sl = slots(range(B), cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], Wk, S, Z)
+    q2 = inputs.draw(78, tuple(t["q"].shape), device=cuda_device)
+    k2 = inputs.draw(79, tuple(t["k"].shape), device=cuda_device)
+    v2 = inputs.draw(80, tuple(t["v"].shape), device=cuda_device)
+    hb.hb_commit_block(cfg, sl, t["k"], t["v"], Wk, S, Z)  # the block before the active one
+    o = hb.hb_block_attend(cfg, sl, q2, k2, v2, S, Z, Wq, t["gate"])
+    assert_status_ok()
+    cu = t["cu_prefix"].cpu()
+    for b in (0, B - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        k_prev = np.concatenate([f64(t["prefix_k"][a:e]), f64(t["k"][b])])
+        v_prev = np.concatenate([f64(t["prefix_v"][a:e]), f64(t["v"][b])])
+        ref = ob.attend_bruteforce(f64(q2[b]), f64(k2[b]), f64(v2[b]), k_prev, v_prev, f64(Wq),
+                                   f64(t["gate"]), MERGES[merge], Wk=f64(Wk))
+        assert out_err(f64(o[b]), ref) <= TOL_OUT_BF16, b

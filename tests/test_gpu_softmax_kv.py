@@ -63,7 +63,8 @@ def _paged_problem(cuda_device, dt, lens, pt, H=4, seed=41):
 
 
 @pytest.mark.parametrize("dt,pt", [(torch.bfloat16, 32), (torch.bfloat16, 64),
-                                   (torch.bfloat16, 16), (torch.float32, 32)])
+                                   (torch.bfloat16, 256), (torch.bfloat16, 16),
+                                   (torch.float32, 32)])
 def test_softmax_kv_paged_ragged(cuda_device, dt, pt):
     """Ragged prefixes (empty, inside one page, on page and tile edges, many
     tiles) in pages scattered over a pool whose unused pages and slots hold
