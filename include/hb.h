@@ -126,7 +126,10 @@ hb_status hb_feature_map(const hb_config* cfg, int64_t n_tokens, const void* x,
  *   q, k, v      [batch, L, H, d] activation dtype: the active block
  *   S_pool       [num_slots, H, F, d] fp32, read only
  *   Z_pool       [num_slots, H, F] fp32, read only
- *   W            [H, d, f] activation dtype (one W per head for q and k)
+ *   W            [H, d, f] activation dtype: the feature map of the queries
+ *                (only phi(q) is formed here, so a state built with a
+ *                separate key map by hb_commit_block / hb_prefill_state is
+ *                read correctly)
  *   gate_logits  [H] fp32: alpha_h (SHARED_NORM) or g_h (CONVEX)
  *   o            [batch, L, H, d] activation dtype, written
  * A request whose slot is out of range gets no output written and sets
@@ -150,6 +153,7 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch,
  * and written back once, instead of being read again by a separate commit.
  *   commit   [batch] int32, device: nonzero = this request commits its block
  *   S_pool, Z_pool  read for every request, written for committing ones
+ *   W        one feature map for both the queries and the committed keys
  *   other arguments as in hb_block_attend.
  * A committing request's slot must not be read by any other request of the
  * same call (distinct slots, as in hb_commit_block).
@@ -180,7 +184,8 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
  *   S_pool, Z_pool  the slots' states: zeroed first when accumulate = 0,
  *                continued from when accumulate = 1; hold the whole
  *                prompt's commit at the end
- *   W, gate_logits as in hb_block_attend
+ *   W            one feature map for both queries and keys
+ *   gate_logits  as in hb_block_attend
  *   o            [batch, seq_len, H, d] activation dtype, written
  * Asynchronous on `stream` and graph-capturable (a state reset when
  * accumulate = 0, then one launch in which each (request, head) walks its
@@ -202,7 +207,7 @@ hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch,
  * S_n = S_{n-1} + sum_t phi(k_t) v_t^T, Z_n = Z_{n-1} + sum_t phi(k_t)).
  *   slot_idx [batch] int32, distinct slots (two requests writing one slot race)
  *   k, v     [batch, L, H, d] activation dtype: the committed block
- *   W        [H, d, f]
+ *   W        [H, d, f]: the feature map of the keys
  *   S_pool, Z_pool updated in place for the listed slots only.
  */
 hb_status hb_commit_block(const hb_config* cfg, int32_t batch,
