@@ -172,16 +172,18 @@ def _traffic(kernel: str):
     return rec.get("bytes_per_launch")
 
 
-def make_layers(device):
+def make_layers(device, rank=0):
     """6 independent layer instances of the continuous-batching workload, with
-    states built by hb_prefill_state from each layer's own prefixes."""
+    states built by hb_prefill_state from each layer's own prefixes. Each rank
+    draws its own requests (rank 0 keeps the single-GPU seeds)."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
     layers = []
     cfg = hb.Config(H, D, FH, L, dtype=hb.DTYPE_BF16, merge=hb.MERGE_SHARED_NORM)
     for layer in range(N_LAYERS):
-        w = inputs.continuous_batching(seed=2 + 100 * layer, device=device, B=B, n_commit=N_COMMIT)
+        w = inputs.continuous_batching(seed=2 + 100 * layer + 100000 * rank, device=device, B=B,
+                                       n_commit=N_COMMIT)
         t = w.tensors
         S = torch.empty((B, H, F, D), dtype=torch.float32, device=device)
         Z = torch.empty((B, H, F), dtype=torch.float32, device=device)
@@ -207,7 +209,7 @@ def run_ours(args, world, rank, local):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    cfg, layers = make_layers(device)
+    cfg, layers = make_layers(device, rank)
     stream = torch.cuda.current_stream()
 
     def step(i):
