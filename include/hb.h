@@ -289,6 +289,24 @@ hb_status hb_state_zero(const hb_config* cfg, int32_t batch,
                         int32_t num_slots, hb_stream_t stream);
 
 /*
+ * hb_state_copy — copy S and Z of slot src_slot[b] to slot dst_slot[b] for
+ * every b < batch, within one pool. The state is a request's whole summary of
+ * its committed blocks (gist.science technical summary, state-compression
+ * bullet), so this snapshots a request before it is preempted, restores it,
+ * or forks it into a second request with the same history.
+ *   src_slot, dst_slot [batch] int32, device. Destinations must be distinct,
+ *                    and no slot may be both a source and a destination of
+ *                    one call (those copies would race); src == dst is a no-op
+ *   S_pool, Z_pool   [num_slots, H, F, d] and [num_slots, H, F] fp32
+ * A pair with a slot outside [0, num_slots) is skipped and flagged as
+ * HB_ERR_DEVICE_BOUNDS.
+ */
+hb_status hb_state_copy(const hb_config* cfg, int32_t batch,
+                        const int32_t* src_slot, const int32_t* dst_slot,
+                        float* S_pool, float* Z_pool, int32_t num_slots,
+                        hb_stream_t stream);
+
+/*
  * hb_softmax_kv_attend — the full-prefix softmax attention that block-hybrid
  * attention replaces (arXiv abstract: every denoising step still attends to
  * all previous blocks; gist.science technical summary, problem statement).

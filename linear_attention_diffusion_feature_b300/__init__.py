@@ -25,6 +25,7 @@ from .hb import (  # noqa: F401
     hb_softmax_kv_attend,
     hb_softmax_kv_attend_paged,
     hb_softmax_kv_workspace_size,
+    hb_state_copy,
     hb_state_zero,
     hb_status_string,
 )

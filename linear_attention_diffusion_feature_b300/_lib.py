@@ -64,6 +64,8 @@ SIGNATURES = {
                                            c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                            c_int32, c_int32, c_void_p]),
     "hb_state_zero": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
+    "hb_state_copy": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                c_void_p]),
     "hb_softmax_kv_attend": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                        c_void_p]),

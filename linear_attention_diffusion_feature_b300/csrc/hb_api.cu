@@ -10,6 +10,7 @@
 #include "hb_fast.cuh"
 #include "hb_internal.cuh"
 #include "hb_paged.cuh"
+#include "hb_copy.cuh"
 
 namespace hb {
 
@@ -301,6 +302,23 @@ hb_status hb_state_zero(const hb_config* cfg, int32_t batch, const int32_t* slot
   if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
   return hb::from_cuda(hb::launch_state_zero(s, batch, slot_idx, S_pool, Z_pool, num_slots,
                                              status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hb_status hb_state_copy(const hb_config* cfg, int32_t batch, const int32_t* src_slot,
+                        const int32_t* dst_slot, float* S_pool, float* Z_pool,
+                        int32_t num_slots, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({src_slot, dst_slot, S_pool, Z_pool})) != HB_OK) return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  return hb::from_cuda(hb::launch_state_copy(s, batch, src_slot, dst_slot, S_pool, Z_pool,
+                                             num_slots, status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t hb_softmax_kv_workspace_size(const hb_config* cfg, int32_t batch, int64_t max_prefix) {

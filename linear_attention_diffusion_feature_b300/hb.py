@@ -269,6 +269,19 @@ def hb_state_zero(cfg: Config, slot_idx, S_pool, Z_pool, stream=None) -> None:
                              _ptr(Z_pool), num_slots, _stream(stream)), "hb_state_zero")
 
 
+def hb_state_copy(cfg: Config, src_slot, dst_slot, S_pool, Z_pool, stream=None) -> None:
+    """Copies the states of slots src_slot[b] to slots dst_slot[b] (distinct
+    destinations, none of them also a source in the same call)."""
+    B = src_slot.shape[0]
+    _check(src_slot, "src_slot", torch.int32, (B,))
+    _check(dst_slot, "dst_slot", torch.int32, (B,))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    lib = _lib.load()
+    _raise(lib.hb_state_copy(ctypes.byref(cfg.c()), B, _ptr(src_slot), _ptr(dst_slot),
+                             _ptr(S_pool), _ptr(Z_pool), num_slots, _stream(stream)),
+           "hb_state_copy")
+
+
 def hb_softmax_kv_workspace_size(cfg: Config, batch: int, max_prefix: int) -> int:
     return int(_lib.load().hb_softmax_kv_workspace_size(ctypes.byref(cfg.c()), batch, max_prefix))
 

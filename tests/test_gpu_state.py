@@ -158,3 +158,26 @@ def test_state_deterministic(cuda_device):
                             t["W"], S, Z)
         outs.append((S, Z))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("H,d,f", [(4, 128, 64), (2, 64, 16)])
+def test_state_copy_between_slots(cuda_device, H, d, f):
+    """hb_state_copy moves S and Z of each source slot to its destination bit
+    for bit and leaves every other slot alone; a pair with a slot outside the
+    pool is skipped and flagged while the other pairs are copied."""
+    cfg = hb.Config(H, d, f, 32)
+    S, Z = new_pool(cfg, 6, cuda_device)
+    S.copy_(inputs.draw(90, tuple(S.shape), torch.float32, device=cuda_device))
+    Z.copy_(inputs.draw(91, tuple(Z.shape), torch.float32, device=cuda_device))
+    S0, Z0 = S.clone(), Z.clone()
+    hb.hb_state_copy(cfg, slots([0, 3, 2], cuda_device), slots([4, 1, 2], cuda_device), S, Z)
+    assert_status_ok()
+    S_exp, Z_exp = S0.clone(), Z0.clone()
+    S_exp[4], Z_exp[4] = S0[0], Z0[0]
+    S_exp[1], Z_exp[1] = S0[3], Z0[3]
+    assert torch.equal(S, S_exp) and torch.equal(Z, Z_exp)
+    S1, Z1 = S.clone(), Z.clone()
+    hb.hb_state_copy(cfg, slots([5, 9], cuda_device), slots([0, 3], cuda_device), S, Z)
+    assert hb.hb_get_device_status() == 5  # HB_ERR_DEVICE_BOUNDS
+    S1[0], Z1[0] = S1[5].clone(), Z1[5].clone()
+    assert torch.equal(S, S1) and torch.equal(Z, Z1)

@@ -179,6 +179,17 @@ def test_softmax_kv_paged_checks(lib):
     assert call(batch=0, table=None, plen=None, q=None, kp=None) == 0
 
 
+def test_state_copy_checks(lib):
+    c = _cfg()
+    # args: cfg, batch, src_slot, dst_slot, S, Z, num_slots, stream
+    assert lib.hb_state_copy(ctypes.byref(c), -1, A, A, A, A, 4, None) == 1
+    assert lib.hb_state_copy(ctypes.byref(c), 1, A, A, A, A, -1, None) == 1
+    assert lib.hb_state_copy(ctypes.byref(c), 1, None, A, A, A, 4, None) == 1
+    assert lib.hb_state_copy(ctypes.byref(c), 1, A, A, M, A, 4, None) == 3
+    assert lib.hb_state_copy(ctypes.byref(_cfg(head_dim=8)), 1, A, A, A, A, 4, None) == 2
+    assert lib.hb_state_copy(ctypes.byref(c), 0, None, None, None, None, 0, None) == 0
+
+
 def test_feature_map_checks(lib):
     c = _cfg()
     assert lib.hb_feature_map(ctypes.byref(c), -1, A, A, A, None) == 1
