@@ -254,20 +254,25 @@ def run_ours(args, world, rank, local):
         for layer in range(k % N_LAYERS):
             singles[layer].replay()
 
+    nvtx = torch.cuda.nvtx  # ranges for profilers (ncu --nvtx-include "timed/")
+    nvtx.range_push("warmup")
     step_graphs = capture(step)
     attend_graphs = capture(attend_only)
     run_steps(step_graphs, max(args.warmup, N_LAYERS))
     torch.cuda.synchronize()
+    nvtx.range_pop()
 
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         _barrier(world)
         clocks.mark()
+        nvtx.range_push("timed")
         start.record(stream)
         run_steps(step_graphs, args.steps)
         end.record(stream)
         torch.cuda.synchronize()
+        nvtx.range_pop()
         _barrier(world)
     total_ms = start.elapsed_time(end)
     # each step is one launch of the step kernel, so its average launch
@@ -275,12 +280,14 @@ def run_ours(args, world, rank, local):
     # the same way for comparison
     step_launch_ms = total_ms / args.steps
     n_cmp = max(N_LAYERS, min(args.steps, 3000))
+    nvtx.range_push("attend_only")
     run_steps(attend_graphs, N_LAYERS)
     a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a_ev.record(stream)
     run_steps(attend_graphs, n_cmp)
     b_ev.record(stream)
     torch.cuda.synchronize()
+    nvtx.range_pop()
     attend_only_ms = a_ev.elapsed_time(b_ev) / n_cmp
     status = hb.hb_get_device_status()
     if status != 0:
@@ -292,7 +299,9 @@ def run_ours(args, world, rank, local):
     attend_bytes = B * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W
     peak, peak_kind = _peaks()
 
+    nvtx.range_push("e2e")
     e2e = run_e2e(args, cfg, layers, device)
+    nvtx.range_pop()
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
