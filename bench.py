@@ -614,7 +614,8 @@ def run_stack(args):
     """6 linearized layers, P=2,048-token prefixes, B in {1, 16, 64, 256}:
     one stack step = hb_block_attend of all 6 layers, timed against
     hb_softmax_kv_attend of the same 6 layers over the same prefixes kept as
-    a KV cache."""
+    a KV cache, and against hb_block_attend_s16 on bf16 copies of the same
+    states (bit-identical output, half the state bytes)."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
@@ -635,8 +636,10 @@ def run_stack(args):
             sl = torch.arange(nB, dtype=torch.int32, device=device)
             hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P,
                                 t["W"], S, Z)
+            S16 = torch.empty((nB, H, F, D), dtype=torch.bfloat16, device=device)
+            hb.hb_state_to_bf16(cfg, sl, S, S16)
             need = hb.hb_softmax_kv_workspace_size(cfg, nB, P)
-            layers.append(dict(t=t, S=S, Z=Z, sl=sl, o=torch.empty_like(t["q"]),
+            layers.append(dict(t=t, S=S, S16=S16, Z=Z, sl=sl, o=torch.empty_like(t["q"]),
                                ws=torch.empty(max(need, 16), dtype=torch.uint8, device=device)))
         torch.cuda.synchronize()
 
@@ -646,6 +649,12 @@ def run_stack(args):
                 hb.hb_block_attend(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S"], ly["Z"],
                                    t["W"], t["gate"], o=ly["o"])
 
+        def hybrid_s16():
+            for ly in layers:
+                t = ly["t"]
+                hb.hb_block_attend_s16(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S16"], ly["Z"],
+                                       t["W"], t["gate"], o=ly["o"])
+
         def softmax():
             for ly in layers:
                 t = ly["t"]
@@ -654,9 +663,12 @@ def run_stack(args):
 
         reps = max(3, min(args.steps, 200))
         h_ms = _graph_ms(hybrid, 1, reps, args.warmup, stream)
+        h16_ms = _graph_ms(hybrid_s16, 1, reps, args.warmup, stream)
         s_ms = _graph_ms(softmax, 1, max(3, reps // 4), args.warmup, stream)
         assert hb.hb_get_device_status() == 0
         hb_bytes = N_LAYERS * (nB * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W)
+        # the bf16 copy halves the state read: S is H * F * d * 2 bytes per request
+        hb16_bytes = hb_bytes - N_LAYERS * nB * H * F * D * 2
         sm_bytes = N_LAYERS * nB * ((P + L) * H * D * 2 * 2 + 2 * L * H * D * 2)
         sweep.append({
             "batch": nB, "hybrid_ms": h_ms, "softmax_kv_ms": s_ms,
@@ -667,6 +679,9 @@ def run_stack(args):
             "softmax_kv_gbs": sm_bytes / (s_ms / 1e3) / 1e9,
             "hybrid_frac": hb_bytes / (h_ms / 1e3) / 1e9 / peak,
             "softmax_kv_frac": sm_bytes / (s_ms / 1e3) / 1e9 / peak,
+            "hybrid_s16_ms": h16_ms, "hybrid_s16_tokens_per_s": nB * L / (h16_ms / 1e3),
+            "hybrid_s16_frac": hb16_bytes / (h16_ms / 1e3) / 1e9 / peak,
+            "s16_speedup": h_ms / h16_ms,
         })
         del layers
         torch.cuda.empty_cache()

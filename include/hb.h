@@ -143,6 +143,41 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch,
                           hb_stream_t stream);
 
 /*
+ * hb_state_to_bf16 — write the bf16 copy of the listed slots' S that
+ * hb_block_attend_s16 reads: S16[slot] = round-to-nearest bf16 of S[slot].
+ * Call it for a request's slot after every change to its fp32 state (a
+ * prompt ingested, a block committed, a copy or a reset); Z needs no copy.
+ *   slot_idx  [batch] int32, device
+ *   S_pool    [num_slots, H, F, d] fp32, read
+ *   S16_pool  [num_slots, H, F, d] bf16, written for the listed slots only
+ * A slot outside [0, num_slots) is skipped and flagged as HB_ERR_DEVICE_BOUNDS.
+ */
+hb_status hb_state_to_bf16(const hb_config* cfg, int32_t batch,
+                           const int32_t* slot_idx, const float* S_pool,
+                           void* S16_pool, int32_t num_slots,
+                           hb_stream_t stream);
+
+/*
+ * hb_block_attend_s16 — hb_block_attend reading the bf16 copy of S written
+ * by hb_state_to_bf16 instead of the fp32 pool. The state contraction takes
+ * S as bf16 operands rounded to nearest in either case, so the output is
+ * bit-identical to hb_block_attend's on the fp32 states the copy was made
+ * from, while each (request, head) reads 32 KiB of state instead of 64.
+ * Production shape only (bf16, d = 128, f = 64, L = 32); any other shape
+ * returns HB_ERR_UNSUPPORTED_SHAPE.
+ *   S16_pool  [num_slots, H, F, d] bf16, read only
+ *   Z_pool    [num_slots, H, F] fp32, read only (the master's Z)
+ *   other arguments as in hb_block_attend.
+ */
+hb_status hb_block_attend_s16(const hb_config* cfg, int32_t batch,
+                              const int32_t* slot_idx, const void* q,
+                              const void* k, const void* v,
+                              const void* S16_pool, const float* Z_pool,
+                              int32_t num_slots, const void* W,
+                              const float* gate_logits, void* o,
+                              hb_stream_t stream);
+
+/*
  * hb_block_attend_commit — hb_block_attend followed, for the requests whose
  * block is finished, by hb_commit_block of that same block, in one pass over
  * the state (gist.science technical summary, state-compression bullet: the

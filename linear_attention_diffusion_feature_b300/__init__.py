@@ -25,7 +25,9 @@ from .hb import (  # noqa: F401
     hb_softmax_kv_attend,
     hb_softmax_kv_attend_paged,
     hb_softmax_kv_workspace_size,
+    hb_block_attend_s16,
     hb_state_copy,
+    hb_state_to_bf16,
     hb_state_zero,
     hb_status_string,
 )

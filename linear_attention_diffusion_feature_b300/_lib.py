@@ -64,6 +64,11 @@ SIGNATURES = {
                                            c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                                            c_int32, c_int32, c_void_p]),
     "hb_state_zero": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
+    "hb_state_to_bf16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int32,
+                                   c_void_p]),
+    "hb_block_attend_s16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                      c_void_p]),
     "hb_state_copy": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                 c_void_p]),
     "hb_softmax_kv_attend": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_int64,

@@ -51,6 +51,7 @@
 
 #include "hb_fast.cuh"
 #include "hb_ptx.cuh"
+#include "hb_state16.cuh"
 
 namespace hb {
 namespace {
@@ -112,7 +113,7 @@ struct Maps {
   // the prompt length and the block's offset for chunkwise prompt
   // processing); commit_all: every request commits (commit_mask unused).
   int rows_per_req, row_base, commit_all;
-  CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}
+  CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16: bf16, box {64, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
   CUtensorMap v;
@@ -127,6 +128,12 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // Byte offset of S[k][n] (fp32) in the four SW128 boxes of the stage.
 __device__ __forceinline__ uint32_t s_off(int k, int n) {
   return (uint32_t)((n >> 5) * 16384 + k * 128 + ((((n & 31) >> 2) ^ (k & 7)) << 4) + (n & 3) * 4);
+}
+// Byte offset of S[k][n] (bf16 copy of the state) in the two SW128 boxes of
+// the stage's S region.
+__device__ __forceinline__ uint32_t s16_off(int k, int n) {
+  return (uint32_t)((n >> 6) * 16384 + k * 128 + ((((n & 63) >> 3) ^ (k & 7)) << 4) +
+                    (n & 7) * 2);
 }
 // Byte offset of v[key][n] (bf16) in the two SW128 boxes of the v tile.
 __device__ __forceinline__ uint32_t v_off(int key, int n) {
@@ -143,13 +150,18 @@ __device__ __forceinline__ uint32_t v_off(int key, int n) {
 // kCommit = false: attend only (commit_mask is ignored; S_pool and Z_pool are
 // not written). kCommit = true: requests with commit_mask[b] != 0 also fold
 // their block into the state after their output has been formed.
-template <bool kCommit, bool kSeq = false>
+// kS16 (attend only): S_pool is a bf16 copy of the states, each value the
+// round-to-nearest of the fp32 master. The state contraction takes S as bf16
+// operands rounded to nearest either way, so the output is bit-identical to
+// the fp32 pool's, while a unit reads 32 KiB of state instead of 64.
+template <bool kCommit, bool kSeq = false, bool kS16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
                   int merge, const int32_t* __restrict__ slot_idx,
                   const int32_t* __restrict__ commit_mask, const float* __restrict__ S_pool,
                   float* __restrict__ Z_pool, const float* __restrict__ gate,
                   __nv_bfloat16* __restrict__ o, unsigned* status) {
+  static_assert(!(kS16 && (kCommit || kSeq)), "the bf16 state copy is read-only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -557,11 +569,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
                     &head_full[s]);
           mbar_arrive(&head_full[s]);
-          mbar_arrive_expect_tx(&s_full[s], kSBytes);
           const int srow = (slot * H + h) * kF;
+          if (kS16) {
+            mbar_arrive_expect_tx(&s_full[s], kSBytes / 2);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(st + kOffS + j * 16384, &maps.S, 64 * j, srow, &s_full[s]);
+          } else {
+            mbar_arrive_expect_tx(&s_full[s], kSBytes);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(st + kOffS + j * 16384, &maps.S, 32 * j, srow, &s_full[s]);
+          }
         }
       }
     };
@@ -569,7 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = unit_b(i), h = unit_h(i), slot = unit_slot(i);
       if (lane != 0 || slot < 0 || slot >= num_slots) return;
       const size_t unit = (size_t)slot * H + h;
-      prefetch_l2(S_pool + unit * kF * kD, kF * kD * 4);
+      prefetch_l2(reinterpret_cast<const uint8_t*>(S_pool) + unit * kF * kD * (kS16 ? 2 : 4),
+                  kF * kD * (kS16 ? 2 : 4));
       prefetch_l2(Z_pool + unit * kF, kF * 4);
       // the request's block of q, k, v is one contiguous range of L rows of
       // all heads; the CTAs working on its heads at the same time each
@@ -955,12 +975,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                   a[m2][3]);
         }
         const int k0 = 16 * kk + 2 * t;
-        const float2 r0 = ld_shared_v2f(sS + s_off(k0, col));
-        const float2 r1 = ld_shared_v2f(sS + s_off(k0 + 1, col));
-        const float2 r8 = ld_shared_v2f(sS + s_off(k0 + 8, col));
-        const float2 r9 = ld_shared_v2f(sS + s_off(k0 + 9, col));
-        const uint32_t b00 = pack_bf16(r0.x, r1.x), b01 = pack_bf16(r8.x, r9.x);
-        const uint32_t b10 = pack_bf16(r0.y, r1.y), b11 = pack_bf16(r8.y, r9.y);
+        uint32_t b00, b01, b10, b11;
+        if (kS16) {
+          // the same operands as below: S[k][col], S[k][col + 1] share a word
+          const uint32_t w0 = ld_shared_u32(sS + s16_off(k0, col));
+          const uint32_t w1 = ld_shared_u32(sS + s16_off(k0 + 1, col));
+          const uint32_t w8 = ld_shared_u32(sS + s16_off(k0 + 8, col));
+          const uint32_t w9 = ld_shared_u32(sS + s16_off(k0 + 9, col));
+          b00 = __byte_perm(w0, w1, 0x5410);
+          b01 = __byte_perm(w8, w9, 0x5410);
+          b10 = __byte_perm(w0, w1, 0x7632);
+          b11 = __byte_perm(w8, w9, 0x7632);
+        } else {
+          const float2 r0 = ld_shared_v2f(sS + s_off(k0, col));
+          const float2 r1 = ld_shared_v2f(sS + s_off(k0 + 1, col));
+          const float2 r8 = ld_shared_v2f(sS + s_off(k0 + 8, col));
+          const float2 r9 = ld_shared_v2f(sS + s_off(k0 + 9, col));
+          b00 = pack_bf16(r0.x, r1.x);
+          b01 = pack_bf16(r8.x, r9.x);
+          b10 = pack_bf16(r0.y, r1.y);
+          b11 = pack_bf16(r8.y, r9.y);
+        }
         float (&acc)[2][2][4] = kk < 4 ? acc_p : acc_m;
 #pragma unroll
         for (int m2 = 0; m2 < 2; ++m2) {
@@ -1109,12 +1144,16 @@ bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per
          (int64_t)batch * rows_per_req < ((int64_t)1 << 31);
 }
 
-cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
-                               const void* k, const void* v, const float* S_pool,
+namespace {
+
+// Both entry points: S_pool is the fp32 pool, or with state_bf16 its bf16
+// copy (attend only).
+cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
+                               const void* k, const void* v, const void* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all, bool sequential) {
+                               bool commit_all, bool sequential, bool state_bf16) {
   Maps maps;
   maps.rows_per_req = rows_per_req;
   maps.row_base = row_base;
@@ -1125,10 +1164,11 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   maps.w = static_cast<const uint8_t*>(W);
   {
     const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
-    const uint64_t strides[1] = {kD * 4};
-    const uint32_t box[2] = {32, 128};
-    if (!encode_tmap(&maps.S, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S_pool, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t strides[1] = {(uint64_t)kD * (state_bf16 ? 2 : 4)};
+    const uint32_t box[2] = {state_bf16 ? 64u : 32u, 128};
+    if (!encode_tmap(&maps.S,
+                     state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     2, S_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
@@ -1150,7 +1190,8 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto* kernel = sequential ? k_attend_fast<true, true>
+  auto* kernel = state_bf16 ? k_attend_fast<false, false, true>
+                 : sequential ? k_attend_fast<true, true>
                  : (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1161,9 +1202,31 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   // its prompt's blocks in order
   const int grid = sequential ? units : (units < num_sms ? units : num_sms);
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, maps, batch, s.H,
-                    num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask, S_pool,
-                    const_cast<float*>(Z_pool), gate, reinterpret_cast<__nv_bfloat16*>(o),
-                    status);
+                    num_slots, s.scale * kLog2e, s.merge, slot_idx, commit_mask,
+                    static_cast<const float*>(S_pool), const_cast<float*>(Z_pool), gate,
+                    reinterpret_cast<__nv_bfloat16*>(o), status);
+}
+
+}  // namespace
+
+cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
+                               const void* k, const void* v, const float* S_pool,
+                               const float* Z_pool, int num_slots, const void* W,
+                               const float* gate, const int32_t* commit_mask, void* o,
+                               unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
+                               bool commit_all, bool sequential) {
+  return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
+                            commit_mask, o, status, st, rows_per_req, row_base, commit_all,
+                            sequential, false);
+}
+
+cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slot_idx,
+                                   const void* q, const void* k, const void* v,
+                                   const void* S16_pool, const float* Z_pool, int num_slots,
+                                   const void* W, const float* gate, void* o, unsigned* status,
+                                   cudaStream_t st) {
+  return launch_attend_impl(s, batch, slot_idx, q, k, v, S16_pool, Z_pool, num_slots, W, gate,
+                            nullptr, o, status, st, kL, 0, false, false, true);
 }
 
 }  // namespace hb

@@ -1,0 +1,28 @@
+// A bf16 copy of the state pool for the attend's read (hb_state_to_bf16,
+// hb_block_attend_s16). Internal to libhb.so; the public signatures are in
+// include/hb.h.
+//
+// The attend's state contraction takes S as bf16 operands rounded to nearest
+// from the fp32 state, so a copy holding exactly those rounded values gives
+// bit-identical outputs while the read of S halves. The fp32 pool stays the
+// master that commits and prompt ingestion update.
+#pragma once
+
+#include "hb_internal.cuh"
+
+namespace hb {
+
+// S16[slot] = round-to-nearest bf16 of S[slot] for the listed slots; a slot
+// outside [0, num_slots) is skipped and flagged (hb_state_copy.cu).
+cudaError_t launch_state_to_bf16(const Shape& s, int batch, const int32_t* slot_idx,
+                                 const float* S_pool, void* S16_pool, int num_slots,
+                                 unsigned* status, cudaStream_t st);
+
+// hb_block_attend on the bf16 copy (production shape only; hb_attend_fast.cu).
+cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slot_idx,
+                                   const void* q, const void* k, const void* v,
+                                   const void* S16_pool, const float* Z_pool, int num_slots,
+                                   const void* W, const float* gate, void* o, unsigned* status,
+                                   cudaStream_t st);
+
+}  // namespace hb

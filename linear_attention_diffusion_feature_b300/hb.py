@@ -141,6 +141,49 @@ def hb_block_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logi
     return o
 
 
+def hb_state_to_bf16(cfg: Config, slot_idx, S_pool, S16_pool, stream=None) -> None:
+    """Writes the bf16 copy of the listed slots' S (round to nearest) that
+    hb_block_attend_s16 reads."""
+    B = slot_idx.shape[0]
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    if S_pool.dim() != 4:
+        raise ValueError("S_pool: expected [num_slots, H, F, d]")
+    num_slots = S_pool.shape[0]
+    shape = (num_slots, cfg.num_heads, cfg.F, cfg.head_dim)
+    _check(S_pool, "S_pool", torch.float32, shape)
+    _check(S16_pool, "S16_pool", torch.bfloat16, shape)
+    lib = _lib.load()
+    _raise(lib.hb_state_to_bf16(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(S_pool),
+                                _ptr(S16_pool), num_slots, _stream(stream)), "hb_state_to_bf16")
+
+
+def hb_block_attend_s16(cfg: Config, slot_idx, q, k, v, S16_pool, Z_pool, W, gate_logits,
+                        o=None, stream=None) -> torch.Tensor:
+    """hb_block_attend on the bf16 copy of S (bit-identical output, half the
+    state bytes); Z_pool is the fp32 master's."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    if S16_pool.dim() != 4:
+        raise ValueError("S16_pool: expected [num_slots, H, F, d]")
+    num_slots = S16_pool.shape[0]
+    _check(S16_pool, "S16_pool", torch.bfloat16, (num_slots, H, cfg.F, d))
+    _check(Z_pool, "Z_pool", torch.float32, (num_slots, H, cfg.F))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_s16(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(S16_pool), _ptr(Z_pool), num_slots, _ptr(W),
+                                   _ptr(gate_logits), _ptr(o), _stream(stream)),
+           "hb_block_attend_s16")
+    return o
+
+
 def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits,
                            commit, o=None, stream=None) -> torch.Tensor:
     """hb_block_attend, then hb_commit_block of the same block for the requests

@@ -1,0 +1,77 @@
+"""hb_block_attend_s16 on the bf16 copy of the states (GPU): the copy written
+by hb_state_to_bf16 is torch's round-to-nearest conversion of the fp32
+states bit for bit, and the attend's output on it is bit-identical to
+hb_block_attend's on the fp32 states, hence to the oracle within the bf16
+bound."""
+
+import pytest
+import torch
+
+import linear_attention_diffusion_feature_b300 as hb
+import oracle.block_hybrid as ob
+from linear_attention_diffusion_feature_b300 import inputs
+from tests.parity import TOL_OUT_BF16, assert_status_ok, config, f64, new_pool, out_err
+
+pytestmark = pytest.mark.gpu
+
+MERGES = {"shared_norm": hb.MERGE_SHARED_NORM, "convex": hb.MERGE_CONVEX}
+
+
+def _scattered_slots(B, spare, seed, device):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randperm(B + spare, generator=g)[:B].to(torch.int32).to(device)
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+@pytest.mark.parametrize("B", [64, 100])
+def test_attend_s16_is_bit_identical(cuda_device, merge, B):
+    w = inputs.continuous_batching(device=cuda_device, B=B, n_commit=0)
+    cfg = config(w, MERGES[merge])
+    t = w.tensors
+    S, Z = new_pool(cfg, B + 5, cuda_device)
+    sl = _scattered_slots(B, 5, 11, cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S, Z)
+    S16 = torch.zeros(S.shape, dtype=torch.bfloat16, device=cuda_device)
+    hb.hb_state_to_bf16(cfg, sl, S, S16)
+    assert_status_ok()
+    idx = sl.long()
+    assert torch.equal(S16[idx], S[idx].to(torch.bfloat16))
+    unused = torch.ones(B + 5, dtype=torch.bool, device=cuda_device)
+    unused[idx] = False
+    assert bool((S16[unused] == 0).all())
+    o32 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
+    o16 = hb.hb_block_attend_s16(cfg, sl, t["q"], t["k"], t["v"], S16, Z, t["W"], t["gate"])
+    assert_status_ok()
+    assert torch.equal(o16, o32)
+    cu = t["cu_prefix"].cpu()
+    for b in (0, B - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        S_ref, Z_ref = ob.prefill(f64(t["prefix_k"][a:e]), f64(t["prefix_v"][a:e]), f64(t["W"]))
+        ref = ob.attend(f64(t["q"][b]), f64(t["k"][b]), f64(t["v"][b]), S_ref, Z_ref,
+                        f64(t["W"]), f64(t["gate"]), MERGES[merge])
+        assert out_err(f64(o16[b]), ref) <= TOL_OUT_BF16
+
+
+def test_attend_s16_bad_slot_flagged(cuda_device):
+    w = inputs.continuous_batching(device=cuda_device, B=4, lo=8, hi=9, n_commit=0)
+    cfg = config(w)
+    t = w.tensors
+    S, Z = new_pool(cfg, 4, cuda_device)
+    sl = torch.arange(4, dtype=torch.int32, device=cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S, Z)
+    S16 = torch.zeros(S.shape, dtype=torch.bfloat16, device=cuda_device)
+    hb.hb_state_to_bf16(cfg, torch.tensor([0, 1, 2, 9], dtype=torch.int32, device=cuda_device),
+                        S, S16)
+    assert hb.hb_get_device_status() == 5
+    assert bool((S16[3] == 0).all())
+    hb.hb_state_to_bf16(cfg, sl, S, S16)
+    assert_status_ok()
+    o = torch.full_like(t["q"], 7.0)
+    bad = torch.tensor([0, 4, 2, -1], dtype=torch.int32, device=cuda_device)
+    hb.hb_block_attend_s16(cfg, bad, t["q"], t["k"], t["v"], S16, Z, t["W"], t["gate"], o=o)
+    assert hb.hb_get_device_status() == 5
+    assert bool((o[1] == 7.0).all()) and bool((o[3] == 7.0).all())
+    ref = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
+    assert torch.equal(o[0], ref[0]) and torch.equal(o[2], ref[2])

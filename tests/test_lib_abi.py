@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(hb_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(hb_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -37,7 +37,7 @@ def test_header_declares_the_boundary():
 def test_every_declared_symbol_is_exported(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (hb_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (hb_[a-z0-9_]+)\b", out))
     missing = [n for n in declared_functions() if n not in exported]
     assert not missing, missing
     for name in declared_functions():
@@ -188,6 +188,25 @@ def test_state_copy_checks(lib):
     assert lib.hb_state_copy(ctypes.byref(c), 1, A, A, M, A, 4, None) == 3
     assert lib.hb_state_copy(ctypes.byref(_cfg(head_dim=8)), 1, A, A, A, A, 4, None) == 2
     assert lib.hb_state_copy(ctypes.byref(c), 0, None, None, None, None, 0, None) == 0
+
+
+def test_state_bf16_copy_checks(lib):
+    c = _cfg()
+    # hb_state_to_bf16: cfg, batch, slot_idx, S, S16, num_slots, stream
+    assert lib.hb_state_to_bf16(ctypes.byref(c), -1, A, A, A, 4, None) == 1
+    assert lib.hb_state_to_bf16(ctypes.byref(c), 1, A, A, None, 4, None) == 1
+    assert lib.hb_state_to_bf16(ctypes.byref(c), 1, A, M, A, 4, None) == 3
+    assert lib.hb_state_to_bf16(ctypes.byref(c), 0, None, None, None, 0, None) == 0
+    # hb_block_attend_s16: cfg, batch, slot_idx, q, k, v, S16, Z, num_slots, W, gate, o, stream
+    args = (A, A, A, A, A, A, 4, A, A, A, None)
+    assert lib.hb_block_attend_s16(ctypes.byref(c), -1, *args) == 1
+    assert lib.hb_block_attend_s16(ctypes.byref(_cfg(head_dim=64)), 1, *args) == 2
+    assert lib.hb_block_attend_s16(ctypes.byref(_cfg(dtype=1)), 1, *args) == 2
+    assert lib.hb_block_attend_s16(ctypes.byref(c), 1, A, A, A, A, None, A, 4, A, A, A,
+                                   None) == 1
+    assert lib.hb_block_attend_s16(ctypes.byref(c), 1, A, A, A, A, M, A, 4, A, A, A,
+                                   None) == 3
+    assert lib.hb_block_attend_s16(ctypes.byref(c), 0, *args) == 0
 
 
 def test_feature_map_checks(lib):
