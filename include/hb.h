@@ -145,8 +145,13 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch,
 /*
  * hb_state_to_bf16 — write the bf16 copy of the listed slots' S that
  * hb_block_attend_s16 reads: S16[slot] = round-to-nearest bf16 of S[slot].
- * Call it for a request's slot after every change to its fp32 state (a
- * prompt ingested, a block committed, a copy or a reset); Z needs no copy.
+ * Nothing keeps the copy in step with the fp32 master by itself. These calls
+ * change a slot's master and leave its copy stale: hb_commit_block,
+ * hb_block_attend_commit (committing requests), hb_prefill_state,
+ * hb_prefill_state_noalloc, hb_prefill_attend, hb_state_copy (destination
+ * slots) and hb_state_zero. After any of them, call hb_state_to_bf16 for the
+ * slots it changed before the next hb_block_attend_s16 on them; a missed
+ * refresh gives outputs computed from the old state. Z needs no copy.
  *   slot_idx  [batch] int32, device
  *   S_pool    [num_slots, H, F, d] fp32, read
  *   S16_pool  [num_slots, H, F, d] bf16, written for the listed slots only
@@ -251,10 +256,14 @@ hb_status hb_commit_block(const hb_config* cfg, int32_t batch,
                           float* Z_pool, int32_t num_slots, hb_stream_t stream);
 
 /*
- * hb_prefill_state — ingest prompts as committed context: the same sums as
- * hb_commit_block over every prompt token (the prompt precedes the first
- * generated block, so it is committed context; the sums are order-free, so
- * the chunking does not change the result).
+ * hb_prefill_state — ingest prompts as committed context (gist.science
+ * technical summary, "Methodology: Block-Hybrid Attention / Architecture
+ * Design", state-compression bullet: the state summarises all previously
+ * committed blocks, and a prompt precedes the first generated block;
+ * pith.science review, "What carries the argument": S and Z are plain sums
+ * over the committed tokens). The same sums as hb_commit_block over every
+ * prompt token; the sums are order-free, so the chunking does not change the
+ * result.
  *   k, v        [total_tokens, H, d] activation dtype, requests packed
  *               back to back (NULL allowed when total_tokens == 0)
  *   cu_seqlens  [batch + 1] int64, device: request b owns token rows
@@ -301,7 +310,11 @@ size_t hb_prefill_workspace_size(const hb_config* cfg, int32_t batch,
  *             other shape needs none.
  *   Set-up    the first call on a device that needs scratch looks up the
  *             array's device address (with that device current) and caches
- *             it; make that first call before any stream capture.
+ *             it; make that first call before any stream capture. Under
+ *             CUDA's lazy module loading (the default), that look-up may be
+ *             what loads the library's device code on that device, and with
+ *             it reserves the 10 MiB array there: the one-time device memory
+ *             cost falls on that first call, not on loading the library.
  *   Sharing   every call on a device uses the same array. Calls whose kernels
  *             overlap on the GPU (different streams, no ordering between
  *             them) race on it; order them on one stream or with events.
@@ -317,8 +330,17 @@ hb_status hb_prefill_state_noalloc(const hb_config* cfg, int32_t batch,
                                    int32_t num_slots, int32_t accumulate,
                                    hb_stream_t stream);
 
-/* hb_state_zero — clear S and Z of the listed slots (a new request with no
- * prompt, or a finished request's slot being recycled). */
+/*
+ * hb_state_zero — clear S and Z of the listed slots: the state of a request
+ * with no committed block yet (gist.science technical summary, state-
+ * compression bullet: the state summarises all previously committed blocks,
+ * so with none it is the empty sum, S = 0 and Z = 0; pith.science review,
+ * "What carries the argument": S_0 = 0, Z_0 = 0 before the first commit).
+ * Used for a new request with no prompt, or a finished request's slot being
+ * recycled.
+ *   slot_idx  [batch] int32, device; a slot outside [0, num_slots) is skipped
+ *             and flagged as HB_ERR_DEVICE_BOUNDS
+ */
 hb_status hb_state_zero(const hb_config* cfg, int32_t batch,
                         const int32_t* slot_idx, float* S_pool, float* Z_pool,
                         int32_t num_slots, hb_stream_t stream);

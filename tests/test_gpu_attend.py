@@ -125,13 +125,14 @@ def test_continuous_batching_step(cuda_device, merge):
             assert torch.equal(S[slot], S_before[slot]) and torch.equal(Z[slot], Z_before[slot])
 
 
+@pytest.mark.parametrize("merge", sorted(MERGES))
 @pytest.mark.parametrize("B", [1, 16, 256])
-def test_stack_layer(cuda_device, B):
+def test_stack_layer(cuda_device, B, merge):
     """One layer of the 6-layer stack shape (2,048-token prefixes), up to the
-    largest batch the stack is timed at (256 requests), sampled at the first,
-    middle and last request."""
+    largest batch the stack is timed at (256 requests), in both merges,
+    sampled at the first, middle and last request."""
     w = inputs.stack_layer(2, B, device=cuda_device)
-    cfg = config(w, hb.MERGE_SHARED_NORM)
+    cfg = config(w, MERGES[merge])
     t = w.tensors
     S, Z = new_pool(cfg, B, cuda_device)
     sl = slots(range(B), cuda_device)
@@ -144,7 +145,7 @@ def test_stack_layer(cuda_device, B):
         S_ref, Z_ref = ob.prefill(f64(t["prefix_k"][b * P:(b + 1) * P]),
                                   f64(t["prefix_v"][b * P:(b + 1) * P]), f64(t["W"]))
         ref = ob.attend(f64(t["q"][b]), f64(t["k"][b]), f64(t["v"][b]), S_ref, Z_ref,
-                        f64(t["W"]), f64(t["gate"]), hb.MERGE_SHARED_NORM)
+                        f64(t["W"]), f64(t["gate"]), MERGES[merge])
         assert out_err(f64(o[b]), ref) <= TOL_OUT_BF16
 
 

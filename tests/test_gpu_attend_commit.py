@@ -3,6 +3,8 @@ the call, and the committing requests' states then hold the oracle's commit
 of the same block; other slots are untouched. Also checked against the two
 separate calls (hb_block_attend, then hb_commit_block on the subset)."""
 
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -212,3 +214,77 @@ def test_attend_commit_many_units_per_cta(cuda_device):
     assert torch.equal(o1, o2)
     assert unit_err(f64(S), f64(S2), 2) <= TOL_STATE
     assert unit_err(f64(Z), f64(Z2), 2) <= TOL_STATE
+
+
+@functools.lru_cache(maxsize=2)
+def _oracle_inputs(B, H, seed, commit_frac=0.25, spare=5, max_prefix=64):
+    """Host side of a batch of B requests of the production shape: seeded
+    activations, states the oracle builds from short seeded prefixes
+    (0 .. max_prefix tokens), permuted slots of a pool with ``spare`` unused
+    slots, and a seeded commit mask (shared by both merges' tests)."""
+    d, f, L = 128, 64, 32
+    g = torch.Generator().manual_seed(seed)
+    W = (torch.randn((H, d, f), generator=g) * d ** -0.5).to(torch.bfloat16)
+    gate = torch.randn((H,), generator=g)
+    q, k, v = (torch.randn((B, L, H, d), generator=g).to(torch.bfloat16) for _ in range(3))
+    lens = torch.randint(0, max_prefix + 1, (B,), generator=g).tolist()
+    W64 = f64(W)
+    states = []
+    for n in lens:
+        pk = torch.randn((n, H, d), generator=g).to(torch.bfloat16)
+        pv = torch.randn((n, H, d), generator=g).to(torch.bfloat16)
+        states.append(ob.prefill(f64(pk), f64(pv), W64))
+    slot_of = torch.randperm(B + spare, generator=g)[:B]
+    commit = (torch.rand(B, generator=g) < commit_frac).to(torch.int32)
+    fill_S = torch.randn((B + spare, H, 2 * f, d), generator=g)  # slots no request names
+    fill_Z = torch.rand((B + spare, H, 2 * f), generator=g) + 1.0
+    return dict(W=W, gate=gate, q=q, k=k, v=v, states=states, slot_of=slot_of, commit=commit,
+                fill_S=fill_S, fill_Z=fill_Z, B=B, spare=spare)
+
+
+def _oracle_pool(c, device):
+    S = c["fill_S"].clone()
+    Z = c["fill_Z"].clone()
+    for b in range(c["B"]):
+        S[int(c["slot_of"][b])] = torch.as_tensor(c["states"][b][0], dtype=torch.float32)
+        Z[int(c["slot_of"][b])] = torch.as_tensor(c["states"][b][1], dtype=torch.float32)
+    return S.to(device), Z.to(device)
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+@pytest.mark.parametrize("B", [64, 320])
+def test_attend_commit_every_request_matches_oracle(cuda_device, merge, B):
+    """The fused step against the oracle on every request, not a sample: at 64
+    requests (the continuous-batching step) and at 320 requests, where every
+    CTA runs more than 32 units, so the unit table moves to a second window
+    and both ring stages wrap many times. Each output is checked against the
+    oracle's attend on the state as it was before the call; each committing
+    slot's S and Z against the oracle's commit; the other slots must be
+    untouched."""
+    c = _oracle_inputs(B, 16, seed=300 + B)
+    cfg = hb.Config(16, 128, 64, 32, merge=MERGES[merge])
+    S, Z = _oracle_pool(c, cuda_device)
+    S0, Z0 = S.clone(), Z.clone()
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    sl = c["slot_of"].to(torch.int32).to(cuda_device)
+    o = hb.hb_block_attend_commit(cfg, sl, dev(c["q"]), dev(c["k"]), dev(c["v"]), S, Z,
+                                  dev(c["W"]), dev(c["gate"]), dev(c["commit"]))
+    assert_status_ok()
+    W64, g64 = f64(c["W"]), f64(c["gate"])
+    o64, S64, Z64 = f64(o), f64(S), f64(Z)
+    named = set(int(x) for x in c["slot_of"])
+    for b in range(B):
+        S_old, Z_old = c["states"][b]
+        q64, k64, v64 = f64(c["q"][b]), f64(c["k"][b]), f64(c["v"][b])
+        ref = ob.attend(q64, k64, v64, S_old, Z_old, W64, g64, MERGES[merge])
+        assert out_err(o64[b], ref) <= TOL_OUT_BF16, b
+        slot = int(c["slot_of"][b])
+        if int(c["commit"][b]):
+            S_new, Z_new = ob.commit(S_old, Z_old, k64, v64, W64)
+            assert unit_err(S64[slot], S_new, 1) <= TOL_STATE, b
+            assert unit_err(Z64[slot], Z_new, 1) <= TOL_STATE, b
+        else:
+            assert torch.equal(S[slot], S0[slot]) and torch.equal(Z[slot], Z0[slot]), b
+    for slot in range(B + c["spare"]):
+        if slot not in named:
+            assert torch.equal(S[slot], S0[slot]) and torch.equal(Z[slot], Z0[slot]), slot

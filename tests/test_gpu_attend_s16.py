@@ -75,3 +75,43 @@ def test_attend_s16_bad_slot_flagged(cuda_device):
     assert bool((o[1] == 7.0).all()) and bool((o[3] == 7.0).all())
     ref = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
     assert torch.equal(o[0], ref[0]) and torch.equal(o[2], ref[2])
+
+
+def test_attend_s16_after_commits_and_refresh(cuda_device):
+    """The copy's life cycle in a decoding loop: the fp32 master changes
+    through hb_block_attend_commit (one subset of requests) and then through
+    hb_commit_block (another subset); after each change only the changed
+    slots' copies are refreshed, and the attend on the copies stays
+    bit-identical to the attend on the masters for every request."""
+    B = 64
+    w = inputs.continuous_batching(device=cuda_device, B=B, n_commit=16)
+    cfg = config(w)
+    t = w.tensors
+    S, Z = new_pool(cfg, B + 5, cuda_device)
+    sl = _scattered_slots(B, 5, 13, cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S, Z)
+    S16 = torch.zeros(S.shape, dtype=torch.bfloat16, device=cuda_device)
+    hb.hb_state_to_bf16(cfg, sl, S, S16)
+    # the fused step commits the first subset
+    ci = t["commit_idx"]
+    mask = torch.zeros(B, dtype=torch.int32, device=cuda_device)
+    mask[ci] = 1
+    S_before = S.clone()
+    hb.hb_block_attend_commit(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"], mask)
+    assert not torch.equal(S[sl[ci].long()], S_before[sl[ci].long()])
+    hb.hb_state_to_bf16(cfg, sl[ci].contiguous(), S, S16)
+    o32 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
+    o16 = hb.hb_block_attend_s16(cfg, sl, t["q"], t["k"], t["v"], S16, Z, t["W"], t["gate"])
+    assert_status_ok()
+    assert torch.equal(o16, o32)
+    # a separate commit of another subset (requests 1, 3, 5, ...)
+    other = torch.arange(1, B, 2, device=cuda_device)
+    hb.hb_commit_block(cfg, sl[other].contiguous(), t["q"][other].contiguous(),
+                       t["v"][other].contiguous(), t["W"], S, Z)
+    hb.hb_state_to_bf16(cfg, sl[other].contiguous(), S, S16)
+    o32 = hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
+    o16 = hb.hb_block_attend_s16(cfg, sl, t["q"], t["k"], t["v"], S16, Z, t["W"], t["gate"])
+    assert_status_ok()
+    assert torch.equal(o16, o32)
+    assert torch.equal(S16[sl.long()], S[sl.long()].to(torch.bfloat16))
