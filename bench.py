@@ -80,7 +80,8 @@ def _barrier(world):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples nvidia-smi clocks and throttle reasons while running; every
+    sample keeps its host time, so a summary can cover one window."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -89,7 +90,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []  # (host time, csv line)
 
     def __enter__(self):
         try:
@@ -100,19 +101,19 @@ class ClockSampler:
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
             t0 = time.time()
-            while not self.lines and time.time() - t0 < 5.0:  # sampler is up
+            while not self.samples and time.time() - t0 < 5.0:  # sampler is up
                 time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
         return self
 
     def mark(self):
-        """Start of the timed region: earlier samples are dropped."""
-        self.lines = []
+        """Start of the window of interest: earlier samples are dropped."""
+        self.samples = []
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -122,10 +123,14 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float = None, t1: float = None):
+        """Median SM clock, max clock and the throttle reasons seen, over the
+        samples taken between host times t0 and t1 (all samples if None)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in list(self.samples):
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -204,12 +209,63 @@ def make_layers(device, rank=0):
     return cfg, layers
 
 
+GRAPH_STEPS = 600  # most steps captured into one CUDA graph
+
+
+class StepGraphs:
+    """CUDA graphs of consecutive steps ``fn(0), fn(1), ...`` (the layer of
+    step i is i mod N_LAYERS), so that any number of steps runs as a few graph
+    replays with the host out of the loop: a graph of GRAPH_STEPS steps and
+    one of the remainder."""
+
+    def __init__(self, fn, n_steps: int):
+        self.fn = fn
+        self.full = self._capture(GRAPH_STEPS) if n_steps >= GRAPH_STEPS else None
+        rem = n_steps % GRAPH_STEPS
+        self.rem = self._capture(rem) if rem else None
+        self.n_full = n_steps // GRAPH_STEPS
+
+    def _capture(self, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                self.fn(i)
+        return g
+
+    def replay(self):
+        for _ in range(self.n_full):
+            self.full.replay()
+        if self.rem is not None:
+            self.rem.replay()
+
+
+def _busy(graph: "StepGraphs", seconds: float, per_replay_ms: float):
+    """Replays ``graph`` for about ``seconds`` of device time (no sync), to keep
+    the GPU under the step's load around a short timed region."""
+    n = max(1, int(seconds * 1e3 / max(per_replay_ms, 1e-3)))
+    for _ in range(n):
+        graph.replay()
+
+
+def _timed_replays(graph: "StepGraphs", n: int, stream) -> float:
+    """Device time of ``n`` replays of ``graph`` between two events (ms)."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
 def run_ours(args, world, rank, local):
     import linear_attention_diffusion_feature_b300 as hb
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     cfg, layers = make_layers(device, rank)
+    mean_prefix = layers[0]["mean_prefix"]
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -224,71 +280,59 @@ def run_ours(args, world, rank, local):
         hb.hb_block_attend(cfg, ly["slots"], ly["q"], ly["k"], ly["v"], ly["S"], ly["Z"],
                            ly["W"], ly["gate"], o=ly["o"])
 
-    # The layers' steps are captured into CUDA graphs, so the timed loop
-    # measures the device, not Python's launch overhead (~10 us per call
-    # through the ctypes binding): one graph runs the step of each of the
-    # N_LAYERS layer instances in turn (as one decoding step of the model
-    # does), one graph per layer serves a remainder of K mod N_LAYERS steps.
-    for i in range(args.warmup):
-        step(i)
-        attend_only(i)
-    torch.cuda.synchronize()
-
-    def capture(fn):
-        cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cycle):
-            for layer in range(N_LAYERS):
-                fn(layer)
-        singles = []
-        for layer in range(N_LAYERS):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn(layer)
-            singles.append(g)
-        return cycle, singles
-
-    def run_steps(graphs, k):
-        cycle, singles = graphs
-        for _ in range(k // N_LAYERS):
-            cycle.replay()
-        for layer in range(k % N_LAYERS):
-            singles[layer].replay()
-
+    # Warm-up steps through the binding, then the timed K steps captured into
+    # CUDA graphs (one graph of up to GRAPH_STEPS consecutive steps, layers in
+    # turn), so the timed region measures the device and not Python's launch
+    # overhead (~10 us per call through ctypes) and has no gaps between
+    # replays. A graph of GRAPH_STEPS steps keeps the GPU under the same load
+    # for ~0.3 s before and after the timed region, so that the clock samples
+    # (every 50 ms) describe the conditions the timed steps ran in, however
+    # short the timed region is.
     nvtx = torch.cuda.nvtx  # ranges for profilers (ncu --nvtx-include "timed/")
     nvtx.range_push("warmup")
-    step_graphs = capture(step)
-    attend_graphs = capture(attend_only)
-    run_steps(step_graphs, max(args.warmup, N_LAYERS))
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
+    timed = StepGraphs(step, args.steps)
+    filler = StepGraphs(step, GRAPH_STEPS)
+    timed.replay()
+    filler_ms = _timed_replays(filler, 1, stream)
     nvtx.range_pop()
 
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         _barrier(world)
+        torch.cuda.synchronize()
         clocks.mark()
+        t_begin = time.time()
+        _busy(filler, 0.3, filler_ms)
         nvtx.range_push("timed")
         start.record(stream)
-        run_steps(step_graphs, args.steps)
+        timed.replay()
         end.record(stream)
-        torch.cuda.synchronize()
         nvtx.range_pop()
+        _busy(filler, 0.3, filler_ms)
+        torch.cuda.synchronize()
+        t_end = time.time()
         _barrier(world)
-    total_ms = start.elapsed_time(end)
-    # each step is one launch of the step kernel, so its average launch
-    # duration is the timed region over K; the attend-only kernel is timed
-    # the same way for comparison
-    step_launch_ms = total_ms / args.steps
-    n_cmp = max(N_LAYERS, min(args.steps, 3000))
-    nvtx.range_push("attend_only")
-    run_steps(attend_graphs, N_LAYERS)
-    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a_ev.record(stream)
-    run_steps(attend_graphs, n_cmp)
-    b_ev.record(stream)
-    torch.cuda.synchronize()
-    nvtx.range_pop()
-    attend_only_ms = a_ev.elapsed_time(b_ev) / n_cmp
+        step_clocks = clocks.summary(t_begin, t_end)
+        total_ms = start.elapsed_time(end)
+        # each step is one launch of the step kernel, so its average launch
+        # duration is the timed region over K
+        step_launch_ms = total_ms / args.steps
+
+        # attend-only launches (hb_block_attend) for comparison, over >= 0.5 s
+        nvtx.range_push("attend_only")
+        attend_graph = StepGraphs(attend_only, GRAPH_STEPS)
+        attend_graph.replay()
+        one = _timed_replays(attend_graph, 1, stream)
+        n_rep = max(1, int(500.0 / one) + 1)
+        t0 = time.time()
+        attend_only_ms = _timed_replays(attend_graph, n_rep, stream) / (n_rep * GRAPH_STEPS)
+        attend_clocks = clocks.summary(t0, time.time())
+        nvtx.range_pop()
+        del attend_graph
     status = hb.hb_get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {hb.hb_status_string(status)}")
@@ -302,6 +346,23 @@ def run_ours(args, world, rank, local):
     nvtx.range_push("e2e")
     e2e = run_e2e(args, cfg, layers, device)
     nvtx.range_pop()
+    del layers
+    torch.cuda.empty_cache()
+
+    components = {
+        "step_launch_ms": step_launch_ms,
+        "attend_only_launch_ms": attend_only_ms,
+        "attend_only_hbm_frac": attend_bytes / (attend_only_ms / 1e3) / 1e9 / peak,
+        "attend_only_timing": f"{n_rep} replays of a {GRAPH_STEPS}-launch CUDA graph "
+                              f"({n_rep * GRAPH_STEPS} launches, >= 0.5 s)",
+        "attend_only_clocks": attend_clocks,
+        "commit_cost_ms": step_launch_ms - attend_only_ms,
+    }
+    if world == 1 and not args.no_components:
+        nvtx.range_push("components")
+        components["stack_b256"] = component_stack(args, device)
+        components["prefill_8x8192"] = component_prefill(args, device)
+        nvtx.range_pop()
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -314,7 +375,7 @@ def run_ours(args, world, rank, local):
                         "fp32 states; attend all 64 + commit 16 (hb_block_attend_commit)",
             "batch": B, "block_len": L, "heads": H, "head_dim": D, "feat_half": FH,
             "commit_per_step": N_COMMIT, "merge": "shared_norm",
-            "mean_prefix_tokens": layers[0]["mean_prefix"],
+            "mean_prefix_tokens": mean_prefix,
             "l2": f"steps cycle through {N_LAYERS} independent layer instances "
                   f"({N_LAYERS} x ~{(B * ATTEND_BYTES_PER_REQUEST) / 1e6:.0f} MB > 126 MB L2)",
             "parallelism": f"replicas x{world}",
@@ -327,21 +388,108 @@ def run_ours(args, world, rank, local):
             "launch_ms": step_launch_ms,
             "traffic": _traffic("hb_block_attend_commit"),
         },
-        "components": {
-            "step_launch_ms": step_launch_ms,
-            "attend_only_launch_ms": attend_only_ms,
-            "attend_only_hbm_frac": attend_bytes / (attend_only_ms / 1e3) / 1e9 / peak,
-            "commit_cost_ms": step_launch_ms - attend_only_ms,
-        },
+        "components": components,
         "e2e": e2e,
         "gpu_launches": args.steps,
-        "timing": "each step is one hb_block_attend_commit launch; the steps of the 6 layer "
-                  "instances are replayed from one CUDA graph; events around the timed region",
-        "clocks": clocks.summary(),
+        "timing": f"the K steps are one launch each, captured into CUDA graphs of up to "
+                  f"{GRAPH_STEPS} consecutive steps (layers in turn) and timed by events around "
+                  f"their replay; 0.3 s of the same steps run before and after, untimed",
+        "clocks": dict(step_clocks, window="samples every 50 ms over the timed region and the "
+                                           "0.3 s of identical steps on either side"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
     return line
+
+
+def component_stack(args, device, nB: int = 256, P: int = 2048):
+    """The largest single-GPU stack configuration: 6 linearized layers at 256
+    requests with 2,048-token prefixes, one stack step = 6 hb_block_attend
+    launches, against hb_softmax_kv_attend of the same 6 layers over the same
+    prefixes kept as a KV cache; each stack step is one CUDA graph, timed over
+    many replays."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    cfg = hb.Config(H, D, FH, L)
+    stream = torch.cuda.current_stream()
+    peak, _ = _peaks()
+    layers = []
+    for layer in range(N_LAYERS):
+        w = inputs.stack_layer(layer, nB, device=device, P=P)
+        t = w.tensors
+        S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
+        Z = torch.empty((nB, H, F), dtype=torch.float32, device=device)
+        sl = torch.arange(nB, dtype=torch.int32, device=device)
+        hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P, t["W"], S, Z)
+        need = hb.hb_softmax_kv_workspace_size(cfg, nB, P)
+        layers.append(dict(t=t, S=S, Z=Z, sl=sl, o=torch.empty_like(t["q"]),
+                           ws=torch.empty(max(need, 16), dtype=torch.uint8, device=device)))
+    torch.cuda.synchronize()
+
+    def hybrid():
+        for ly in layers:
+            t = ly["t"]
+            hb.hb_block_attend(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S"], ly["Z"], t["W"],
+                               t["gate"], o=ly["o"])
+
+    def softmax():
+        for ly in layers:
+            t = ly["t"]
+            hb.hb_softmax_kv_attend(cfg, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P, t["q"],
+                                    t["k"], t["v"], o=ly["o"], workspace=ly["ws"])
+
+    h_ms = _graph_ms(hybrid, 1, 800, args.warmup, stream)       # ~0.3 s
+    s_ms = _graph_ms(softmax, 1, 80, args.warmup, stream)       # ~0.3 s
+    assert hb.hb_get_device_status() == 0
+    hb_bytes = N_LAYERS * (nB * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W)
+    sm_bytes = N_LAYERS * nB * ((P + L) * H * D * 2 * 2 + 2 * L * H * D * 2)
+    del layers
+    torch.cuda.empty_cache()
+    return {"workload": f"6-layer stack, B={nB}, P={P}", "hybrid_ms": h_ms,
+            "hybrid_tokens_per_s": nB * L / (h_ms / 1e3),
+            "hybrid_hbm_frac": hb_bytes / (h_ms / 1e3) / 1e9 / peak,
+            "softmax_kv_ms": s_ms, "softmax_kv_tokens_per_s": nB * L / (s_ms / 1e3),
+            "softmax_kv_hbm_frac": sm_bytes / (s_ms / 1e3) / 1e9 / peak,
+            "speedup": s_ms / h_ms,
+            "timing": "one stack step (6 launches) per CUDA graph; 800 (hybrid) and 80 "
+                      "(softmax) replays between two events"}
+
+
+def component_prefill(args, device):
+    """Prompt ingestion (8 prompts x 8,192 tokens), one hb_prefill_state call
+    per CUDA graph, timed over ~0.3 s of replays."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    w = inputs.prompt_ingestion(device=device)
+    t = w.tensors
+    nB, T = w.meta["B"], w.meta["T"]
+    cfg = hb.Config(H, D, FH, L)
+    S = torch.empty((nB, H, F, D), dtype=torch.float32, device=device)
+    Z = torch.empty((nB, H, F), dtype=torch.float32, device=device)
+    sl = torch.arange(nB, dtype=torch.int32, device=device)
+    need = hb.hb_prefill_workspace_size(cfg, nB, T)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+    def call():
+        hb.hb_prefill_state(cfg, sl, t["k"], t["v"], t["cu_seqlens"], T, t["W"], S, Z,
+                            workspace=ws)
+
+    ms = _graph_ms(call, 1, 2000, args.warmup, torch.cuda.current_stream())
+    assert hb.hb_get_device_status() == 0
+    tokens = nB * T
+    nbytes = 2 * tokens * H * D * 2 + nB * H * (F * D + F) * 4 + H * D * FH * 2
+    flops = tokens * H * (2 * D * FH + 2 * 2 * F * D)
+    peak, _ = _peaks()
+    tpeak, _ = _tensor_peak()
+    del w, t, S, Z, ws
+    torch.cuda.empty_cache()
+    return {"workload": "hb_prefill_state, 8 prompts x 8,192 tokens, overwrite", "ms": ms,
+            "tokens_per_s": tokens / (ms / 1e3),
+            "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak,
+            "tensor_frac": flops / (ms / 1e3) / 1e12 / tpeak,
+            "timing": "one call per CUDA graph, 2000 replays between two events"}
 
 
 def run_e2e(args, cfg, layers, device):
@@ -349,8 +497,9 @@ def run_e2e(args, cfg, layers, device):
     copies that step's activations and per-request metadata host->device and
     reads o back. As a serving loop would, the copies run on their own
     streams, so step i's kernel overlaps step i+1's upload and step i-1's
-    download (device inputs are double-buffered); the timed region spans
-    every copy and kernel of every step."""
+    download (device inputs and host outputs are double-buffered); the timed
+    region spans every copy and kernel of every step. A layer's output buffer
+    is written again only after the download of its previous contents."""
     import linear_attention_diffusion_feature_b300 as hb
 
     ly0 = layers[0]
@@ -358,15 +507,16 @@ def run_e2e(args, cfg, layers, device):
     # the commit mask) come from the host each step
     names = ("q", "k", "v", "slots", "mask")
     host = {name: ly0[name].cpu().pin_memory() for name in names}
-    host_o = torch.empty_like(host["q"]).pin_memory()
+    host_o = [torch.empty_like(host["q"]).pin_memory() for _ in range(2)]
     dev = [{name: torch.empty_like(ly0[name]) for name in names} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = host_o.numel() * host_o.element_size()
+    d2h = host_o[0].numel() * host_o[0].element_size()
     up, comp, down = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
     n_steps = min(args.steps, 200)
     total = args.warmup + n_steps
     uploaded = [torch.cuda.Event() for _ in range(total)]
     computed = [torch.cuda.Event() for _ in range(total)]
+    downloaded = [torch.cuda.Event() for _ in range(total)]
 
     def step(i):
         ly = layers[i % N_LAYERS]
@@ -379,12 +529,18 @@ def run_e2e(args, cfg, layers, device):
             uploaded[i].record(up)
         with torch.cuda.stream(comp):
             comp.wait_event(uploaded[i])
+            if i >= N_LAYERS:
+                # the previous download of this layer's output buffer is done
+                comp.wait_event(downloaded[i - N_LAYERS])
             hb.hb_block_attend_commit(cfg, buf["slots"], buf["q"], buf["k"], buf["v"], ly["S"],
                                       ly["Z"], ly["W"], ly["gate"], buf["mask"], o=ly["o"])
             computed[i].record(comp)
         with torch.cuda.stream(down):
             down.wait_event(computed[i])
-            host_o.copy_(ly["o"], non_blocking=True)
+            if i >= 2:
+                down.wait_event(downloaded[i - 2])  # host buffer i % 2 is free again
+            host_o[i % 2].copy_(ly["o"], non_blocking=True)
+            downloaded[i].record(down)
 
     torch.cuda.synchronize()
     for i in range(args.warmup):
@@ -400,6 +556,9 @@ def run_e2e(args, cfg, layers, device):
     end.record(down)  # after the last download, which waits on every stream's last work
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / n_steps
+    last = total - 1
+    # the last download holds that step's own output
+    assert torch.equal(host_o[last % 2], layers[last % N_LAYERS]["o"].cpu())
     return {"value": B * L / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "overlap": "upload, kernel and download on separate streams"}
@@ -518,8 +677,11 @@ def run_prefill(args):
 
 
 def run_decode(args):
-    """Single-layer decode step: 1 request, 16 heads, 2,048-token state,
-    one hb_block_attend (latency) and one hb_commit_block."""
+    """Single-layer decode, 1 request, 16 heads, 2,048-token state. The step
+    timed is the block's last denoising step: hb_block_attend_commit (attend
+    and commit of the finished block in one launch). Also reported: the
+    attend alone (every other denoising step of a block) and the same commit
+    as two launches (hb_block_attend, then hb_commit_block)."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
@@ -535,41 +697,50 @@ def run_decode(args):
         hb.hb_commit_block(cfg, sl, t["commit_k"][blk], t["commit_v"][blk], t["W"], S, Z)
     o = torch.empty_like(t["q"])
     stream = torch.cuda.current_stream()
+    one = torch.ones(1, dtype=torch.int32, device=device)
+    S1, Z1 = S.clone(), Z.clone()
+    S2, Z2 = S.clone(), Z.clone()
+
+    def fused():
+        hb.hb_block_attend_commit(cfg, sl, t["q"], t["k"], t["v"], S1, Z1, t["W"], t["gate"], one,
+                                  o=o)
 
     def attend():
         hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"], o=o)
 
-    S2, Z2 = S.clone(), Z.clone()
-
-    def commit():
+    def two_launches():
+        hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S2, Z2, t["W"], t["gate"], o=o)
         hb.hb_commit_block(cfg, sl, t["k"], t["v"], t["W"], S2, Z2)
 
     # launch-to-launch device time: 50 calls per CUDA graph, host out of the loop
     reps = max(1, args.steps // 50)
+    f_ms = _graph_ms(fused, 50, reps, args.warmup, stream)
     a_ms = _graph_ms(attend, 50, reps, args.warmup, stream)
-    c_ms = _graph_ms(commit, 50, reps, args.warmup, stream)
-    # the same calls issued one by one from Python, for context
-    a_host = _median(_timed(attend, min(args.steps, 200), args.warmup, stream))
+    t_ms = _graph_ms(two_launches, 50, reps, args.warmup, stream)
+    # the same call issued one by one from Python, for context
+    f_host = _median(_timed(fused, min(args.steps, 200), args.warmup, stream))
     assert hb.hb_get_device_status() == 0
-    nbytes = ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W
+    nbytes = ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W + H * (F * D + F) * 4
     peak, kind = _peaks()
     return {
-        "metric": "single-layer decode: active-block tokens/s (attend latency)",
-        "value": L / (a_ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": a_ms, "higher_is_better": True,
+        "metric": "single-layer decode: active-block tokens/s (committing step latency)",
+        "value": L / (f_ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": f_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "single-layer decode: 1 request, 16 heads, d=128, f=64, L=32, "
-                               "2,048-token state from 64 commits",
+                               "2,048-token state from 64 commits; step = attend + commit of "
+                               "the finished block (hb_block_attend_commit)",
                    "l2": "state 1 MB stays L2-resident between calls (latency measurement)"},
-        "roofline": {"kernel": "hb_block_attend", "bound": "hbm",
-                     "achieved": nbytes / (a_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": nbytes / (a_ms / 1e3) / 1e9 / peak, "peak_kind": kind,
-                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": a_ms,
+        "roofline": {"kernel": "hb_block_attend_commit", "bound": "hbm",
+                     "achieved": nbytes / (f_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": nbytes / (f_ms / 1e3) / 1e9 / peak, "peak_kind": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": f_ms,
                      "traffic": None},
-        "components": {"attend_us": a_ms * 1e3, "commit_us": c_ms * 1e3,
-                       "attend_us_eager_python": a_host * 1e3,
+        "components": {"attend_commit_fused_us": f_ms * 1e3, "attend_only_us": a_ms * 1e3,
+                       "attend_then_commit_two_launches_us": t_ms * 1e3,
+                       "fused_us_eager_python": f_host * 1e3,
                        "timing": "CUDA graph of 50 back-to-back calls, replayed"},
-        "gpu_launches": 2 * 50 * reps,
+        "gpu_launches": 4 * 50 * reps,
     }
 
 
@@ -682,6 +853,8 @@ def run_stack(args):
             "hybrid_s16_ms": h16_ms, "hybrid_s16_tokens_per_s": nB * L / (h16_ms / 1e3),
             "hybrid_s16_frac": hb16_bytes / (h16_ms / 1e3) / 1e9 / peak,
             "s16_speedup": h_ms / h16_ms,
+            "s16_note": "attend only, on copies written once before timing; the refresh a "
+                        "commit makes necessary (hb_state_to_bf16) is not in this number",
         })
         del layers
         torch.cuda.empty_cache()
@@ -1005,6 +1178,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true",
+                    help="skip the stack (B=256) and prompt-ingestion components of the "
+                         "default line")
     ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map", "psweep",
                              "prefill_attend"],
                     default="step",
@@ -1019,6 +1195,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = _dist()
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: for N > 1 GPUs launch one "
+                 f"process per GPU with torchrun (python -m torch.distributed.run "
+                 f"--nproc-per-node N ... bench.py --gpus N)")
     if args.impl == "reference":
         line = run_reference(args, world, rank)
         if line is not None:

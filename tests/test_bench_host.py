@@ -72,3 +72,13 @@ def test_bench_rejects_fewer_than_three_warmup_steps(argv):
 
     with pytest.raises(SystemExit):
         bench.main(argv)
+
+
+def test_bench_rejects_gpus_without_matching_world(monkeypatch):
+    """--gpus N must match the launcher's WORLD_SIZE (one process per GPU)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "2", "--no-cpu-baseline"])
