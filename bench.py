@@ -48,6 +48,12 @@ COMMIT_BYTES_PER_REQUEST = H * 2 * (F * D * 4 + F * 4) + 2 * L * H * D * 2
 # hb_block_attend_commit: the attend bytes, plus the write of S and Z for each
 # committing request (its state and block were already read by the attend).
 STEP_BYTES = B * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W + N_COMMIT * H * (F * D * 4 + F * 4)
+# hb_block_attend_commit_s16: a request that does not commit reads its bf16
+# copy of S (F*d bf16) instead of the fp32 master; a committing one reads the
+# master and writes the new master, Z and the new copy.
+ATTEND_S16_BYTES_PER_REQUEST = H * (F * D * 2 + F * 4) + 4 * L * H * D * 2
+DUAL_STEP_BYTES = ((B - N_COMMIT) * ATTEND_S16_BYTES_PER_REQUEST + ATTEND_BYTES_W
+                   + N_COMMIT * (ATTEND_BYTES_PER_REQUEST + H * (F * D * 4 + F * 4) + H * F * D * 2))
 
 
 def _dist():
@@ -346,6 +352,9 @@ def run_ours(args, world, rank, local):
     nvtx.range_push("e2e")
     e2e = run_e2e(args, cfg, layers, device)
     nvtx.range_pop()
+    nvtx.range_push("dual_copy")
+    dual = component_dual_copy(args, cfg, layers, stream)
+    nvtx.range_pop()
     del layers
     torch.cuda.empty_cache()
 
@@ -357,6 +366,7 @@ def run_ours(args, world, rank, local):
                               f"({n_rep * GRAPH_STEPS} launches, >= 0.5 s)",
         "attend_only_clocks": attend_clocks,
         "commit_cost_ms": step_launch_ms - attend_only_ms,
+        "step_dual_copy": dual,
     }
     if world == 1 and not args.no_components:
         nvtx.range_push("components")
@@ -400,6 +410,59 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
     return line
+
+
+def component_dual_copy(args, cfg, layers, stream):
+    """The same continuous-batching step on a pool that keeps a bf16 copy of
+    S beside each fp32 master: hb_block_attend_commit_s16 reads the copy for
+    the 48 requests that do not commit and the master for the 16 that do,
+    and writes the committing ones' new masters and copies (same output bits
+    as the fp32 step). For comparison, the same step built from the attend on
+    the copies plus a separate commit and copy refresh of the committing
+    slots (three launches). Each timed over >= 0.5 s of graph replays."""
+    import linear_attention_diffusion_feature_b300 as hb
+
+    peak, _ = _peaks()
+    for ly in layers:
+        ly["S16"] = torch.empty(ly["S"].shape, dtype=torch.bfloat16, device=ly["S"].device)
+        hb.hb_state_to_bf16(cfg, ly["slots"], ly["S"], ly["S16"])
+
+    def dual_step(i):
+        ly = layers[i % N_LAYERS]
+        hb.hb_block_attend_commit_s16(cfg, ly["slots"], ly["q"], ly["k"], ly["v"], ly["S"],
+                                      ly["S16"], ly["Z"], ly["W"], ly["gate"], ly["mask"],
+                                      o=ly["o"])
+
+    def refresh_step(i):
+        ly = layers[i % N_LAYERS]
+        hb.hb_block_attend_s16(cfg, ly["slots"], ly["q"], ly["k"], ly["v"], ly["S16"], ly["Z"],
+                               ly["W"], ly["gate"], o=ly["o"])
+        hb.hb_commit_block(cfg, ly["commit_slots"], ly["commit_k"], ly["commit_v"], ly["W"],
+                           ly["S"], ly["Z"])
+        hb.hb_state_to_bf16(cfg, ly["commit_slots"], ly["S"], ly["S16"])
+
+    out = {}
+    for name, fn, launches in (("fused", dual_step, 1), ("attend_commit_refresh", refresh_step, 3)):
+        for i in range(args.warmup):
+            fn(i)
+        g = StepGraphs(fn, GRAPH_STEPS)
+        g.replay()
+        one = _timed_replays(g, 1, stream)
+        n_rep = max(1, int(500.0 / one) + 1)
+        out[name + "_ms"] = _timed_replays(g, n_rep, stream) / (n_rep * GRAPH_STEPS)
+        out[name + "_launches_per_step"] = launches
+        del g
+    assert hb.hb_get_device_status() == 0
+    for ly in layers:
+        del ly["S16"]
+    ms = out["fused_ms"]
+    out.update({
+        "tokens_per_s": B * L / (ms / 1e3),
+        "algorithmic_bytes_per_launch": DUAL_STEP_BYTES,
+        "hbm_frac": DUAL_STEP_BYTES / (ms / 1e3) / 1e9 / peak,
+        "timing": "graphs of 600 steps (layers in turn), replayed for >= 0.5 s each",
+    })
+    return out
 
 
 def component_stack(args, device, nB: int = 256, P: int = 2048):

@@ -207,6 +207,35 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
                                  hb_stream_t stream);
 
 /*
+ * hb_block_attend_commit_s16 — hb_block_attend_commit for a pool that keeps,
+ * beside every slot's fp32 master S, the bf16 copy hb_state_to_bf16 writes
+ * (gist.science technical summary, state-compression bullet: the state is
+ * read every step and changes only when a block is committed; pith.science
+ * review, "What carries the argument": the read is O(Fd) per query). A
+ * request that does not commit reads its slot's copy (32 KiB per head
+ * instead of 64); a committing request reads the master, adds its block, and
+ * stores the new master and the new copy (round to nearest), so the copy
+ * stays in step without a separate hb_state_to_bf16 pass. While every listed
+ * slot's copy is the round-to-nearest of its master on entry, o, S_pool and
+ * Z_pool come out bit-identical to hb_block_attend_commit's on the masters.
+ * Production shape only (bf16, d = 128, f = 64, L = 32); any other shape
+ * returns HB_ERR_UNSUPPORTED_SHAPE.
+ *   S_pool    [num_slots, H, F, d] fp32 masters: read for committing
+ *             requests and written for them
+ *   S16_pool  [num_slots, H, F, d] bf16 copies: read for the others,
+ *             written for committing requests
+ *   other arguments as in hb_block_attend_commit.
+ */
+hb_status hb_block_attend_commit_s16(const hb_config* cfg, int32_t batch,
+                                     const int32_t* slot_idx, const void* q,
+                                     const void* k, const void* v, float* S_pool,
+                                     void* S16_pool, float* Z_pool,
+                                     int32_t num_slots, const void* W,
+                                     const float* gate_logits,
+                                     const int32_t* commit, void* o,
+                                     hb_stream_t stream);
+
+/*
  * hb_prefill_attend — a prompt processed block by block with block-hybrid
  * attention, so that every prompt token also gets its output (gist.science
  * technical summary, "Methodology: Block-Hybrid Attention / Architecture

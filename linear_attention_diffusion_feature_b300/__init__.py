@@ -15,6 +15,7 @@ from .hb import (  # noqa: F401
     HBError,
     hb_block_attend,
     hb_block_attend_commit,
+    hb_block_attend_commit_s16,
     hb_commit_block,
     hb_feature_map,
     hb_get_device_status,

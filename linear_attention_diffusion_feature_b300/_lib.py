@@ -50,6 +50,9 @@ SIGNATURES = {
     "hb_block_attend_commit": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p]),
+    "hb_block_attend_commit_s16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "hb_prefill_attend": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                     c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32,
                                     c_void_p, c_void_p]),

@@ -87,6 +87,12 @@ static_assert(kOffSums + 7 * 32 * 4 * 4 <= kOffV, "scratch overflows the k tile"
 // and lo, each 2 x [32 tokens][64 bf16] SWIZZLE_128B.
 constexpr int kOffPhiKHi = kOffW;
 constexpr int kOffPhiKLo = kOffW + 8192;
+// Dual-copy step, committing units only, once dS has been formed: the bf16
+// copy of the new S, 2 x [128 F-rows][64 bf16] SWIZZLE_128B, over the unit's
+// q, k, v tiles and the first half of W_h's (all dead by then).
+constexpr int kOffS16New = kOffQ;
+static_assert(kOffS16New % 1024 == 0 && kOffS16New + 2 * 16384 <= kStageStride,
+              "the copy's staging overflows the stage");
 // Shared area after the two stages.
 constexpr int kOffZ = 2 * kStageStride;     // 2 x [128] fp32 (per stage)
 constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, min of u(k): 5 x [32][4]
@@ -113,7 +119,9 @@ struct Maps {
   // the prompt length and the block's offset for chunkwise prompt
   // processing); commit_all: every request commits (commit_mask unused).
   int rows_per_req, row_base, commit_all;
-  CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16: bf16, box {64, 128}
+  const uint8_t* s16;  // dual-copy step: the bf16 copies (L2 prefetch of a unit's copy)
+  CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16 attend only: bf16, box {64, 128}
+  CUtensorMap S16;  // dual-copy step: the bf16 copies [slots*H*F rows][d], box {64, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
   CUtensorMap v;
@@ -154,6 +162,12 @@ __device__ __forceinline__ uint32_t v_off(int key, int n) {
 // round-to-nearest of the fp32 master. The state contraction takes S as bf16
 // operands rounded to nearest either way, so the output is bit-identical to
 // the fp32 pool's, while a unit reads 32 KiB of state instead of 64.
+// kS16 with kCommit (the dual-copy step): every slot has the fp32 master in
+// S_pool and its bf16 copy behind maps.S16. A request that does not commit
+// reads the copy; a committing request reads the master, adds its block,
+// and stores the new master and its round-to-nearest copy. The output bits
+// are those of the fp32-only step whenever the copies are in step with the
+// masters.
 template <bool kCommit, bool kSeq = false, bool kS16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
@@ -161,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int32_t* __restrict__ commit_mask, const float* __restrict__ S_pool,
                   float* __restrict__ Z_pool, const float* __restrict__ gate,
                   __nv_bfloat16* __restrict__ o, unsigned* status) {
-  static_assert(!(kS16 && (kCommit || kSeq)), "the bf16 state copy is read-only");
+  static_assert(!(kS16 && kSeq), "the sequential mode keeps the fp32 state on chip");
+  constexpr bool kDual = kS16 && kCommit;  // the dual-copy step
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -337,6 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bx = 0; bx < 4; ++bx)
               tma_store_2d(&maps.S, 32 * bx, row, st + kOffS + bx * 16384);
+            if (kDual) {
+              // the new state's bf16 copy, staged in the unit's dead head tiles
+#pragma unroll
+              for (int bx = 0; bx < 2; ++bx)
+                tma_store_2d(&maps.S16, 64 * bx, row, st + kOffS16New + bx * 16384);
+            }
             bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, smem + kOffZ + s * 512, kF * 4);
             bulk_commit();
             bulk_wait_read();
@@ -570,11 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     &head_full[s]);
           mbar_arrive(&head_full[s]);
           const int srow = (slot * H + h) * kF;
-          if (kS16) {
+          if (kS16 && !(kDual && (flags & kUnitCommit))) {
+            // the bf16 copy (a dual-copy step's committing unit reads the master)
             mbar_arrive_expect_tx(&s_full[s], kSBytes / 2);
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              tma_load_2d(st + kOffS + j * 16384, &maps.S, 64 * j, srow, &s_full[s]);
+              tma_load_2d(st + kOffS + j * 16384, kDual ? &maps.S16 : &maps.S, 64 * j, srow,
+                          &s_full[s]);
           } else {
             mbar_arrive_expect_tx(&s_full[s], kSBytes);
 #pragma unroll
@@ -585,11 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     auto l2_prefetch = [&](int i) {
-      const int b = unit_b(i), h = unit_h(i), slot = unit_slot(i);
+      const int b = unit_b(i), h = unit_h(i), slot = unit_slot(i), flags = unit_flags(i);
       if (lane != 0 || slot < 0 || slot >= num_slots) return;
       const size_t unit = (size_t)slot * H + h;
-      prefetch_l2(reinterpret_cast<const uint8_t*>(S_pool) + unit * kF * kD * (kS16 ? 2 : 4),
-                  kF * kD * (kS16 ? 2 : 4));
+      if (kDual && !(flags & kUnitCommit))
+        prefetch_l2(maps.s16 + unit * kF * kD * 2, kF * kD * 2);
+      else
+        prefetch_l2(reinterpret_cast<const uint8_t*>(S_pool) + unit * kF * kD * (kS16 && !kDual ? 2 : 4),
+                    kF * kD * (kS16 && !kDual ? 2 : 4));
       prefetch_l2(Z_pool + unit * kF, kF * 4);
       // the request's block of q, k, v is one contiguous range of L rows of
       // all heads; the CTAs working on its heads at the same time each
@@ -976,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int k0 = 16 * kk + 2 * t;
         uint32_t b00, b01, b10, b11;
-        if (kS16) {
+        if (kS16 && !cm) {
           // the same operands as below: S[k][col], S[k][col + 1] share a word
           const uint32_t w0 = ld_shared_u32(sS + s16_off(k0, col));
           const uint32_t w1 = ld_shared_u32(sS + s16_off(k0 + 1, col));
@@ -1091,6 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int F = 32 * (warp & 3) + lane;
       const int n0 = 64 * (warp >> 2);
       const uint32_t lane_bits = (uint32_t)(32 * (warp & 3)) << 16;
+      const uint32_t sS16New = smem_u32(st + kOffS16New);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float r[32];
@@ -1098,11 +1125,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const uint32_t a = sS + s_off(F, n0 + 32 * part + 4 * q4);
+          const int n = n0 + 32 * part + 4 * q4;
+          const uint32_t a = sS + s_off(F, n);
           const float4 old = ld_shared_v4f(a);
-          st_shared_v4(a, __float_as_uint(old.x + r[4 * q4]), __float_as_uint(old.y + r[4 * q4 + 1]),
-                       __float_as_uint(old.z + r[4 * q4 + 2]),
-                       __float_as_uint(old.w + r[4 * q4 + 3]));
+          const float4 nw = make_float4(old.x + r[4 * q4], old.y + r[4 * q4 + 1],
+                                        old.z + r[4 * q4 + 2], old.w + r[4 * q4 + 3]);
+          st_shared_v4(a, __float_as_uint(nw.x), __float_as_uint(nw.y), __float_as_uint(nw.z),
+                       __float_as_uint(nw.w));
+          if (kDual)  // the copy: round to nearest, as hb_state_to_bf16 does
+            st_shared_v2u(sS16New + s16_off(F, n), pack_bf16(nw.x, nw.y), pack_bf16(nw.z, nw.w));
         }
       }
       tc_fence_before();
@@ -1146,15 +1177,19 @@ bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per
 
 namespace {
 
-// Both entry points: S_pool is the fp32 pool, or with state_bf16 its bf16
-// copy (attend only).
+// Every entry point: S_pool is the fp32 pool, or with state_bf16 and no
+// commit its bf16 copy (attend only). S16_pool (dual-copy step, with a
+// commit mask): the bf16 copies beside the fp32 masters in S_pool.
 cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const void* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all, bool sequential, bool state_bf16) {
+                               bool commit_all, bool sequential, bool state_bf16,
+                               void* S16_pool = nullptr) {
+  const bool dual = S16_pool != nullptr;
   Maps maps;
+  maps.s16 = static_cast<const uint8_t*>(S16_pool);
   maps.rows_per_req = rows_per_req;
   maps.row_base = row_base;
   maps.commit_all = commit_all ? 1 : 0;
@@ -1169,6 +1204,15 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
     if (!encode_tmap(&maps.S,
                      state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      2, S_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    maps.S16 = maps.S;  // unused unless dual
+  }
+  if (dual) {
+    const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
+    const uint64_t strides[1] = {(uint64_t)kD * 2};
+    const uint32_t box[2] = {64u, 128};
+    if (!encode_tmap(&maps.S16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, S16_pool, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
@@ -1190,7 +1234,8 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto* kernel = state_bf16 ? k_attend_fast<false, false, true>
+  auto* kernel = dual         ? k_attend_fast<true, false, true>
+                 : state_bf16 ? k_attend_fast<false, false, true>
                  : sequential ? k_attend_fast<true, true>
                  : (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
@@ -1208,6 +1253,15 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
 }
 
 }  // namespace
+
+cudaError_t launch_attend_commit_dual(const Shape& s, int batch, const int32_t* slot_idx,
+                                      const void* q, const void* k, const void* v, float* S_pool,
+                                      void* S16_pool, float* Z_pool, int num_slots, const void* W,
+                                      const float* gate, const int32_t* commit_mask, void* o,
+                                      unsigned* status, cudaStream_t st) {
+  return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
+                            commit_mask, o, status, st, kL, 0, false, false, false, S16_pool);
+}
 
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,

@@ -25,4 +25,14 @@ cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slo
                                    const void* W, const float* gate, void* o, unsigned* status,
                                    cudaStream_t st);
 
+// hb_block_attend_commit with the bf16 copies beside the fp32 masters:
+// requests that do not commit read their copy, committing ones read the
+// master and store the new master and its copy (production shape only;
+// hb_attend_fast.cu).
+cudaError_t launch_attend_commit_dual(const Shape& s, int batch, const int32_t* slot_idx,
+                                      const void* q, const void* k, const void* v, float* S_pool,
+                                      void* S16_pool, float* Z_pool, int num_slots, const void* W,
+                                      const float* gate, const int32_t* commit_mask, void* o,
+                                      unsigned* status, cudaStream_t st);
+
 }  // namespace hb

@@ -208,6 +208,33 @@ def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, ga
     return o
 
 
+def hb_block_attend_commit_s16(cfg: Config, slot_idx, q, k, v, S_pool, S16_pool, Z_pool, W,
+                               gate_logits, commit, o=None, stream=None) -> torch.Tensor:
+    """hb_block_attend_commit on a pool with bf16 copies beside the fp32
+    masters: requests that do not commit read their copy, committing ones
+    read the master and write the new master and copy."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(commit, "commit", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    _check(S16_pool, "S16_pool", torch.bfloat16, (num_slots, H, cfg.F, d))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_commit_s16(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q),
+                                          _ptr(k), _ptr(v), _ptr(S_pool), _ptr(S16_pool),
+                                          _ptr(Z_pool), num_slots, _ptr(W), _ptr(gate_logits),
+                                          _ptr(commit), _ptr(o), _stream(stream)),
+           "hb_block_attend_commit_s16")
+    return o
+
+
 def hb_prefill_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits,
                       accumulate: bool = False, o=None, stream=None) -> torch.Tensor:
     """Prompts q/k/v [B, T, H, d] (T a multiple of L) processed block by

@@ -115,3 +115,72 @@ def test_attend_s16_after_commits_and_refresh(cuda_device):
     assert_status_ok()
     assert torch.equal(o16, o32)
     assert torch.equal(S16[sl.long()], S[sl.long()].to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+@pytest.mark.parametrize("B", [64, 320])
+def test_attend_commit_s16_equals_fp32_step(cuda_device, merge, B):
+    """The dual-copy step (copies read for requests that do not commit,
+    masters read and both written for committing ones) gives the fp32 step's
+    output, masters and Z bit for bit, leaves every listed slot's copy equal
+    to the round-to-nearest of its new master, and keeps doing so over a
+    second step with another commit mask. 320 requests make every CTA run
+    more than 32 units."""
+    w = inputs.continuous_batching(device=cuda_device, B=B, n_commit=B // 4, lo=2, hi=16)
+    cfg = config(w, MERGES[merge])
+    t = w.tensors
+    S, Z = new_pool(cfg, B + 5, cuda_device)
+    sl = _scattered_slots(B, 5, 17, cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S, Z)
+    S16 = torch.full(S.shape, 3.0, dtype=torch.bfloat16, device=cuda_device)
+    hb.hb_state_to_bf16(cfg, sl, S, S16)
+    S_ref, Z_ref = S.clone(), Z.clone()
+    g = torch.Generator().manual_seed(B)
+    idx = sl.long()
+    unused = torch.ones(B + 5, dtype=torch.bool, device=cuda_device)
+    unused[idx] = False
+    for step in range(2):
+        mask = (torch.rand(B, generator=g) < 0.25).to(torch.int32).to(cuda_device)
+        o_ref = hb.hb_block_attend_commit(cfg, sl, t["q"], t["k"], t["v"], S_ref, Z_ref, t["W"],
+                                          t["gate"], mask)
+        o = hb.hb_block_attend_commit_s16(cfg, sl, t["q"], t["k"], t["v"], S, S16, Z, t["W"],
+                                          t["gate"], mask)
+        assert_status_ok()
+        assert torch.equal(o, o_ref), step
+        assert torch.equal(S, S_ref), step
+        assert torch.equal(Z, Z_ref), step
+        assert torch.equal(S16[idx], S[idx].to(torch.bfloat16)), step
+        assert bool((S16[unused] == 3.0).all()), step
+
+
+@pytest.mark.parametrize("merge", sorted(MERGES))
+def test_attend_commit_s16_matches_oracle(cuda_device, merge):
+    """The dual-copy step against the oracle on every one of 64 requests:
+    outputs from the state before the call, and the committing slots' new
+    master and its copy from the oracle's commit."""
+    from tests.parity import TOL_STATE, unit_err
+    from tests.test_gpu_attend_commit import _oracle_inputs, _oracle_pool
+
+    c = _oracle_inputs(64, 16, seed=364)
+    cfg = hb.Config(16, 128, 64, 32, merge=MERGES[merge])
+    S, Z = _oracle_pool(c, cuda_device)
+    S16 = S.to(torch.bfloat16)
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    sl = c["slot_of"].to(torch.int32).to(cuda_device)
+    o = hb.hb_block_attend_commit_s16(cfg, sl, dev(c["q"]), dev(c["k"]), dev(c["v"]), S, S16, Z,
+                                      dev(c["W"]), dev(c["gate"]), dev(c["commit"]))
+    assert_status_ok()
+    W64, g64 = f64(c["W"]), f64(c["gate"])
+    o64, S64, S1664 = f64(o), f64(S), f64(S16)
+    for b in range(64):
+        S_old, Z_old = c["states"][b]
+        q64, k64, v64 = f64(c["q"][b]), f64(c["k"][b]), f64(c["v"][b])
+        ref = ob.attend(q64, k64, v64, S_old, Z_old, W64, g64, MERGES[merge])
+        assert out_err(o64[b], ref) <= TOL_OUT_BF16, b
+        if int(c["commit"][b]):
+            slot = int(c["slot_of"][b])
+            S_new, _ = ob.commit(S_old, Z_old, k64, v64, W64)
+            assert unit_err(S64[slot], S_new, 1) <= TOL_STATE, b
+            # the copy is the master rounded to bf16: within 2^-8 relative
+            assert unit_err(S1664[slot], S_new, 1) <= 2.0 ** -8, b
