@@ -464,6 +464,23 @@ hb_status hb_softmax_kv_attend_paged(const hb_config* cfg, int32_t batch,
  */
 hb_status hb_get_device_status(hb_stream_t stream);
 
+/*
+ * hb_set_wait_limit — fault injection for tests of the timeout path; the
+ * pages have no counterpart. Every wait inside the unit pipeline of the
+ * attend kernels (hb_block_attend, hb_block_attend_s16,
+ * hb_block_attend_commit, hb_block_attend_commit_s16, hb_prefill_attend)
+ * gives up after `cycles` SM clocks, records HB_ERR_TIMEOUT in the device
+ * status word, and the kernel winds down: it hands back no stage whose
+ * copies were not seen to land, and before exiting it waits, with the
+ * default limit, for the copies and tensor-core work it already issued.
+ * Work after the first wait that ran out is skipped, so outputs and states
+ * of that call are unspecified. cycles = 0 restores the default, 2^32 clocks
+ * (about 2 s), which no wait of a healthy call comes near; values above 2^40
+ * are clamped. Process-wide; it applies to launches made after the call and
+ * is not meant for production use. The other kernels keep the default.
+ */
+hb_status hb_set_wait_limit(uint64_t cycles);
+
 /* Static, NUL-terminated description of a status code. */
 const char* hb_status_string(hb_status status);
 

@@ -19,6 +19,7 @@ from .hb import (  # noqa: F401
     hb_commit_block,
     hb_feature_map,
     hb_get_device_status,
+    hb_set_wait_limit,
     hb_prefill_attend,
     hb_prefill_state,
     hb_prefill_state_noalloc,

@@ -82,6 +82,7 @@ SIGNATURES = {
                                              c_void_p, c_int32, c_void_p, c_int64, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                              c_void_p]),
+    "hb_set_wait_limit": (c_int32, [ctypes.c_uint64]),
     "hb_get_device_status": (c_int32, [c_void_p]),
     "hb_status_string": (ctypes.c_char_p, [c_int32]),
 }

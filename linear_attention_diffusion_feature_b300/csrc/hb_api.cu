@@ -3,6 +3,7 @@
 // or synchronises, except hb_get_device_status.
 #include <math.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -18,6 +19,11 @@ namespace hb {
 // Device-side fault bits (kStatusBounds, kStatusTimeout). One instance per
 // device context; kernels receive its device address as an argument.
 __device__ unsigned g_status_word;
+
+// Wait limit of the attend kernels' unit pipeline, in SM clocks
+// (hb_set_wait_limit; process-wide).
+static std::atomic<long long> g_wait_limit{1ll << 32};
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -457,6 +463,13 @@ hb_status hb_softmax_kv_attend_paged(const hb_config* cfg, int32_t batch, const 
   return hb::from_cuda(hb::launch_softmax_kv_paged(s, batch, k_pages, v_pages, pg, max_prefix, q,
                                                    k, v, o, workspace, status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hb_status hb_set_wait_limit(uint64_t cycles) {
+  constexpr uint64_t kDefault = 1ull << 32, kMax = 1ull << 40;
+  hb::g_wait_limit.store((long long)(cycles == 0 ? kDefault : (cycles > kMax ? kMax : cycles)),
+                         std::memory_order_relaxed);
+  return HB_OK;
 }
 
 hb_status hb_get_device_status(hb_stream_t stream) {

@@ -119,6 +119,9 @@ struct Maps {
   // the prompt length and the block's offset for chunkwise prompt
   // processing); commit_all: every request commits (commit_mask unused).
   int rows_per_req, row_base, commit_all;
+  // SM clocks after which a wait of the unit pipeline gives up (hb_set_wait_limit);
+  // the final drain of copies already issued always takes the full limit
+  long long wait_limit;
   const uint8_t* s16;  // dual-copy step: the bf16 copies (L2 prefetch of a unit's copy)
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16 attend only: bf16, box {64, 128}
   CUtensorMap S16;  // dual-copy step: the bf16 copies [slots*H*F rows][d], box {64, 128}
@@ -188,6 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_full = head_full + 10;    // committing units: the tensor cores' dS is in TMEM
   uint64_t* s_updated = head_full + 11;  // committing units: new S, Z are in the stage
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  // units whose tiles the producer has issued (read by the final drain)
+  volatile int* n_issued = reinterpret_cast<volatile int*>(smem + kOffTmemSlot + 4);
+  const long long lim = maps.wait_limit;
   int* meta = reinterpret_cast<int*>(smem + kOffMeta);
   float* pmax = reinterpret_cast<float*>(smem + kOffPart);  // [32][4]
   float* pmin = pmax + 128;                                 // [32][4]
@@ -212,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s_updated[0], kConsumerWarps);
     mbar_init(&s_updated[1], kConsumerWarps);
     fence_mbar_init();
+    *n_issued = 0;
   }
   // committing variant: 128 TMEM columns hold dS = phi(k)^T V [128 F][128 d]
   if (kCommit && warp == 0) tmem_alloc(tmem_slot, 128);
@@ -246,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dep_wait();
   grid_dep_launch();
+  int ds_issued = 0;  // thread 0: dS MMAs issued (committing units)
   // units of this CTA: every gridDim.x-th (request, head) unit, or in the
   // sequential mode the blocks of its (request, head)
   const int n_units_cta =
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t su_phase[2] = {0u, 0u};  // parity of s_updated per stage
     for (int i = 0; i < n_units_cta; ++i) {
       const int s = i & 1, n = i >> 1;
-      if (!mbar_wait(&sums_ready[s], n & 1)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sums_ready[s], n & 1, lim))) {
         if (lane == 0) atomicOr(status, kStatusTimeout);
         break;
       }
@@ -320,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the prompt's last block: store the state once the consumers have
         // updated it; every block: the row sums have been read
         if (meta[s] & kUnitLast) {
-          const bool ok = mbar_wait(&s_updated[s], su_phase[s]);
+          const bool ok = mbar_wait(&s_updated[s], su_phase[s], lim);
           su_phase[s] ^= 1u;
           if (lane == 0) {
             if (ok) {
@@ -341,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (kCommit && (meta[s] & kUnitCommit)) {
         // the consumers have written the new S and Z into the stage: store
         // them (TMA), and hand the stage back on their behalf once the store
-        // has read it
-        const bool ok = mbar_wait(&s_updated[s], su_phase[s]);
+        // has read it (not after a wait that ran out: the stage's loads may
+        // still be landing, so it is never refilled)
+        const bool ok = mbar_wait(&s_updated[s], su_phase[s], lim);
         su_phase[s] ^= 1u;
         if (lane == 0) {
           if (ok) {
@@ -361,19 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_store(Z_pool + (size_t)(uslot * H + h) * kF, smem + kOffZ + s * 512, kF * 4);
             bulk_commit();
             bulk_wait_read();
+            mbar_arrive_cnt(&empty[s], kConsumerWarps + 1);
           } else {
             atomicOr(status, kStatusTimeout);
           }
-          mbar_arrive_cnt(&empty[s], kConsumerWarps + 1);
         }
       } else if (lane == 0) {
         mbar_arrive(&empty[s]);  // the row sums in the stage have been read
       }
     }
-    return;
-  }
-
-  if (warp == kProducerWarp) {
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; lane 0 issues the copies. A unit's q, k,
     // v and W_h do not depend on its state slot, so the first unit's are
@@ -400,12 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_local; ++i) {
         const int s = i & 1, n = i >> 1;
         bool ok = true;
-        if (lane == 0 && n > 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
+        if (lane == 0 && n > 0) ok = mbar_wait(&empty[s], (n - 1) & 1, lim);
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
           if (lane == 0) atomicOr(status, kStatusTimeout);
           break;
         }
         if (lane == 0) {
+          *n_issued = i + 1;
           uint8_t* st = smem + s * kStageStride;
           const int row = b * maps.rows_per_req + i * kL;
           mbar_expect_tx(&head_full[s], kHeadBytes);
@@ -450,8 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      return;
-    }
+    } else {
     // Unit schedule. Position p = first + i * stride of the grid-wide order
     // is this CTA's i-th unit. Committing requests are heavier (their state
     // is also updated and stored), so in the committing variant their units
@@ -559,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = unit_b(i), h = unit_h(i);
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
+        *n_issued = i + 1;  // issue_state(i) always follows
         mbar_expect_tx(&head_full[s], kHeadBytes);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -636,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n_local > 1) {
       issue_head(1);
-      if (lane == 0) mbar_wait(&s_full[0], 0);  // a wait that runs out only delays
+      if (lane == 0) mbar_wait(&s_full[0], 0, lim);  // a wait that runs out only delays
       __syncwarp();
       issue_state(1);
     }
@@ -649,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         win_next = fill_window(win_base + 1);
       }
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[s], (n - 1) & 1);
+      if (lane == 0) ok = mbar_wait(&empty[s], (n - 1) & 1, lim);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
         if (lane == 0) atomicOr(status, kStatusTimeout);
         break;
@@ -658,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_state(i);
       if (i + 1 < n_local) l2_prefetch(i + 1);
     }
-    return;
-  }
+    }  // non-sequential producer
+  } else {
 
   // -------------------------------------------------------------- consumers
   // Warp w: row tile mt = w & 1 (rows 16 mt .. 16 mt + 15), column quarter
@@ -679,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t cm_phase = 0;  // parity of ds_full for the next committing unit
   for (; i < n_units_cta; ++i) {
     const int s = i & 1, n = i >> 1;
-    const bool head_ok = mbar_wait(&head_full[s], n & 1);
+    const bool head_ok = mbar_wait(&head_full[s], n & 1, lim);
     uint8_t* st = smem + s * kStageStride;
     // the sequential mode keeps one state, in the first stage's buffers
     const uint32_t sS = smem_u32(kSeq ? smem + kOffS : st + kOffS);
@@ -979,13 +986,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tbase, aLo, bV, idS, 1u);
         }
         umma_commit(ds_full);
+        ++ds_issued;
       }
     }
 
     // ---- phase D: num+- = e+- S and U = P V for columns 16w .. 16w + 15
     // (a unit with a bad slot, flagged by the producer, runs on stale bytes
     // and writes nothing)
-    const bool s_ok = mbar_wait(&s_full[s], n & 1);
+    const bool s_ok = mbar_wait(&s_full[s], n & 1, lim);
     const int valid = meta[s];  // read before the stage is handed back
     float acc_p[2][2][4] = {}, acc_m[2][2][4] = {}, acc_v[2][2][4] = {};
     {
@@ -1051,24 +1059,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the stage is no longer read: hand it back to the producer (a
     // committing unit keeps it until its new S has been stored)
+    // (only once this lane has seen the stage's loads land: after a wait that
+    // ran out, the stage is never handed back, so no copy is issued into it
+    // while an earlier one may still be landing)
+    bool release_ok = s_ok;
     if (kSeq && cm) {
       // the stage's V and phi(k) are read by the dS MMA; once it is done,
       // the stage (q, k, v, W_h) is free: the state lives elsewhere
-      const bool ds_ok = mbar_wait(ds_full, cm_phase);
+      const bool ds_ok = mbar_wait(ds_full, cm_phase, lim);
       cm_phase ^= 1u;
       if (!ds_ok) {
         late_fail = true;
+        release_ok = false;
         if (lane == 0) atomicOr(status, kStatusTimeout);
       }
     }
     __syncwarp();
-    if (lane == 0 && (kSeq || !cm)) mbar_arrive(&empty[s]);
+    if (lane == 0 && (kSeq || !cm) && release_ok) mbar_arrive(&empty[s]);
     if (!s_ok) {
       late_fail = true;  // voted on at the next unit's first barrier
       if (lane == 0) atomicOr(status, kStatusTimeout);
     }
     if (!(valid & kUnitValid)) continue;
-    if (!mbar_wait(&fin_ready[s], n & 1)) {
+    if (!mbar_wait(&fin_ready[s], n & 1, lim)) {
       late_fail = true;
       if (lane == 0) atomicOr(status, kStatusTimeout);
     }
@@ -1106,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // once every warp's state contraction has finished reading it
       named_bar_sync(1, kConsumers);
       if (!kSeq) {
-        const bool ds_ok = mbar_wait(ds_full, cm_phase);
+        const bool ds_ok = mbar_wait(ds_full, cm_phase, lim);
         cm_phase ^= 1u;
         if (!ds_ok) {
           late_fail = true;
@@ -1143,26 +1156,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!kSeq || (flags & kUnitLast)) {
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_updated[s]);
+        // (not after the stage's state load ran out: the coefficient warp's
+        // wait then runs out too, and the stage is never refilled)
+        if (lane == 0 && s_ok) mbar_arrive(&s_updated[s]);
       }
     }
   }
-  if (aborted && threadIdx.x == 0) {
-    // let the copies of this unit and the next, if issued, land before the
-    // CTA exits (each wait is bounded too)
-    for (int j = i; j <= i + 1 && j < n_units_cta; ++j) {
+  (void)aborted;
+  }  // consumers
+
+  // Every warp has left its loop (each wait is bounded), so the producer has
+  // issued everything it will. A stage is refilled only after its previous
+  // loads were seen to land, so only the last unit issued into each stage can
+  // still have copies in flight: wait for those (full limit) so that no copy
+  // lands in the shared memory of an exited CTA, and for the last dS MMA
+  // before its tensor memory is freed.
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int issued = *n_issued;
+    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
       mbar_wait(&head_full[j & 1], (j >> 1) & 1);
       mbar_wait(&s_full[j & 1], (j >> 1) & 1);
     }
+    if (kCommit && ds_issued > 0) mbar_wait(ds_full, (uint32_t)(ds_issued - 1) & 1u);
   }
-  if (kCommit) {
-    // every consumer is past its last TMEM read (all leave the loop together)
-    tc_fence_before();
-    named_bar_sync(1, kConsumers);
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(tbase, 128);
-    }
+  if (kCommit && warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
   }
 }
 
@@ -1191,6 +1213,7 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
   Maps maps;
   maps.s16 = static_cast<const uint8_t*>(S16_pool);
   maps.rows_per_req = rows_per_req;
+  maps.wait_limit = wait_limit_cycles();
   maps.row_base = row_base;
   maps.commit_all = commit_all ? 1 : 0;
   maps.qkv[0] = static_cast<const uint8_t*>(q);

@@ -132,5 +132,8 @@ cudaError_t launch_softmax_kv_generic(const Shape& s, int batch, const void* k_c
 cudaError_t ensure_smem_attr(const void* fn, int bytes);
 // Streaming multiprocessors of the current device (cached per device).
 cudaError_t current_sm_count(int* n);
+// SM clocks after which a wait of the attend kernels' unit pipeline gives up
+// (hb_set_wait_limit).
+long long wait_limit_cycles();
 
 }  // namespace hb

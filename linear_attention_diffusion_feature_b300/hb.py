@@ -417,6 +417,12 @@ def hb_softmax_kv_attend_paged(cfg: Config, k_pages, v_pages, page_table, prefix
     return o
 
 
+def hb_set_wait_limit(cycles: int) -> None:
+    """Test hook: the attend kernels' pipeline waits give up after ``cycles``
+    SM clocks (0 restores the default); process-wide."""
+    _raise(_lib.load().hb_set_wait_limit(int(cycles)), "hb_set_wait_limit")
+
+
 def hb_get_device_status(stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device status code."""
     return int(_lib.load().hb_get_device_status(_stream(stream)))

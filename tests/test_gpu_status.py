@@ -112,3 +112,55 @@ def test_tensors_on_another_device_are_refused(cuda_device, monkeypatch):
     torch.cuda.synchronize()
     assert bool((o == 7.0).all())
     assert hb.hb_get_device_status() == 0
+
+
+TIMEOUT = 6
+
+
+@pytest.mark.parametrize("variant", ["attend", "attend_commit", "prefill_attend"])
+def test_wait_that_runs_out_is_reported_and_the_context_survives(cuda_device, variant):
+    """Failure detection without a GPU fault: with the pipeline's wait limit
+    lowered to a few clocks, the waits of the attend kernels run out before
+    their copies land. The call must end on its own, report HB_ERR_TIMEOUT
+    through the status word, and leave the context usable: with the default
+    limit back, the same call on fresh inputs gives the bits a call before
+    the fault gave."""
+    B = 64 if variant != "prefill_attend" else 4
+    w = inputs.continuous_batching(device=cuda_device, B=B, lo=2, hi=8, n_commit=B // 4)
+    cfg = config(w)
+    t = w.tensors
+    S0, Z0 = new_pool(cfg, B, cuda_device)
+    sl = slots(range(B), cuda_device)
+    hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                        w.meta["max_prefix"], t["W"], S0, Z0)
+    mask = torch.zeros(B, dtype=torch.int32, device=cuda_device)
+    mask[t["commit_idx"]] = 1
+    if variant == "prefill_attend":
+        g = torch.Generator().manual_seed(9)
+        q, k, v = (torch.randn((B, 8 * 32, 16, 128), generator=g).to(torch.bfloat16)
+                   .to(cuda_device) for _ in range(3))
+
+    def call(S, Z):
+        if variant == "attend":
+            return hb.hb_block_attend(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"], t["gate"])
+        if variant == "attend_commit":
+            return hb.hb_block_attend_commit(cfg, sl, t["q"], t["k"], t["v"], S, Z, t["W"],
+                                             t["gate"], mask)
+        return hb.hb_prefill_attend(cfg, sl, q, k, v, S, Z, t["W"], t["gate"])
+
+    S1, Z1 = S0.clone(), Z0.clone()
+    ref = call(S1, Z1)
+    assert_status_ok()
+    hb.hb_set_wait_limit(2)
+    try:
+        S2, Z2 = S0.clone(), Z0.clone()
+        call(S2, Z2)
+        status = hb.hb_get_device_status()
+    finally:
+        hb.hb_set_wait_limit(0)
+    assert status == TIMEOUT
+    S3, Z3 = S0.clone(), Z0.clone()
+    again = call(S3, Z3)
+    assert_status_ok()
+    assert torch.equal(again, ref)
+    assert torch.equal(S3, S1) and torch.equal(Z3, Z1)
