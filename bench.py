@@ -1096,6 +1096,50 @@ def run_prefill_attend(args):
     }
 
 
+def run_serve(args):
+    """Continuous-batching simulation on the library's own calls (the pages'
+    end-to-end protocol on synthetic layers): the same stream of requests
+    (2,048 generated tokens each, prompts of 128-512 tokens, 8 denoising
+    steps per block) served by the hybrid layers (fixed-size states) and by
+    the same layers as softmax over a paged KV cache, at each concurrency cap
+    of the sweep, under one attention-memory budget for the 20-layer model."""
+    from linear_attention_diffusion_feature_b300 import serving
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    sweep = []
+    for C in args.serve_concurrency:
+        cfg = serving.ServeConfig(n_requests=max(2 * C, 4), max_concurrency=C,
+                                  memory_budget=args.serve_budget_gib << 30)
+        res = serving.compare(cfg, device)
+        res["max_concurrency"] = C
+        res["n_requests"] = cfg.n_requests
+        sweep.append(res)
+        torch.cuda.empty_cache()
+    import linear_attention_diffusion_feature_b300 as hb
+
+    assert hb.hb_get_device_status() == 0
+    top = sweep[-1]
+    return {
+        "metric": "continuous-batching simulation: generated tokens/s, hybrid vs softmax "
+                  "attention layers", "value": top["hybrid"]["tokens_per_s_wall"],
+        "unit": "tokens/s", "n_gpus": 1, "steps": top["hybrid"]["steps"], "warmup": 0,
+        "ms_per_step": top["hybrid"]["wall_s"] * 1e3 / max(top["hybrid"]["steps"], 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "6 attention layers (16 heads, d=128, f=64, L=32) served with "
+                               "continuous batching; 2,048 generated tokens per request, prompts "
+                               "32*U{4..16} tokens, 8 denoising steps per block; memory model: "
+                               "20-layer model, 6 linearized",
+                   "memory_budget_gib": args.serve_budget_gib,
+                   "concurrency": args.serve_concurrency,
+                   "timing": "wall clock around the whole stream (host scheduling included) "
+                             "and the sum of per-step CUDA-event times"},
+        "sweep": sweep,
+        "gpu_launches": None,
+    }
+
+
 def cpu_baseline_prefill(max_seconds: float = 15.0, T: int = 256):
     """The oracle's prefill on one 256-token prompt of the same shape."""
     import numpy as np
@@ -1245,12 +1289,14 @@ def main(argv=None):
                     help="skip the stack (B=256) and prompt-ingestion components of the "
                          "default line")
     ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map", "psweep",
-                             "prefill_attend"],
+                             "prefill_attend", "serve"],
                     default="step",
                     help="step: continuous-batching step (default); decode: single-layer "
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
                          "softmax over a KV cache; feature_map: standalone phi")
     ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
+    ap.add_argument("--serve-concurrency", type=int, nargs="+", default=[1, 16, 64, 128])
+    ap.add_argument("--serve-budget-gib", type=int, default=40)
     ap.add_argument("--psweep-batches", type=int, nargs="+", default=[1, 64])
     ap.add_argument("--psweep-prefixes", type=int, nargs="+",
                     default=[1024, 2048, 4096, 8192, 16384, 32768])
@@ -1272,7 +1318,7 @@ def main(argv=None):
             ap.error("--workload other than step runs on one GPU")
         runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack,
                   "feature_map": run_feature_map, "psweep": run_psweep,
-                  "prefill_attend": run_prefill_attend}
+                  "prefill_attend": run_prefill_attend, "serve": run_serve}
         print(json.dumps(runner[args.workload](args)), flush=True)
         return 0
     if world > 1:
