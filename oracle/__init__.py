@@ -10,11 +10,14 @@ from .block_hybrid import (  # noqa: F401
     MERGE_CONVEX,
     MERGE_SHARED_NORM,
     attend,
+    attend_gqa,
     attend_bruteforce,
     commit,
     feature_map,
     gather_pages,
+    kv_head,
     prefill,
+    prefill_attend,
     sigmoid,
     softmax_kv_attend,
     softmax_kv_attend_paged,

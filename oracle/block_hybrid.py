@@ -228,8 +228,41 @@ def attend_bruteforce(q, k, v, k_prev, v_prev, W, gate,
     return o
 
 
+def kv_head(h: int, H: int, H_kv: int) -> int:
+    """The key/value head that query head h reads under grouped-query
+    attention: query heads come in H_kv consecutive groups of H / H_kv, and
+    group g shares key/value head g. The pages do not speak of head counts
+    (the specification's layers have H_kv = H); this is the usual grouping,
+    in which a layer with fewer key/value heads stores one state per
+    key/value head."""
+    if H % H_kv != 0:
+        raise ValueError("the number of key/value heads must divide the number of query heads")
+    return h // (H // H_kv)
+
+
+def attend_gqa(q, k, v, S, Z, Wq, gate, merge: int = MERGE_SHARED_NORM, scale=None):
+    """``attend`` with grouped query heads: every query head h is ``attend``
+    of that one head against key/value head g = kv_head(h, H, H_kv), that is
+    the block's keys and values of head g and the state (S, Z) of head g,
+    with its own query map Wq[h] and gate[h].
+
+    q [L, H, d], Wq [H, d, f], gate [H]; k/v [L, H_kv, d], S [H_kv, F, d],
+    Z [H_kv, F]. Returns o [L, H, d] in float64.
+    """
+    q, k, v, S, Z, Wq = (_f64(a) for a in (q, k, v, S, Z, Wq))
+    gate = _f64(gate)
+    L, H, d = q.shape
+    H_kv = k.shape[1]
+    o = np.empty((L, H, d))
+    for h in range(H):
+        g = kv_head(h, H, H_kv)
+        o[:, h:h + 1, :] = attend(q[:, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], S[g:g + 1],
+                                  Z[g:g + 1], Wq[h:h + 1], gate[h:h + 1], merge, scale)
+    return o
+
+
 def prefill_attend(q, k, v, W, gate, L: int, merge: int = MERGE_SHARED_NORM, scale=None,
-                   S0=None, Z0=None):
+                   S0=None, Z0=None, Wk=None):
     """A prompt processed block by block with block-hybrid attention, so that
     every prompt token gets its output ([GIST] "Methodology: Block-Hybrid
     Attention / Architecture Design": exact softmax inside the active block,
@@ -243,20 +276,30 @@ def prefill_attend(q, k, v, W, gate, L: int, merge: int = MERGE_SHARED_NORM, sca
     are trained against their softmax teacher ([GIST] "Retrofitting
     Strategy", stage 1) and give no other prefill formula.
 
-    Returns (o [T, H, d], S [H, F, d], Z [H, F]) in float64.
+    With ``Wk`` given, W is the query map and Wk the key map (the state is
+    built with Wk); k/v may then have H_kv < H heads (grouped-query
+    attention, ``attend_gqa``), with Wk [H_kv, d, f] and the state per
+    key/value head.
+
+    Returns (o [T, H, d], S [H_kv, F, d], Z [H_kv, F]) in float64.
     """
     q, k, v, W = (_f64(a) for a in (q, k, v, W))
+    Wk = W if Wk is None else _f64(Wk)
     T, H, d = q.shape
+    H_kv = k.shape[1]
     if T % L != 0:
         raise ValueError("prompt length must be a multiple of the block length")
     f = W.shape[2]
-    S = np.zeros((H, 2 * f, d)) if S0 is None else _f64(S0).copy()
-    Z = np.zeros((H, 2 * f)) if Z0 is None else _f64(Z0).copy()
+    S = np.zeros((H_kv, 2 * f, d)) if S0 is None else _f64(S0).copy()
+    Z = np.zeros((H_kv, 2 * f)) if Z0 is None else _f64(Z0).copy()
     o = np.empty((T, H, d))
     for j0 in range(0, T, L):
         blk = slice(j0, j0 + L)
-        o[blk] = attend(q[blk], k[blk], v[blk], S, Z, W, gate, merge, scale)
-        S, Z = commit(S, Z, k[blk], v[blk], W)
+        if H_kv == H:
+            o[blk] = attend(q[blk], k[blk], v[blk], S, Z, W, gate, merge, scale)
+        else:
+            o[blk] = attend_gqa(q[blk], k[blk], v[blk], S, Z, W, gate, merge, scale)
+        S, Z = commit(S, Z, k[blk], v[blk], Wk)
     return o, S, Z
 
 

@@ -387,6 +387,102 @@ def check_prefill_attend_first_block_is_softmax(ob):
     _close(o[:L], _sdpa(p["q"][:L], p["k"][:L], p["v"][:L]), rtol=1e-10, atol=1e-12)
 
 
+# ------------------------------------ grouped-query heads, separate key map
+
+def _gqa_problem(seed, L=5, H=4, H_kv=2, d=6, f=2, N=7):
+    g = np.random.default_rng(seed)
+    return dict(
+        q=g.standard_normal((L, H, d)), k=g.standard_normal((L, H_kv, d)),
+        v=g.standard_normal((L, H_kv, d)), k_prev=g.standard_normal((N, H_kv, d)),
+        v_prev=g.standard_normal((N, H_kv, d)), Wq=g.standard_normal((H, d, f)) / np.sqrt(d),
+        Wk=g.standard_normal((H_kv, d, f)) / np.sqrt(d), gate=g.standard_normal(H))
+
+
+def check_gqa_reduces_to_repeated_heads(ob):
+    """Grouped-query attention with H_kv key/value heads is ordinary
+    attention after each key/value head (its k, v and state) is repeated for
+    the H / H_kv consecutive query heads of its group (numpy's repeat along
+    the head axis); with H_kv = H it is attend itself."""
+    p = _gqa_problem(31)
+    G = p["q"].shape[1] // p["k"].shape[1]
+    S, Z = ob.prefill(p["k_prev"], p["v_prev"], p["Wk"])
+    rep = lambda x, axis: np.repeat(x, G, axis=axis)  # noqa: E731
+    for merge in (ob.MERGE_SHARED_NORM, ob.MERGE_CONVEX):
+        o = ob.attend_gqa(p["q"], p["k"], p["v"], S, Z, p["Wq"], p["gate"], merge)
+        ref = ob.attend(p["q"], rep(p["k"], 1), rep(p["v"], 1), rep(S, 0), rep(Z, 0), p["Wq"],
+                        p["gate"], merge)
+        _close(o, ref)
+        # one key/value head per query head: nothing is grouped
+        S4, Z4 = ob.prefill(rep(p["k_prev"], 1), rep(p["v_prev"], 1), rep(p["Wk"], 0))
+        o4 = ob.attend_gqa(p["q"], rep(p["k"], 1), rep(p["v"], 1), S4, Z4, p["Wq"], p["gate"],
+                           merge)
+        _close(o4, ob.attend(p["q"], rep(p["k"], 1), rep(p["v"], 1), S4, Z4, p["Wq"], p["gate"],
+                             merge))
+
+
+def check_gqa_vs_bruteforce(ob):
+    """Query head h of a group reads the state its key/value head g = h // G
+    built with the key map: its output is the token-by-token sum with
+    weights phi_Wq[h](q) . phi_Wk[g](k_t) over g's committed tokens."""
+    p = _gqa_problem(32)
+    H, H_kv = p["q"].shape[1], p["k"].shape[1]
+    G = H // H_kv
+    S, Z = ob.prefill(p["k_prev"], p["v_prev"], p["Wk"])
+    for merge in (ob.MERGE_SHARED_NORM, ob.MERGE_CONVEX):
+        o = ob.attend_gqa(p["q"], p["k"], p["v"], S, Z, p["Wq"], p["gate"], merge)
+        for h in range(H):
+            g = h // G
+            ref = ob.attend_bruteforce(p["q"][:, h:h + 1], p["k"][:, g:g + 1], p["v"][:, g:g + 1],
+                                       p["k_prev"][:, g:g + 1], p["v_prev"][:, g:g + 1],
+                                       p["Wq"][h:h + 1], p["gate"][h:h + 1], merge,
+                                       Wk=p["Wk"][g:g + 1])
+            _close(o[:, h:h + 1], ref, rtol=1e-10, atol=1e-12)
+
+
+def check_prefill_attend_state_free_of_block_length(ob):
+    """The state a prompt leaves is the plain sum over its tokens with the key
+    map, whatever block length cuts it (1, 2, 3, 4, 6 or 12 tokens per
+    block), with a separate key map and with grouped heads."""
+    g = np.random.default_rng(33)
+    T, H, H_kv, d, f = 12, 4, 2, 6, 2
+    q = g.standard_normal((T, H, d))
+    k, v = g.standard_normal((T, H_kv, d)), g.standard_normal((T, H_kv, d))
+    Wq = g.standard_normal((H, d, f)) / np.sqrt(d)
+    Wk = g.standard_normal((H_kv, d, f)) / np.sqrt(d)
+    gate = g.standard_normal(H)
+    for L in (1, 2, 3, 4, 6, 12):
+        _, S, Z = ob.prefill_attend(q, k, v, Wq, gate, L, Wk=Wk)
+        for h in range(H_kv):
+            S_ref = sum(np.outer(ob.feature_map(k[t, h], Wk[h]), v[t, h]) for t in range(T))
+            Z_ref = sum(ob.feature_map(k[t, h], Wk[h]) for t in range(T))
+            _close(S[h], S_ref, rtol=1e-10, atol=1e-12)
+            _close(Z[h], Z_ref, rtol=1e-10, atol=1e-12)
+
+
+def check_prefill_attend_gqa_vs_bruteforce(ob):
+    """A prompt with grouped heads and separate maps: block j of query head h
+    attends to exactly the tokens before it of key/value head h // G, through
+    phi_Wq[h] . phi_Wk[h // G]."""
+    g = np.random.default_rng(34)
+    T, L, H, H_kv, d, f = 8, 4, 4, 2, 6, 2
+    q = g.standard_normal((T, H, d))
+    k, v = g.standard_normal((T, H_kv, d)), g.standard_normal((T, H_kv, d))
+    Wq = g.standard_normal((H, d, f)) / np.sqrt(d)
+    Wk = g.standard_normal((H_kv, d, f)) / np.sqrt(d)
+    gate = g.standard_normal(H)
+    G = H // H_kv
+    for merge in (ob.MERGE_SHARED_NORM, ob.MERGE_CONVEX):
+        o, _, _ = ob.prefill_attend(q, k, v, Wq, gate, L, merge, Wk=Wk)
+        for j0 in range(0, T, L):
+            blk = slice(j0, j0 + L)
+            for h in range(H):
+                gg = h // G
+                ref = ob.attend_bruteforce(q[blk, h:h + 1], k[blk, gg:gg + 1], v[blk, gg:gg + 1],
+                                           k[:j0, gg:gg + 1], v[:j0, gg:gg + 1], Wq[h:h + 1],
+                                           gate[h:h + 1], merge, Wk=Wk[gg:gg + 1])
+                _close(o[blk, h:h + 1], ref, rtol=1e-10, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_feature_map_golden,
     check_feature_map_vs_scipy,
@@ -409,4 +505,8 @@ ALL_CHECKS = [
     check_paged_softmax_kv_vs_sdpa,
     check_prefill_attend_vs_bruteforce,
     check_prefill_attend_first_block_is_softmax,
+    check_gqa_reduces_to_repeated_heads,
+    check_gqa_vs_bruteforce,
+    check_prefill_attend_state_free_of_block_length,
+    check_prefill_attend_gqa_vs_bruteforce,
 ]

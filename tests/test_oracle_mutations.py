@@ -134,9 +134,24 @@ def _gather_whole_pages(pages, page_ids, P):
     return _ORIG["gather_pages"](pages, page_ids, -(-int(P) // p) * p)
 
 
+def _kv_head_modulo(h, H, H_kv):
+    """Groups query heads by h mod H_kv instead of consecutive runs."""
+    return h % H_kv
+
+
+def _prefill_attend_commit_with_query_map(q, k, v, W, gate, L, merge=ob.MERGE_SHARED_NORM,
+                                          scale=None, S0=None, Z0=None, Wk=None):
+    """Builds the state with the query map, ignoring the key map."""
+    if Wk is not None and np.asarray(Wk).shape == np.asarray(W).shape:
+        Wk = W
+    elif Wk is not None:
+        Wk = np.asarray(W)[::np.asarray(W).shape[0] // np.asarray(Wk).shape[0]]
+    return _ORIG["prefill_attend"](q, k, v, W, gate, L, merge, scale, S0, Z0, Wk)
+
+
 _ORIG = {name: getattr(ob, name) for name in
          ("commit", "sigmoid", "softmax_kv_attend", "feature_map", "_softmax_last", "_scale", "attend",
-          "prefill_attend", "gather_pages")}
+          "prefill_attend", "gather_pages", "kv_head")}
 
 MUTATIONS = {
     "phi halves swapped": {"feature_map": _fm_swapped_halves},
@@ -158,6 +173,9 @@ MUTATIONS = {
     "paged gather ignores the page table": {"gather_pages": _gather_pool_order},
     "paged gather swaps page and slot": {"gather_pages": _gather_page_slot_swapped},
     "paged gather reads whole pages": {"gather_pages": _gather_whole_pages},
+    "grouped heads taken modulo": {"kv_head": _kv_head_modulo},
+    "prompt state built with the query map": {
+        "prefill_attend": _prefill_attend_commit_with_query_map},
 }
 
 
