@@ -270,6 +270,61 @@ hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch,
                             int32_t accumulate, void* o, hb_stream_t stream);
 
 /*
+ * hb_block_attend_ex — hb_block_attend, or with `commit` hb_block_attend_commit,
+ * for layers with grouped-query heads and/or separate query and key feature
+ * maps. The pages name "feature map matrices W" of a layer without saying
+ * whether queries and keys share one (gist.science technical summary,
+ * "Retrofitting Strategy", stage 1 bullet) and say nothing of head counts;
+ * this call takes both readings: query head h uses the query map Wq[h] and
+ * reads key/value head g = h / (H / H_kv), whose keys, values and state
+ * (S, Z) it shares with the other query heads of its group, the state being
+ * built with the key map Wk[g] (the read phi_Wq(q)^T S of pith.science,
+ * "What carries the argument", with S = sum_t phi_Wk(k_t) v_t^T).
+ *   num_kv_heads H_kv, which divides H = cfg->num_heads
+ *   q, o         [batch, L, H, d] activation dtype (o written)
+ *   k, v         [batch, L, H_kv, d] activation dtype
+ *   S_pool       [num_slots, H_kv, F, d] fp32; Z_pool [num_slots, H_kv, F] fp32
+ *   Wq           [H, d, f] the queries' map;  Wk [H_kv, d, f] the keys' map
+ *                (used only by commits; may be NULL when commit is NULL)
+ *   gate_logits  [H] fp32, per query head
+ *   commit       [batch] int32 or NULL: with it, requests with commit[b] != 0
+ *                then fold their block's k, v (key/value heads, map Wk) into
+ *                their slot; outputs use the state as it was before the call
+ * With H_kv = H and Wk == Wq (the same pointer) this is exactly
+ * hb_block_attend(_commit). Otherwise the attend runs first (one launch, the
+ * tensor-core kernel for the production shape when H / H_kv divides 512)
+ * and the commit second (one launch), in stream order.
+ */
+hb_status hb_block_attend_ex(const hb_config* cfg, int32_t num_kv_heads,
+                             int32_t batch, const int32_t* slot_idx,
+                             const void* q, const void* k, const void* v,
+                             float* S_pool, float* Z_pool, int32_t num_slots,
+                             const void* Wq, const void* Wk,
+                             const float* gate_logits, const int32_t* commit,
+                             void* o, hb_stream_t stream);
+
+/*
+ * hb_prefill_attend_ex — hb_prefill_attend with grouped-query heads and/or a
+ * separate key map, in the same reading as hb_block_attend_ex: block j of
+ * query head h attends (map Wq[h]) to the state of key/value head
+ * h / (H / H_kv) left by blocks 0 .. j - 1, then every key/value head's state
+ * takes the block's k, v through Wk.
+ *   q, o [batch, seq_len, H, d]; k, v [batch, seq_len, H_kv, d]
+ *   S_pool, Z_pool  [num_slots, H_kv, ...]; Wq [H, d, f]; Wk [H_kv, d, f]
+ *   other arguments as in hb_prefill_attend.
+ * With H_kv = H the production shape runs one launch whatever the maps (the
+ * key map is kept on chip beside the state); grouped heads take an attend
+ * and a commit launch per block.
+ */
+hb_status hb_prefill_attend_ex(const hb_config* cfg, int32_t num_kv_heads,
+                               int32_t batch, const int32_t* slot_idx,
+                               const void* q, const void* k, const void* v,
+                               int64_t seq_len, float* S_pool, float* Z_pool,
+                               int32_t num_slots, const void* Wq, const void* Wk,
+                               const float* gate_logits, int32_t accumulate,
+                               void* o, hb_stream_t stream);
+
+/*
  * hb_commit_block — fold a finished block into the state (gist.science
  * technical summary, state-compression bullet: the states change only when a
  * block is committed; pith.science review, "What carries the argument":

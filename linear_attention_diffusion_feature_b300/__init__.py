@@ -16,11 +16,13 @@ from .hb import (  # noqa: F401
     hb_block_attend,
     hb_block_attend_commit,
     hb_block_attend_commit_s16,
+    hb_block_attend_ex,
     hb_commit_block,
     hb_feature_map,
     hb_get_device_status,
     hb_set_wait_limit,
     hb_prefill_attend,
+    hb_prefill_attend_ex,
     hb_prefill_state,
     hb_prefill_state_noalloc,
     hb_prefill_workspace_size,

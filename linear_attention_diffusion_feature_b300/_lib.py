@@ -56,6 +56,12 @@ SIGNATURES = {
     "hb_prefill_attend": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                                     c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32,
                                     c_void_p, c_void_p]),
+    "hb_block_attend_ex": (c_int32, [_P, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p]),
+    "hb_prefill_attend_ex": (c_int32, [_P, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_int64, c_void_p, c_void_p, c_int32, c_void_p,
+                                       c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "hb_commit_block": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_int32, c_void_p]),
     "hb_prefill_state": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int64, c_void_p,

@@ -296,6 +296,122 @@ hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch, const int32_t* 
   return HB_OK;
 }
 
+namespace {
+
+// Shape of the key/value side of a grouped-query call: Hkv heads.
+hb::Shape kv_shape(const hb::Shape& s, int Hkv) {
+  hb::Shape k = s;
+  k.H = Hkv;
+  return k;
+}
+
+// The fast attend kernel takes grouped heads when a group's share of the
+// block's key/value bytes stays a whole number of 16-byte pieces.
+bool fast_group_ok(int G) { return G >= 1 && 512 % G == 0; }
+
+// Attend only, grouped heads: the tensor-core kernel for the production
+// shape, else the generic one. Request b's block is rows
+// b * rows_per_req + row_base .. of q, k, v and o.
+cudaError_t attend_grouped(const hb::Shape& s, int Hkv, int batch, const int32_t* slot_idx,
+                           const void* q, const void* k, const void* v, const float* S_pool,
+                           const float* Z_pool, int num_slots, const void* Wq,
+                           const float* gate, void* o, unsigned* status, cudaStream_t st,
+                           int64_t rows_per_req, int64_t row_base) {
+  if (hb::fast_attend_ok(s) && fast_group_ok(s.H / Hkv) &&
+      hb::attend_fast_fits(s, batch, num_slots, rows_per_req))
+    return hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
+                                  gate, nullptr, o, status, st, (int)rows_per_req, (int)row_base,
+                                  false, false, Hkv, nullptr);
+  return hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
+                                   gate, o, status, st, rows_per_req, row_base, Hkv);
+}
+
+}  // namespace
+
+hb_status hb_block_attend_ex(const hb_config* cfg, int32_t num_kv_heads, int32_t batch,
+                             const int32_t* slot_idx, const void* q, const void* k,
+                             const void* v, float* S_pool, float* Z_pool, int32_t num_slots,
+                             const void* Wq, const void* Wk, const float* gate_logits,
+                             const int32_t* commit, void* o, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (num_kv_heads < 1 || num_kv_heads > s.H || s.H % num_kv_heads != 0)
+    return HB_ERR_UNSUPPORTED_SHAPE;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, q, k, v, S_pool, Z_pool, Wq, gate_logits, o})) != HB_OK)
+    return r;
+  if (commit && (r = hb::check_ptrs({commit, Wk})) != HB_OK) return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int Hkv = num_kv_heads;
+  const Shape skv = kv_shape(s, Hkv);
+  if (commit && Hkv == s.H && Wk == Wq)  // one map, one state per head: the fused step
+    return hb_block_attend_commit(cfg, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
+                                  gate_logits, commit, o, stream);
+  // the attend reads every state; then, in stream order, the committing
+  // requests fold their block in with the key map, one state per key/value head
+  cudaError_t e = attend_grouped(s, Hkv, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
+                                 gate_logits, o, status, st, s.L, 0);
+  if (e != cudaSuccess || !commit) return hb::from_cuda(e);
+  if (hb::fast_state_ok(skv) && hb::commit_tc_fits(skv, batch, num_slots))
+    return hb::from_cuda(hb::launch_commit_tc(skv, batch, slot_idx, k, v, Wk, S_pool, Z_pool,
+                                              num_slots, status, st, commit));
+  return hb::from_cuda(hb::launch_commit_masked_generic(skv, batch, slot_idx, commit, k, v, Wk,
+                                                        S_pool, Z_pool, num_slots, status, st));
+}
+
+hb_status hb_prefill_attend_ex(const hb_config* cfg, int32_t num_kv_heads, int32_t batch,
+                               const int32_t* slot_idx, const void* q, const void* k,
+                               const void* v, int64_t seq_len, float* S_pool, float* Z_pool,
+                               int32_t num_slots, const void* Wq, const void* Wk,
+                               const float* gate_logits, int32_t accumulate, void* o,
+                               hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0 || seq_len < 0) return HB_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return HB_ERR_INVALID_ARG;
+  if (num_kv_heads < 1 || num_kv_heads > s.H || s.H % num_kv_heads != 0)
+    return HB_ERR_UNSUPPORTED_SHAPE;
+  if (seq_len % s.L != 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, S_pool, Z_pool, Wq, Wk, gate_logits})) != HB_OK) return r;
+  if (seq_len > 0 && (r = hb::check_ptrs({q, k, v, o})) != HB_OK) return r;
+  if ((int64_t)batch * seq_len >= ((int64_t)1 << 31)) return HB_ERR_UNSUPPORTED_SHAPE;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int Hkv = num_kv_heads;
+  const Shape skv = kv_shape(s, Hkv);
+  cudaError_t e = cudaSuccess;
+  if (accumulate == 0 &&
+      (e = hb::launch_state_zero(skv, batch, slot_idx, S_pool, Z_pool, num_slots, status, st)) !=
+          cudaSuccess)
+    return HB_ERR_CUDA;
+  if (seq_len == 0) return HB_OK;
+  if (Hkv == s.H && hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len))
+    // one CTA per (request, head) walks the prompt's blocks with the state
+    // (and the key map, when it is a separate one) kept on chip
+    return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
+                                                num_slots, Wq, gate_logits, nullptr, o, status,
+                                                st, (int)seq_len, 0, true, true, Hkv, Wk));
+  // grouped heads or other shapes: an attend and a commit launch per block
+  for (int64_t row = 0; row < seq_len; row += s.L) {
+    e = attend_grouped(s, Hkv, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
+                       gate_logits, o, status, st, seq_len, row);
+    if (e == cudaSuccess)
+      e = hb::launch_commit_rows_generic(skv, batch, slot_idx, k, v, seq_len, row, Wk, S_pool,
+                                         Z_pool, num_slots, status, st);
+    if (e != cudaSuccess) return hb::from_cuda(e);
+  }
+  return HB_OK;
+}
+
 hb_status hb_commit_block(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
                           const void* k, const void* v, const void* W, float* S_pool,
                           float* Z_pool, int32_t num_slots, hb_stream_t stream) {

@@ -119,6 +119,12 @@ struct Maps {
   // the prompt length and the block's offset for chunkwise prompt
   // processing); commit_all: every request commits (commit_mask unused).
   int rows_per_req, row_base, commit_all;
+  // grouped-query heads (attend only): query head h reads k, v, S and Z of
+  // head h / kv_group (1: one key/value head per query head)
+  int kv_group;
+  // sequential mode: the keys take their own map (maps.Wk), kept for the
+  // whole walk in the second stage's S buffer, which that mode does not use
+  int sep_wk;
   // SM clocks after which a wait of the unit pipeline gives up (hb_set_wait_limit);
   // the final drain of copies already issued always takes the full limit
   long long wait_limit;
@@ -128,7 +134,9 @@ struct Maps {
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
   CUtensorMap k;
   CUtensorMap v;
-  CUtensorMap W;  // [H*d rows][f] bf16, box {64, 128}
+  CUtensorMap W;  // [H*d rows][f] bf16, box {64, 128}: the query map (and the key map
+                  // unless sep_wk)
+  CUtensorMap Wk;  // sep_wk: the key map, as W
 };
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a
@@ -233,13 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // is safe before the wait. Every load and store of global memory comes
   // after grid_dep_wait().
   if (warp == kProducerWarp && lane == 0) {
-    const size_t qkv_bytes = (size_t)batch * maps.rows_per_req * H * kD * 2;
+    const size_t q_bytes = (size_t)batch * maps.rows_per_req * H * kD * 2;
+    const size_t kv_bytes = q_bytes / maps.kv_group;  // k, v have H / kv_group heads
     const size_t w_bytes = (size_t)H * kD * kFH * 2;
-    if (3 * qkv_bytes + w_bytes <= kPrefetchBudget) {
+    if (q_bytes + 2 * kv_bytes + w_bytes <= kPrefetchBudget) {
       const uint8_t* base[4] = {maps.qkv[0], maps.qkv[1], maps.qkv[2], maps.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const size_t bytes = j < 3 ? qkv_bytes : w_bytes;
+        const size_t bytes = j == 0 ? q_bytes : j < 3 ? kv_bytes : w_bytes;
         // 16-byte aligned share of this CTA, issued in pieces of <= 32 KiB
         const size_t share = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
         size_t lo = (size_t)blockIdx.x * share;
@@ -433,6 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             meta[s] = kUnitValid | kUnitCommit | (i == n_local - 1 ? kUnitLast : 0);
             meta[2 + s] = slot;
             if (i == 0) {
+              if (maps.sep_wk) {  // the key map, kept for the whole walk
+                mbar_expect_tx(&head_full[s], 16384);
+                tma_load_2d(smem + kStageStride + kOffS, &maps.Wk, 0, h * kD, &head_full[s]);
+              }
               mbar_expect_tx(&head_full[s], 512);
               bulk_load(smem + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &head_full[s]);
               mbar_arrive(&head_full[s]);
@@ -563,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_head = [&](int i) {
       const int s = i & 1;
       const int b = unit_b(i), h = unit_h(i);
+      const int g = h / maps.kv_group;  // key/value head
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
         *n_issued = i + 1;  // issue_state(i) always follows
@@ -571,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 2; ++j) {
           const int row = b * maps.rows_per_req + maps.row_base;
           tma_load_3d(st + kOffQ + j * 4096, &maps.q, 64 * j, h, row, &head_full[s]);
-          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, row, &head_full[s]);
-          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, row, &head_full[s]);
+          tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, g, row, &head_full[s]);
+          tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, g, row, &head_full[s]);
         }
         tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
       }
@@ -580,6 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_state = [&](int i) {
       const int s = i & 1;
       const int b = unit_b(i), h = unit_h(i);
+      const int hs = h / maps.kv_group;  // the state's head
+      const int Hs = H / maps.kv_group;
       const int flags = unit_flags(i), slot = unit_slot(i);
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
@@ -594,10 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           meta[s] = kUnitValid | flags;
           meta[2 + s] = slot;
           mbar_expect_tx(&head_full[s], 512);
-          bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * H + h) * kF, 512,
+          bulk_load(smem + kOffZ + s * 512, Z_pool + (size_t)(slot * Hs + hs) * kF, 512,
                     &head_full[s]);
           mbar_arrive(&head_full[s]);
-          const int srow = (slot * H + h) * kF;
+          const int srow = (slot * Hs + hs) * kF;
           if (kS16 && !(kDual && (flags & kUnitCommit))) {
             // the bf16 copy (a dual-copy step's committing unit reads the master)
             mbar_arrive_expect_tx(&s_full[s], kSBytes / 2);
@@ -617,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto l2_prefetch = [&](int i) {
       const int b = unit_b(i), h = unit_h(i), slot = unit_slot(i), flags = unit_flags(i);
       if (lane != 0 || slot < 0 || slot >= num_slots) return;
-      const size_t unit = (size_t)slot * H + h;
+      const int G = maps.kv_group;
+      const size_t unit = (size_t)slot * (H / G) + h / G;
       if (kDual && !(flags & kUnitCommit))
         prefetch_l2(maps.s16 + unit * kF * kD * 2, kF * kD * 2);
       else
@@ -627,11 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the request's block of q, k, v is one contiguous range of L rows of
       // all heads; the CTAs working on its heads at the same time each
       // prefetch a 1/H slice of it, so DRAM reads it as one long run
-      const size_t slice = (size_t)kL * kD * 2;  // = block bytes / H
-      const size_t off =
-          ((size_t)b * maps.rows_per_req + maps.row_base) * H * kD * 2 + (size_t)h * slice;
+      // (k and v have H / G heads: their block is G times smaller)
+      const size_t slice = (size_t)kL * kD * 2;  // = q block bytes / H
+      const size_t row0 = (size_t)b * maps.rows_per_req + maps.row_base;
+      prefetch_l2(maps.qkv[0] + row0 * H * kD * 2 + (size_t)h * slice, (uint32_t)slice);
+      const size_t kv_slice = slice / G;
+      const size_t kv_off = row0 * (H / G) * kD * 2 + (size_t)h * kv_slice;
 #pragma unroll
-      for (int j = 0; j < 3; ++j) prefetch_l2(maps.qkv[j] + off, (uint32_t)slice);
+      for (int j = 1; j < 3; ++j) prefetch_l2(maps.qkv[j] + kv_off, (uint32_t)kv_slice);
     };
     // Both stages are free at the start. Unit 0 goes out first and whole;
     // unit 1's head follows, but its state only once unit 0's has landed,
@@ -747,8 +767,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(acc_u[0], half ? a1 : a0, wb[0], wb[1]);
           mma_bf16(acc_u[1], half ? a1 : a0, wb[2], wb[3]);
           if (cm) {
-            mma_bf16(acc_uk[0], half ? ka1 : ka0, wb[0], wb[1]);
-            mma_bf16(acc_uk[1], half ? ka1 : ka0, wb[2], wb[3]);
+            uint32_t wk[4] = {wb[0], wb[1], wb[2], wb[3]};
+            if (kSeq && maps.sep_wk)  // the key map, in the second stage's S buffer
+              ldsm_x4_t(smem_u32(smem + kStageStride + kOffS) + sw128(krow, nch), wk[0], wk[1],
+                        wk[2], wk[3]);
+            mma_bf16(acc_uk[0], half ? ka1 : ka0, wk[0], wk[1]);
+            mma_bf16(acc_uk[1], half ? ka1 : ka0, wk[2], wk[3]);
           }
         }
       }
@@ -1208,9 +1232,19 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
                                bool commit_all, bool sequential, bool state_bf16,
-                               void* S16_pool = nullptr) {
+                               void* S16_pool = nullptr, int Hkv = -1,
+                               const void* Wk = nullptr) {
   const bool dual = S16_pool != nullptr;
+  if (Hkv <= 0) Hkv = s.H;
+  // grouped heads in the attend-only kernels; a separate key map in the
+  // sequential mode
+  if (s.H % Hkv != 0 || (Hkv != s.H && (commit_mask || commit_all || sequential || dual)))
+    return cudaErrorInvalidValue;
+  const bool sep_wk = Wk != nullptr && Wk != W;
+  if (sep_wk && !sequential) return cudaErrorInvalidValue;
   Maps maps;
+  maps.kv_group = s.H / Hkv;
+  maps.sep_wk = sep_wk ? 1 : 0;
   maps.s16 = static_cast<const uint8_t*>(S16_pool);
   maps.rows_per_req = rows_per_req;
   maps.wait_limit = wait_limit_cycles();
@@ -1221,7 +1255,7 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
   maps.qkv[2] = static_cast<const uint8_t*>(v);
   maps.w = static_cast<const uint8_t*>(W);
   {
-    const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * s.H * kF};
+    const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * Hkv * kF};
     const uint64_t strides[1] = {(uint64_t)kD * (state_bf16 ? 2 : 4)};
     const uint32_t box[2] = {state_bf16 ? 64u : 32u, 128};
     if (!encode_tmap(&maps.S,
@@ -1239,15 +1273,18 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * rows_per_req};
-    const uint64_t strides[2] = {kD * 2, (uint64_t)s.H * kD * 2};
+    // q with H heads; k, v with Hkv
     const uint32_t box[3] = {64, 1, 32};
     const void* ptrs[3] = {q, k, v};
     CUtensorMap* dst[3] = {&maps.q, &maps.k, &maps.v};
-    for (int j = 0; j < 3; ++j)
+    for (int j = 0; j < 3; ++j) {
+      const uint64_t heads = j == 0 ? (uint64_t)s.H : (uint64_t)Hkv;
+      const uint64_t dims[3] = {(uint64_t)kD, heads, (uint64_t)batch * rows_per_req};
+      const uint64_t strides[2] = {kD * 2, heads * kD * 2};
       if (!encode_tmap(dst[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptrs[j], dims, strides, box,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    }
   }
   {
     const uint64_t dims[2] = {(uint64_t)kFH, (uint64_t)s.H * kD};
@@ -1255,6 +1292,10 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
     const uint32_t box[2] = {64, 128};
     if (!encode_tmap(&maps.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    maps.Wk = maps.W;
+    if (sep_wk && !encode_tmap(&maps.Wk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wk, dims, strides,
+                               box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   auto* kernel = dual         ? k_attend_fast<true, false, true>
@@ -1291,10 +1332,10 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all, bool sequential) {
+                               bool commit_all, bool sequential, int Hkv, const void* Wk) {
   return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
                             commit_mask, o, status, st, rows_per_req, row_base, commit_all,
-                            sequential, false);
+                            sequential, false, nullptr, Hkv, Wk);
 }
 
 cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slot_idx,

@@ -83,8 +83,8 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
 
 __global__ void __launch_bounds__(kThreads, 2)
     k_commit_tc(const __grid_constant__ Maps maps, int H, int num_slots,
-                const int32_t* __restrict__ slot_idx, float* __restrict__ Z_pool,
-                unsigned* status) {
+                const int32_t* __restrict__ slot_idx, const int32_t* __restrict__ mask,
+                float* __restrict__ Z_pool, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
+  if (mask != nullptr && mask[b] == 0) return;  // this request does not commit
   const int slot = slot_idx[b];
   if (slot < 0 || slot >= num_slots) {
     if (threadIdx.x == 0) atomicOr(status, kStatusBounds);
@@ -298,7 +299,8 @@ bool commit_tc_fits(const Shape& s, int batch, int num_slots) {
 
 cudaError_t launch_commit_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                              const void* v, const void* W, float* S_pool, float* Z_pool,
-                             int num_slots, unsigned* status, cudaStream_t st) {
+                             int num_slots, unsigned* status, cudaStream_t st,
+                             const int32_t* mask) {
   Maps maps;
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * kL};
@@ -329,7 +331,7 @@ cudaError_t launch_commit_tc(const Shape& s, int batch, const int32_t* slot_idx,
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_commit_tc), kSmemBytes);
   if (e != cudaSuccess) return e;
   k_commit_tc<<<dim3(s.H, batch), kThreads, kSmemBytes, st>>>(maps, s.H, num_slots, slot_idx,
-                                                               Z_pool, status);
+                                                               mask, Z_pool, status);
   return cudaGetLastError();
 }
 

@@ -46,22 +46,28 @@ cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, co
 // b * rows_per_req + row_base .. + L - 1 of q, k, v and o. sequential: one
 // CTA per (request, head) runs all rows_per_req / L blocks of the request in
 // order (each attends to the state left by the ones before, then commits;
-// row_base and commit_mask unused).
+// row_base and commit_mask unused). Hkv > 0 (attend only, Hkv divides H and
+// H / Hkv is at most 16): grouped-query heads, k, v, S and Z have Hkv heads
+// and query head h reads head h / (H / Hkv); W is the query map [H, d, f].
+// Wk (sequential mode only): a separate key map [H, d, f] for the commits.
 bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,
                                const float* gate, const int32_t* commit_mask, void* o,
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
-                               bool commit_all, bool sequential = false);
+                               bool commit_all, bool sequential = false, int Hkv = -1,
+                               const void* Wk = nullptr);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);
 // One 32-token block per (request, head), two CTAs per SM (hb_commit_fast.cu).
+// With mask, only the requests with mask[b] != 0 commit.
 bool commit_tc_fits(const Shape& s, int batch, int num_slots);
 cudaError_t launch_commit_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                              const void* v, const void* W, float* S_pool, float* Z_pool,
-                             int num_slots, unsigned* status, cudaStream_t st);
+                             int num_slots, unsigned* status, cudaStream_t st,
+                             const int32_t* mask = nullptr);
 size_t prefill_fast_workspace_bytes(const Shape& s, int batch, int64_t max_seqlen);
 cudaError_t launch_prefill_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                 const void* v, int64_t total_tokens, const int64_t* cu_seqlens,

@@ -177,9 +177,11 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ S_pool, const float* __restrict__ Z_pool, int num_slots,
     const T* __restrict__ W, const float* __restrict__ gate, T* __restrict__ o, unsigned* status,
-    int64_t row_stride, int64_t row_base) {
+    int64_t row_stride, int64_t row_base, int Hkv) {
   const int F = 2 * f;
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  // grouped-query heads: query head h reads key/value head g (k, v, S, Z)
+  const int g = h / (H / Hkv);
   const int slot = slot_idx[b];
   if (slot < 0 || slot >= num_slots) {
     if (tid == 0) atomicOr(status, kStatusBounds);
@@ -198,19 +200,20 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
   float* s_P = s_m + L;                       // row sum of e^{s - m}
   float* s_den = s_P + L;                     // phi(q)^T Z
 
-  const size_t tok_stride = (size_t)H * d;
+  const size_t tok_stride = (size_t)H * d, kv_tok_stride = (size_t)Hkv * d;
   // request b's block: rows b * row_stride + row_base .. + L - 1
-  const size_t base = (((size_t)b * row_stride + row_base) * H + h) * d;
+  const size_t row0 = (size_t)b * row_stride + row_base;
+  const size_t base = (row0 * H + h) * d;
+  const size_t kv_base = (row0 * Hkv + g) * d;
   for (int i = tid; i < L * d; i += kThreads) {
     const int t = i / d, a = i - t * d;
-    const size_t g = base + t * tok_stride + a;
-    sq[i] = to_f32(q[g]);
-    sk[i] = to_f32(k[g]);
-    sv[i] = to_f32(v[g]);
+    sq[i] = to_f32(q[base + t * tok_stride + a]);
+    sk[i] = to_f32(k[kv_base + t * kv_tok_stride + a]);
+    sv[i] = to_f32(v[kv_base + t * kv_tok_stride + a]);
   }
   for (int i = tid; i < d * f; i += kThreads) sW[i] = to_f32(W[(size_t)h * d * f + i]);
-  const float* S = S_pool + ((size_t)slot * H + h) * (size_t)F * d;
-  const float* Zg = Z_pool + ((size_t)slot * H + h) * (size_t)F;
+  const float* S = S_pool + ((size_t)slot * Hkv + g) * (size_t)F * d;
+  const float* Zg = Z_pool + ((size_t)slot * Hkv + g) * (size_t)F;
   for (int i = tid; i < F; i += kThreads) sZ[i] = Zg[i];
   __syncthreads();
 
@@ -260,8 +263,8 @@ __global__ void __launch_bounds__(kThreads) k_attend_generic(
   }
   __syncthreads();
 
-  const float g = gate[h];
-  const float aux = merge == HB_MERGE_SHARED_NORM ? log_sigmoid(g) : sigmoid(g);
+  const float gl = gate[h];
+  const float aux = merge == HB_MERGE_SHARED_NORM ? log_sigmoid(gl) : sigmoid(gl);
   const int nE = L * d;
   float accN[kMaxO];
 #pragma unroll
@@ -533,8 +536,9 @@ cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot
                                   const void* q, const void* k, const void* v, const float* S_pool,
                                   const float* Z_pool, int num_slots, const void* W,
                                   const float* gate, void* o, unsigned* status, cudaStream_t st,
-                                  int64_t rows_per_req, int64_t row_base) {
+                                  int64_t rows_per_req, int64_t row_base, int Hkv) {
   if (rows_per_req < 0) rows_per_req = s.L;
+  if (Hkv <= 0) Hkv = s.H;
   const int scr_ld = s.L > s.f ? s.L : s.f;
   const size_t smem = sizeof(float) * ((size_t)3 * s.L * s.d + s.d * s.f + s.L * s.F +
                                        s.L * scr_ld + s.F + 3 * s.L);
@@ -547,14 +551,14 @@ cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, S_pool, Z_pool, num_slots,
                                      (const __nv_bfloat16*)W, gate, (__nv_bfloat16*)o, status,
-                                     rows_per_req, row_base);
+                                     rows_per_req, row_base, Hkv);
   } else {
     auto* fn = k_attend_generic<float>;
     if ((e = prepare(fn, smem)) != cudaSuccess) return e;
     fn<<<grid, kThreads, smem, st>>>(s.H, s.d, s.f, s.L, s.scale, s.merge, slot_idx,
                                      (const float*)q, (const float*)k, (const float*)v, S_pool,
                                      Z_pool, num_slots, (const float*)W, gate, (float*)o, status,
-                                     rows_per_req, row_base);
+                                     rows_per_req, row_base, Hkv);
   }
   return cudaGetLastError();
 }

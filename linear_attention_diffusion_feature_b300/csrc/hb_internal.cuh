@@ -94,12 +94,14 @@ __device__ __forceinline__ float merge_out(int merge, float U, float P, float m,
 cudaError_t launch_feature_map_generic(const Shape& s, int64_t n, const void* x, const void* W,
                                        float* phi, cudaStream_t st);
 // Request b's block is rows b * rows_per_req + row_base .. + L - 1 of q, k, v
-// and o (rows_per_req < 0 means L).
+// and o (rows_per_req < 0 means L). Hkv > 0: grouped-query heads, k, v, S
+// and Z have Hkv heads and query head h reads head h / (H / Hkv); W is the
+// query map [H, d, f].
 cudaError_t launch_attend_generic(const Shape& s, int batch, const int32_t* slot_idx,
                                   const void* q, const void* k, const void* v, const float* S_pool,
                                   const float* Z_pool, int num_slots, const void* W,
                                   const float* gate, void* o, unsigned* status, cudaStream_t st,
-                                  int64_t rows_per_req = -1, int64_t row_base = 0);
+                                  int64_t rows_per_req = -1, int64_t row_base = 0, int Hkv = -1);
 // commit (cu_seqlens == nullptr: request b owns rows [b*L, b*L+L)) and prefill.
 cudaError_t launch_state_accumulate_generic(const Shape& s, int batch, const int32_t* slot_idx,
                                             const void* k, const void* v, int64_t total_tokens,

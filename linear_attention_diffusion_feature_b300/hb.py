@@ -262,6 +262,76 @@ def hb_prefill_attend(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_lo
     return o
 
 
+def hb_block_attend_ex(cfg: Config, num_kv_heads: int, slot_idx, q, k, v, S_pool, Z_pool, Wq,
+                       gate_logits, Wk=None, commit=None, o=None, stream=None) -> torch.Tensor:
+    """Grouped-query heads and/or separate query and key maps: q [B, L, H, d],
+    k/v [B, L, H_kv, d], states per key/value head, Wq [H, d, f],
+    Wk [H_kv, d, f] (commits only). With ``commit``, requests with
+    commit[b] != 0 then fold their block into their slot."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    Hkv = int(num_kv_heads)
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(q, "q", cfg.torch_dtype, (B, L, H, d))
+    _check(k, "k", cfg.torch_dtype, (B, L, Hkv, d))
+    _check(v, "v", cfg.torch_dtype, (B, L, Hkv, d))
+    if S_pool.dim() != 4:
+        raise ValueError("S_pool: expected [num_slots, H_kv, F, d]")
+    num_slots = S_pool.shape[0]
+    _check(S_pool, "S_pool", torch.float32, (num_slots, Hkv, cfg.F, d))
+    _check(Z_pool, "Z_pool", torch.float32, (num_slots, Hkv, cfg.F))
+    _check(Wq, "Wq", cfg.torch_dtype, (H, d, f))
+    if Wk is not None:
+        _check(Wk, "Wk", cfg.torch_dtype, (Hkv, d, f))
+    if commit is not None:
+        _check(commit, "commit", torch.int32, (B,))
+        if Wk is None:
+            raise ValueError("Wk: the key map is needed to commit")
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_ex(ctypes.byref(cfg.c()), Hkv, B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(S_pool), _ptr(Z_pool), num_slots, _ptr(Wq),
+                                  _ptr(Wk), _ptr(gate_logits), _ptr(commit), _ptr(o),
+                                  _stream(stream)), "hb_block_attend_ex")
+    return o
+
+
+def hb_prefill_attend_ex(cfg: Config, num_kv_heads: int, slot_idx, q, k, v, S_pool, Z_pool, Wq,
+                         Wk, gate_logits, accumulate: bool = False, o=None,
+                         stream=None) -> torch.Tensor:
+    """hb_prefill_attend with grouped-query heads and/or separate maps:
+    q [B, T, H, d], k/v [B, T, H_kv, d], states per key/value head."""
+    B = slot_idx.shape[0]
+    H, d, f = cfg.num_heads, cfg.head_dim, cfg.feat_half
+    Hkv = int(num_kv_heads)
+    T = q.shape[1] if q.dim() == 4 else -1
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    _check(q, "q", cfg.torch_dtype, (B, T, H, d))
+    _check(k, "k", cfg.torch_dtype, (B, T, Hkv, d))
+    _check(v, "v", cfg.torch_dtype, (B, T, Hkv, d))
+    if S_pool.dim() != 4:
+        raise ValueError("S_pool: expected [num_slots, H_kv, F, d]")
+    num_slots = S_pool.shape[0]
+    _check(S_pool, "S_pool", torch.float32, (num_slots, Hkv, cfg.F, d))
+    _check(Z_pool, "Z_pool", torch.float32, (num_slots, Hkv, cfg.F))
+    _check(Wq, "Wq", cfg.torch_dtype, (H, d, f))
+    _check(Wk, "Wk", cfg.torch_dtype, (Hkv, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, T, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_prefill_attend_ex(ctypes.byref(cfg.c()), Hkv, B, _ptr(slot_idx), _ptr(q),
+                                    _ptr(k), _ptr(v), T, _ptr(S_pool), _ptr(Z_pool), num_slots,
+                                    _ptr(Wq), _ptr(Wk), _ptr(gate_logits),
+                                    int(bool(accumulate)), _ptr(o), _stream(stream)),
+           "hb_prefill_attend_ex")
+    return o
+
+
 def hb_commit_block(cfg: Config, slot_idx, k, v, W, S_pool, Z_pool, stream=None) -> None:
     """S += sum_t phi(k_t) v_t^T, Z += sum_t phi(k_t) for each listed slot."""
     B = slot_idx.shape[0]
