@@ -1050,7 +1050,7 @@ def run_prefill_attend(args):
 
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    nB, T = 8, 8192
+    nB, T = args.pa_batch, args.pa_len
     cfg = hb.Config(H, D, FH, L)
     g = inputs.prompt_ingestion(device=device, B=nB, T=T)
     k = g.tensors["k"].view(nB, T, H, D)
@@ -1081,12 +1081,12 @@ def run_prefill_attend(args):
         "unit": "tokens/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "hb_prefill_attend: 8 prompts x 8,192 tokens, 16 heads, d=128, "
-                               "f=64, L=32, from empty states",
+        "config": {"workload": f"hb_prefill_attend: {nB} prompts x {T} tokens, 16 heads, "
+                               "d=128, f=64, L=32, from empty states",
                    "timing": "one call (a state reset and one prompt kernel) per CUDA graph, "
                              "replayed",
-                   "l2": "q, k, v, o 1.07 GB > L2"},
-        "roofline": {"kernel": "hb_prefill_attend (k_attend_fast, sequential mode)",
+                   "l2": f"q, k, v, o {4 * nB * T * H * D * 2 / 1e9:.2f} GB"},
+        "roofline": {"kernel": "hb_prefill_attend (k_prompt_tc)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": kind,
                      "algorithmic_bytes_per_call": nbytes,
@@ -1295,6 +1295,8 @@ def main(argv=None):
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
                          "softmax over a KV cache; feature_map: standalone phi")
     ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
+    ap.add_argument("--pa-batch", type=int, default=8, help="prefill_attend: prompts")
+    ap.add_argument("--pa-len", type=int, default=8192, help="prefill_attend: tokens each")
     ap.add_argument("--serve-concurrency", type=int, nargs="+", default=[1, 16, 64, 128])
     ap.add_argument("--serve-budget-gib", type=int, default=40)
     ap.add_argument("--psweep-batches", type=int, nargs="+", default=[1, 64])

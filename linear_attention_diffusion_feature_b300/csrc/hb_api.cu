@@ -278,12 +278,11 @@ hb_status hb_prefill_attend(const hb_config* cfg, int32_t batch, const int32_t* 
           cudaSuccess)
     return HB_ERR_CUDA;
   if (seq_len == 0) return HB_OK;
-  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len))
-    // one CTA per (request, head) walks the prompt's blocks with the state
-    // kept on chip
-    return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
-                                                num_slots, W, gate_logits, nullptr, o, status,
-                                                st, (int)seq_len, 0, true, true));
+  if (hb::prompt_tc_fits(s, batch, num_slots, seq_len))
+    // one CTA per (request, head) walks the prompt in 128-token segments on
+    // the tensor cores, with the state in tensor memory
+    return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, seq_len, S_pool,
+                                              Z_pool, num_slots, W, gate_logits, o, status, st));
   // other shapes: an attend and a commit launch per block, in stream order
   for (int64_t row = 0; row < seq_len; row += s.L) {
     e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W,
@@ -394,9 +393,12 @@ hb_status hb_prefill_attend_ex(const hb_config* cfg, int32_t num_kv_heads, int32
           cudaSuccess)
     return HB_ERR_CUDA;
   if (seq_len == 0) return HB_OK;
+  if (Hkv == s.H && Wk == Wq && hb::prompt_tc_fits(s, batch, num_slots, seq_len))
+    return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, seq_len, S_pool,
+                                              Z_pool, num_slots, Wq, gate_logits, o, status, st));
   if (Hkv == s.H && hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, seq_len))
-    // one CTA per (request, head) walks the prompt's blocks with the state
-    // (and the key map, when it is a separate one) kept on chip
+    // separate maps: one CTA per (request, head) walks the prompt's blocks
+    // with the state and the key map kept on chip
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, Wq, gate_logits, nullptr, o, status,
                                                 st, (int)seq_len, 0, true, true, Hkv, Wk));

@@ -58,6 +58,15 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
                                bool commit_all, bool sequential = false, int Hkv = -1,
                                const void* Wk = nullptr);
+// Prompts with outputs, chunked onto tcgen05 (hb_prompt_tc.cu): one CTA per
+// (request, head) walks its prompt in 128-token segments with the state in
+// tensor memory; q, k, v, o are [batch, seq_len, H, d], seq_len a multiple
+// of 32; the slots' states are read at the start and written at the end.
+bool prompt_tc_fits(const Shape& s, int batch, int num_slots, int64_t seq_len);
+cudaError_t launch_prompt_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
+                             const void* k, const void* v, int64_t seq_len, float* S_pool,
+                             float* Z_pool, int num_slots, const void* W, const float* gate,
+                             void* o, unsigned* status, cudaStream_t st);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);

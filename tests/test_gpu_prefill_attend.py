@@ -1,6 +1,6 @@
 """hb_prefill_attend (GPU): every block of a prompt gets the oracle's
 block-hybrid output against the state of the blocks before it, and the slot
-ends with the whole prompt's state; also equal to chaining
+ends with the whole prompt's state; also within the bounds of chaining
 hb_block_attend_commit block by block."""
 
 import numpy as np
@@ -86,9 +86,37 @@ def test_prefill_attend_tiny_shape(cuda_device):
                           hb.MERGE_SHARED_NORM, TOL_OUT_FP32)
 
 
-def test_prefill_attend_equals_chained_steps(cuda_device):
-    """8 prompts of 512 tokens: the same bits as hb_block_attend_commit run
-    block by block on copies of each block (every request committing)."""
+@pytest.mark.parametrize("merge", sorted(MERGES))
+@pytest.mark.parametrize("T", [32, 160, 416, 512])
+def test_prefill_attend_segments_match_oracle(cuda_device, merge, T):
+    """Prompts of 1 to 16 blocks, so that the 128-token segments of the
+    tensor-core kernel come full and partial (32, 160 = 128 + 32,
+    416 = 3 x 128 + 32, 512 = 4 x 128 tokens), 4 prompts each with permuted
+    slots holding earlier context: every block's output and the final state
+    against the oracle."""
+    B, H, d, f, L = 4, 16, 128, 64, 32
+    cfg = hb.Config(H, d, f, L, merge=MERGES[merge])
+    W, gate, q, k, v = _prompts(700 + T, B, T, H, d, f, torch.bfloat16)
+    S, Z = new_pool(cfg, 6, cuda_device)
+    S0, Z0 = [], []
+    slot_of = [5, 1, 3, 0]
+    for b in range(B):
+        n = 24 * b  # 0, 24, 48, 72 tokens of earlier context
+        pk = inputs.draw(800 + 2 * b, (n, H, d), torch.bfloat16)
+        pv = inputs.draw(801 + 2 * b, (n, H, d), torch.bfloat16)
+        s0, z0 = ob.prefill(f64(pk), f64(pv), f64(W))
+        S0.append(s0)
+        Z0.append(z0)
+        S[slot_of[b]] = torch.as_tensor(s0, dtype=torch.float32, device=cuda_device)
+        Z[slot_of[b]] = torch.as_tensor(z0, dtype=torch.float32, device=cuda_device)
+    _check_against_oracle(cuda_device, cfg, B, T, W, gate, q, k, v, slot_of, S, Z,
+                          MERGES[merge], TOL_OUT_BF16, S0=S0, Z0=Z0)
+
+
+def test_prefill_attend_close_to_chained_steps(cuda_device):
+    """8 prompts of 512 tokens: within the bf16 bound of hb_block_attend_commit
+    run block by block (every request committing), and the same state within
+    the state bound."""
     B, T, H, d, f, L = 8, 512, 16, 128, 64, 32
     cfg = hb.Config(H, d, f, L)
     W, gate, q, k, v = (x.to(cuda_device) for x in _prompts(500, B, T, H, d, f, torch.bfloat16))
@@ -104,8 +132,11 @@ def test_prefill_attend_equals_chained_steps(cuda_device):
                                                k[:, blk].contiguous(), v[:, blk].contiguous(),
                                                S2, Z2, W, gate, ones)
     assert_status_ok()
-    assert torch.equal(o1, o2)
-    assert torch.equal(S1, S2) and torch.equal(Z1, Z2)
+    for b in range(B):
+        for j0 in range(0, T, L):
+            assert out_err(f64(o1[b, j0:j0 + L]), f64(o2[b, j0:j0 + L])) <= TOL_OUT_BF16, (b, j0)
+    assert unit_err(f64(S1), f64(S2), 2) <= TOL_STATE
+    assert unit_err(f64(Z1), f64(Z2), 2) <= TOL_STATE
 
 
 def test_prefill_attend_bad_slot_is_flagged(cuda_device):
