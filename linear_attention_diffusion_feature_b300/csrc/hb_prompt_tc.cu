@@ -45,9 +45,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // loader, MMA issuer, epilogue
 // Shared memory (bytes from a 1024-aligned base). Every 128-row bf16 tile is
 // two SWIZZLE_128B boxes of [128 rows][64 columns] (16 KiB each).
 constexpr int kOffW = 0;                 // W_h [d rows][f]
-constexpr int kOffQ = 16384;             // Q, then phi(Q), then C
+constexpr int kOffQ = 16384;             // Q, then phi(Q)
 constexpr int kOffK = kOffQ + 32768;     // K, then phi(K) hi
-constexpr int kOffKlo = kOffK + 32768;   // phi(K) lo
+constexpr int kOffKlo = kOffK + 32768;   // phi(K) lo, then C, then the outputs o
 constexpr int kOffV = kOffKlo + 32768;   // V, two buffers
 constexpr int kOffS16 = kOffV + 65536;   // bf16 copy of the state [F rows][d]
 constexpr int kOffX = kOffS16 + 32768;   // exchange: 4 arrays of [4 quarters][128 rows] fp32
@@ -73,7 +73,18 @@ constexpr uint32_t kColA = 384;  // phi(Q) phi(K)^T
 struct Maps {
   CUtensorMap q, k, v;  // [B*T rows][H][d] bf16, box {64, 1, 128}
   CUtensorMap W;        // [H*d rows][f] bf16, box {64, 128}
+  CUtensorMap o;        // [B][T][H][d] bf16, box {64, 1, 128, 1}: stores clip at T
 };
+
+// Shared -> global copy of one box of a 4-D tensor map (bulk async-group).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int x, int y, int z, int w,
+                                             const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          map),
+      "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+      : "memory");
+}
 
 struct Args {
   int H, num_slots, merge;
@@ -195,15 +206,22 @@ __global__ void __maxnreg__(96)
         l2(2);
       }
       for (int s = 1; s < n_seg; ++s) {
-        // Q and K of the segment before have been used (its last MMA, O1,
-        // reads C from the Q buffer), and so has the V buffer of s - 1
-        if (!mbar_wait(&bar[kBarO], (s - 1) & 1, a.wait_limit)) {
+        // phi(Q) and phi(K) of the segment before, over its Q and K, have
+        // been read once its A, O2 and state-update MMAs are done; its V
+        // buffer once O1 is done too
+        if (!mbar_wait(&bar[kBarL], (s - 1) & 1, a.wait_limit)) {
           atomicOr(a.status, kStatusTimeout);
           break;
         }
         load_qk(s);
-        if (s + 1 < n_seg) load_v(s + 1);
         l2(s + 2);
+        if (s + 1 < n_seg) {
+          if (!mbar_wait(&bar[kBarO], (s - 1) & 1, a.wait_limit)) {
+            atomicOr(a.status, kStatusTimeout);
+            break;
+          }
+          load_v(s + 1);
+        }
       }
       // no copy may land in the shared memory of an exited CTA: wait for the
       // last one issued on each barrier (immediate when already consumed)
@@ -260,7 +278,7 @@ __global__ void __maxnreg__(96)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tbase + kColS, desc_k(sQ, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
+          umma_bf16(tbase + kColS, desc_k(sKlo, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarO]);
       }
       if (!ok) atomicOr(a.status, kStatusTimeout);
@@ -325,19 +343,13 @@ __global__ void __maxnreg__(96)
       // by the four threads of the row: row max, min and sums exchanged
       float ph[32];
       auto softmaxes = [&]() {
+        // each thread's 16 columns with its own max and min; one exchange
+        // merges the four threads' (max, sum) and (min, sum) pairs exactly
         float mx = -FLT_MAX, mn = FLT_MAX;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           mx = fmaxf(mx, u[j]);
           mn = fminf(mn, u[j]);
-        }
-        xa[sub * 128 + r] = mx;
-        xb[sub * 128 + r] = mn;
-        named_bar_sync(1, 32 * kEpiWarps);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mx = fmaxf(mx, xa[q * 128 + r]);
-          mn = fminf(mn, xb[q * 128 + r]);
         }
         float sp = 0.f, sm = 0.f;
 #pragma unroll
@@ -347,17 +359,33 @@ __global__ void __maxnreg__(96)
           sp += ph[j];
           sm += ph[16 + j];
         }
+        xa[sub * 128 + r] = mx;
+        xb[sub * 128 + r] = mn;
         xc[sub * 128 + r] = sp;
         xd[sub * 128 + r] = sm;
         named_bar_sync(1, 32 * kEpiWarps);
-        sp = (xc[r] + xc[128 + r]) + (xc[256 + r] + xc[384 + r]);
-        sm = (xd[r] + xd[128 + r]) + (xd[256 + r] + xd[384 + r]);
-        const float ip = rcp_approx(sp), im = rcp_approx(sm);  // sums >= 1
+        float M = mx, N = mn;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          M = fmaxf(M, xa[q * 128 + r]);
+          N = fminf(N, xb[q * 128 + r]);
+        }
+        float tp = 0.f, tm = 0.f;  // row totals e^{u - M}, e^{N - u} (each >= 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tp = fmaf(xc[q * 128 + r], ex2_approx((xa[q * 128 + r] - M) * kLog2e), tp);
+          tm = fmaf(xd[q * 128 + r], ex2_approx((N - xb[q * 128 + r]) * kLog2e), tm);
+        }
+        const float cp = ex2_approx((mx - M) * kLog2e) * rcp_approx(tp);
+        const float cm = ex2_approx((N - mn) * kLog2e) * rcp_approx(tm);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          ph[j] *= ip;
-          ph[16 + j] *= im;
+          ph[j] *= cp;
+          ph[16 + j] *= cm;
         }
+        // the exchange slots are rewritten by the next call only after every
+        // thread has passed this barrier
+        named_bar_sync(1, 32 * kEpiWarps);
       };
       // queries: phi(Q) (bf16) over Q, and phi(q) . Z of this thread's columns
       tmem_ld16(tbase + lane_bits + kColU + 16 * sub, u);
@@ -519,7 +547,7 @@ __global__ void __maxnreg__(96)
             const int j = 8 * q4 + 2 * p;
             w4[p] = sub <= quad ? pack_bf16(c * v32[j], c * v32[j + 1]) : 0u;
           }
-          st_shared_v4(sQ + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
+          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
         }
       }
       fence_proxy_async_smem();
@@ -530,28 +558,37 @@ __global__ void __maxnreg__(96)
       // ---- E4: o = O1 + cN O2 for this thread's 32 columns of row r
       if (ok) ok = mbar_wait(&bar[kBarO], s & 1, a.wait_limit);
       tc_fence_after();
-      const size_t orow = (size_t)b * a.T + (size_t)s * kSeg + r;
-      uint4* dst = reinterpret_cast<uint4*>(a.o + (orow * a.H + h) * kD + 32 * sub);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float o1[16], o2[16];
         tmem_ld16(tbase + lane_bits + kColS + 32 * sub + 16 * hf, o1);
         tmem_ld16(tbase + lane_bits + kColU + 32 * sub + 16 * hf, o2);
         tmem_wait_ld();
-        if (live && ok) {
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            uint4 w;
-            const int j = 8 * q2;
-            w.x = pack_bf16(fmaf(cN, o2[j], o1[j]), fmaf(cN, o2[j + 1], o1[j + 1]));
-            w.y = pack_bf16(fmaf(cN, o2[j + 2], o1[j + 2]), fmaf(cN, o2[j + 3], o1[j + 3]));
-            w.z = pack_bf16(fmaf(cN, o2[j + 4], o1[j + 4]), fmaf(cN, o2[j + 5], o1[j + 5]));
-            w.w = pack_bf16(fmaf(cN, o2[j + 6], o1[j + 6]), fmaf(cN, o2[j + 7], o1[j + 7]));
-            dst[2 * hf + q2] = w;
-          }
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int j = 8 * q2;
+          // d columns 32 sub + 16 hf + 8 q2 .. + 7: chunk 4 sub + 2 hf + q2
+          st_shared_v4(sKlo + tile_off(r, 4 * sub + 2 * hf + q2),
+                       pack_bf16(fmaf(cN, o2[j], o1[j]), fmaf(cN, o2[j + 1], o1[j + 1])),
+                       pack_bf16(fmaf(cN, o2[j + 2], o1[j + 2]), fmaf(cN, o2[j + 3], o1[j + 3])),
+                       pack_bf16(fmaf(cN, o2[j + 4], o1[j + 4]), fmaf(cN, o2[j + 5], o1[j + 5])),
+                       pack_bf16(fmaf(cN, o2[j + 6], o1[j + 6]), fmaf(cN, o2[j + 7], o1[j + 7])));
         }
       }
+      // the segment's outputs: two TMA stores (rows past the prompt are
+      // clipped by the map); the lo buffer is handed on once they have read it
+      fence_proxy_async_smem();
       tc_fence_before();
+      named_bar_sync(1, 32 * kEpiWarps);
+      if (threadIdx.x == 64) {
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_store_4d(&maps.o, 64 * j, h, s * kSeg, b, smem + kOffKlo + j * 16384);
+          bulk_commit();
+          bulk_wait_read();
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarE]);
     }
@@ -595,6 +632,15 @@ cudaError_t launch_prompt_tc(const Shape& s, int batch, const int32_t* slot_idx,
     const uint64_t strides[1] = {kFH * 2};
     const uint32_t box[2] = {64, 128};
     if (!encode_tmap(&maps.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)seq_len, (uint64_t)batch};
+    const uint64_t strides[3] = {kD * 2, (uint64_t)s.H * kD * 2,
+                                 (uint64_t)seq_len * s.H * kD * 2};
+    const uint32_t box[4] = {64, 1, kSeg, 1};
+    if (!encode_tmap(&maps.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, o, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
