@@ -1096,6 +1096,75 @@ def run_prefill_attend(args):
     }
 
 
+def run_blocklen(args):
+    """The continuous-batching step (64 requests, 16 committing, hb_block_attend_commit)
+    at block lengths L = 16, 32 and 64: L = 32 takes the persistent attend
+    kernel, 16 and 64 the segment kernel on a one-block prompt. Six layer
+    instances in turn, graphs of 600 steps replayed for >= 0.5 s."""
+    import linear_attention_diffusion_feature_b300 as hb
+    from linear_attention_diffusion_feature_b300 import inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream()
+    peak, kind = _peaks()
+    out = []
+    for Lb in args.block_lens:
+        cfg = hb.Config(H, D, FH, Lb)
+        layers = []
+        for layer in range(N_LAYERS):
+            w = inputs.continuous_batching(seed=50 + layer, device=device, B=B, n_commit=N_COMMIT)
+            t = w.tensors
+            S = torch.empty((B, H, F, D), dtype=torch.float32, device=device)
+            Z = torch.empty((B, H, F), dtype=torch.float32, device=device)
+            sl = torch.arange(B, dtype=torch.int32, device=device)
+            hb.hb_prefill_state(cfg, sl, t["prefix_k"], t["prefix_v"], t["cu_prefix"],
+                                w.meta["max_prefix"], t["W"], S, Z)
+            qkv = [inputs.draw(60 + 3 * layer + j, (B, Lb, H, D), torch.bfloat16, device)
+                   for j in range(3)]
+            mask = torch.zeros(B, dtype=torch.int32, device=device)
+            mask[t["commit_idx"]] = 1
+            layers.append(dict(S=S, Z=Z, sl=sl, W=t["W"], gate=t["gate"], q=qkv[0], k=qkv[1],
+                               v=qkv[2], mask=mask, o=torch.empty_like(qkv[0])))
+            del t, w
+        torch.cuda.synchronize()
+
+        def step(i):
+            ly = layers[i % N_LAYERS]
+            hb.hb_block_attend_commit(cfg, ly["sl"], ly["q"], ly["k"], ly["v"], ly["S"], ly["Z"],
+                                      ly["W"], ly["gate"], ly["mask"], o=ly["o"])
+
+        for i in range(args.warmup):
+            step(i)
+        g = StepGraphs(step, GRAPH_STEPS)
+        g.replay()
+        one = _timed_replays(g, 1, stream)
+        n_rep = max(1, int(500.0 / one) + 1)
+        ms = _timed_replays(g, n_rep, stream) / (n_rep * GRAPH_STEPS)
+        assert hb.hb_get_device_status() == 0
+        nbytes = (B * (H * (F * D * 4 + F * 4) + 4 * Lb * H * D * 2) + H * D * FH * 2
+                  + N_COMMIT * H * (F * D * 4 + F * 4))
+        out.append({"block_len": Lb, "ms": ms, "tokens_per_s": B * Lb / (ms / 1e3),
+                    "algorithmic_bytes": nbytes, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak,
+                    "kernel": "k_attend_fast (persistent)" if Lb == 32 else "k_prompt_tc"})
+        del layers, g
+        torch.cuda.empty_cache()
+    top = out[0]
+    return {
+        "metric": "continuous-batching step at several block lengths: active-block tokens/s",
+        "value": top["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": top["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "hb_block_attend_commit, 64 requests x 16 heads, d=128, f=64, "
+                               "16 committing, prefixes 32*U{8..128}", "block_lens": args.block_lens,
+                   "timing": "graphs of 600 steps over 6 layer instances, >= 0.5 s of replays"},
+        "roofline": {"kernel": top["kernel"], "bound": "hbm", "achieved": None, "peak": peak,
+                     "unit": "GB/s", "frac": top["hbm_frac"], "peak_kind": kind, "traffic": None},
+        "sweep": out,
+        "gpu_launches": None,
+    }
+
+
 def run_serve(args):
     """Continuous-batching simulation on the library's own calls (the pages'
     end-to-end protocol on synthetic layers): the same stream of requests
@@ -1289,12 +1358,13 @@ def main(argv=None):
                     help="skip the stack (B=256) and prompt-ingestion components of the "
                          "default line")
     ap.add_argument("--workload", choices=["step", "decode", "prefill", "stack", "feature_map", "psweep",
-                             "prefill_attend", "serve"],
+                             "prefill_attend", "serve", "blocklen"],
                     default="step",
                     help="step: continuous-batching step (default); decode: single-layer "
                          "latency; prefill: prompt ingestion; stack: 6-layer sweep vs "
                          "softmax over a KV cache; feature_map: standalone phi")
     ap.add_argument("--stack-batches", type=int, nargs="+", default=[1, 16, 64, 256])
+    ap.add_argument("--block-lens", type=int, nargs="+", default=[16, 32, 64])
     ap.add_argument("--pa-batch", type=int, default=8, help="prefill_attend: prompts")
     ap.add_argument("--pa-len", type=int, default=8192, help="prefill_attend: tokens each")
     ap.add_argument("--serve-concurrency", type=int, nargs="+", default=[1, 16, 64, 128])
@@ -1320,7 +1390,8 @@ def main(argv=None):
             ap.error("--workload other than step runs on one GPU")
         runner = {"decode": run_decode, "prefill": run_prefill, "stack": run_stack,
                   "feature_map": run_feature_map, "psweep": run_psweep,
-                  "prefill_attend": run_prefill_attend, "serve": run_serve}
+                  "prefill_attend": run_prefill_attend, "serve": run_serve,
+                  "blocklen": run_blocklen}
         print(json.dumps(runner[args.workload](args)), flush=True)
         return 0
     if world > 1:

@@ -158,6 +158,13 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch, const int32_t* sl
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, nullptr, o, status,
                                                 st, s.L, 0, false));
+  if (hb::prompt_tc_fits(s, batch, num_slots, s.L))
+    // blocks of 16 or 64 tokens: the segment kernel on a one-block prompt,
+    // the states only read
+    return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, s.L,
+                                              const_cast<float*>(S_pool),
+                                              const_cast<float*>(Z_pool), num_slots, W,
+                                              gate_logits, o, status, st, false, nullptr));
   return hb::from_cuda(hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                  num_slots, W, gate_logits, o, status, st));
 }
@@ -220,6 +227,12 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int3
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, commit, o, status,
                                                 st, s.L, 0, false));
+  if (hb::prompt_tc_fits(s, batch, num_slots, s.L))
+    // blocks of 16 or 64 tokens: the segment kernel on a one-block prompt;
+    // committing requests write their new state back
+    return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, s.L, S_pool, Z_pool,
+                                              num_slots, W, gate_logits, o, status, st, false,
+                                              commit));
   // other shapes: the attend pass reads every state, then the committing
   // requests fold their block in, in stream order
   cudaError_t e = hb::launch_attend_generic(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots,

@@ -61,12 +61,15 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
 // Prompts with outputs, chunked onto tcgen05 (hb_prompt_tc.cu): one CTA per
 // (request, head) walks its prompt in 128-token segments with the state in
 // tensor memory; q, k, v, o are [batch, seq_len, H, d], seq_len a multiple
-// of 32; the slots' states are read at the start and written at the end.
+// of L (16, 32 or 64); the slots' states are read at the start and written
+// back at the end for the requests that commit (commit_all, or
+// commit_mask[b] != 0). With seq_len = L it is one decoding step.
 bool prompt_tc_fits(const Shape& s, int batch, int num_slots, int64_t seq_len);
 cudaError_t launch_prompt_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                              const void* k, const void* v, int64_t seq_len, float* S_pool,
                              float* Z_pool, int num_slots, const void* W, const float* gate,
-                             void* o, unsigned* status, cudaStream_t st);
+                             void* o, unsigned* status, cudaStream_t st, bool commit_all = true,
+                             const int32_t* commit_mask = nullptr);
 cudaError_t launch_commit_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* k,
                                const void* v, const void* W, float* S_pool, float* Z_pool,
                                int num_slots, unsigned* status, cudaStream_t st);

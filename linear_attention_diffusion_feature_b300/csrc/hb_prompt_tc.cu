@@ -52,9 +52,9 @@ constexpr int kOffV = kOffKlo + 32768;   // V, two buffers
 constexpr int kOffS16 = kOffV + 65536;   // bf16 copy of the state [F rows][d]
 constexpr int kOffX = kOffS16 + 32768;   // exchange: 4 arrays of [4 quarters][128 rows] fp32
 constexpr int kOffXden = kOffX + 8192;   // [4][128]: phi(q) . Z partial sums
-constexpr int kOffXm = kOffXden + 2048;  // [128]: block score row max (base 2)
-constexpr int kOffXP = kOffXm + 512;     // [128]: block softmax row sum
-constexpr int kOffZ = kOffXP + 512;      // [128]: Z
+constexpr int kOffXm = kOffXden + 2048;  // [4][128]: partial row max of the own block's scores
+constexpr int kOffXP = kOffXm + 2048;    // [4][128]: the matching partial sums
+constexpr int kOffZ = kOffXP + 2048;     // [128]: Z
 constexpr int kOffZq = kOffZ + 512;      // [4][128]: the segment's column sums of phi(K)
 constexpr int kOffBar = kOffZq + 2048;
 constexpr int kNumBars = 11;
@@ -88,6 +88,10 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int x, int 
 
 struct Args {
   int H, num_slots, merge;
+  // request b's final state is written back when commit_all or
+  // commit_mask[b] != 0 (otherwise the slot is only read)
+  int commit_all;
+  const int32_t* commit_mask;
   int64_t T;  // prompt length (a multiple of 32)
   float scale_log2;
   const int32_t* slot_idx;
@@ -115,10 +119,14 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// kBL: the block length L (16, 32 or 64), a divisor of the 128-token
+// segment; row r of a segment is in block r / kBL.
 // 18 warps put five on two of the four sub-partitions, whose 16 Ki
 // registers then allow at most 102 per thread: capped at 96.
+template <int kBL>
 __global__ void __maxnreg__(96)
     k_prompt_tc(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
+  static_assert(kBL == 16 || kBL == 32 || kBL == 64, "block length");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -133,6 +141,7 @@ __global__ void __maxnreg__(96)
   }
   const int n_seg = (int)((a.T + kSeg - 1) / kSeg);
   const size_t unit = (size_t)slot * a.H + h;
+  const bool commits = a.commit_all != 0 || (a.commit_mask != nullptr && a.commit_mask[b] != 0);
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarW], 1);
@@ -471,50 +480,81 @@ __global__ void __maxnreg__(96)
                          pack_bf16(st[8 * q4 + 2], st[8 * q4 + 3]),
                          pack_bf16(st[8 * q4 + 4], st[8 * q4 + 5]),
                          pack_bf16(st[8 * q4 + 6], st[8 * q4 + 7]));
-        } else if (ok) {
+        } else if (ok && commits) {
           float4* dst = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD + r * kD + 32 * sub);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
             dst[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
         }
       }
+      // This thread's 32 keys (32 sub .. 32 sub + 31 of the segment): key j
+      // is in block kb = (32 sub + j) / kBL; it is the row's own block
+      // (block softmax) when kb == r / kBL, an earlier block (linear weight
+      // from A) when kb < r / kBL, and a later one (0) otherwise. v holds the
+      // scores (base 2) of own-block keys and A of earlier ones.
+      const int rb = r / kBL;
       float v32[32];
-      float part = 0.f;
-      if (sub <= quad) {
-        tmem_ld32(tbase + lane_bits + (sub == quad ? kColS : kColA) + 32 * sub, v32);
-        tmem_wait_ld();
-      }
-      if (sub == quad) {  // this row's own block: P = 2^{s - m}
-        float m2 = -FLT_MAX;
+      uint32_t own = 0u, early = 0u;  // bit j: key j's class
+      if (kBL >= 32) {  // one block per 32 keys, the same class for the whole warp
+        const int kb = (32 * sub) / kBL;
+        if (kb <= rb) {
+          tmem_ld32(tbase + lane_bits + (kb == rb ? kColS : kColA) + 32 * sub, v32);
+          tmem_wait_ld();
+          if (kb == rb) own = 0xffffffffu; else early = 0xffffffffu;
+        }
+      } else {  // two 16-key blocks per quarter; a warp's rows are in two blocks
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int hk = 0; hk < 2; ++hk) {
+          float sc[16], aw[16];
+          tmem_ld16(tbase + lane_bits + kColS + 32 * sub + 16 * hk, sc);
+          tmem_ld16(tbase + lane_bits + kColA + 32 * sub + 16 * hk, aw);
+          tmem_wait_ld();
+          const int kb = 2 * sub + hk;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v32[16 * hk + j] = kb == rb ? sc[j] : aw[j];
+          if (kb == rb) own |= 0xffffu << (16 * hk);
+          else if (kb < rb) early |= 0xffffu << (16 * hk);
+        }
+      }
+      // own-block keys: local max and sum, merged across the quarters below
+      float m_t = -FLT_MAX, P_t = 0.f, part = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if ((own >> j) & 1u) {
           v32[j] *= a.scale_log2;
-          m2 = fmaxf(m2, v32[j]);
+          m_t = fmaxf(m_t, v32[j]);
         }
-        float P = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v32[j] = ex2_approx(v32[j] - m2);
-          P += v32[j];
+      for (int j = 0; j < 32; ++j) {
+        if ((own >> j) & 1u) {
+          v32[j] = ex2_approx(v32[j] - m_t);
+          P_t += v32[j];
+        } else if ((early >> j) & 1u) {
+          part += v32[j];
         }
-        xm[r] = m2;
-        xP[r] = P;
-      } else if (sub < quad) {  // an earlier block of the segment
-#pragma unroll
-        for (int j = 0; j < 32; ++j) part += v32[j];
       }
+      xm[sub * 128 + r] = m_t;
+      xP[sub * 128 + r] = P_t;
       xa[sub * 128 + r] = part;
       named_bar_sync(1, 32 * kEpiWarps);
       // Z takes the segment's keys (every thread used Z for this segment in
       // E1; the column sums zq are complete since the barrier)
       if (sub == 0) {
         Zs[r] += (zq[r] + zq[128 + r]) + (zq[256 + r] + zq[384 + r]);
-        if (s + 1 == n_seg && ok) a.Z_pool[unit * kF + r] = Zs[r];
+        if (s + 1 == n_seg && ok && commits) a.Z_pool[unit * kF + r] = Zs[r];
       }
-      // row r's merge coefficients (its four threads compute the same)
+      // row r's merge coefficients (its four threads compute the same): the
+      // own block's max m2 and sum P merged exactly over the quarters
       float dn = (xden[r] + xden[128 + r]) + (xden[256 + r] + xden[384 + r]);
-      for (int q = 0; q < quad; ++q) dn += xa[q * 128 + r];
-      const float P = xP[r], m2 = xm[r];
+      dn += (xa[r] + xa[128 + r]) + (xa[256 + r] + xa[384 + r]);
+      float m2 = -FLT_MAX;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m2 = fmaxf(m2, xm[q * 128 + r]);
+      float P = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (xP[q * 128 + r] > 0.f) P = fmaf(xP[q * 128 + r], ex2_approx(xm[q * 128 + r] - m2), P);
+      const float own_scale = P_t > 0.f ? ex2_approx(m_t - m2) : 0.f;
       float cU, cN;
       if (a.merge == HB_MERGE_SHARED_NORM) {
         const float lam2 = log_sigmoid(gl) * kLog2e + m2;
@@ -538,16 +578,17 @@ __global__ void __maxnreg__(96)
         }
       }
       {
-        const float c = sub == quad ? cU : sub < quad ? cN : 0.f;
+        const float cu = cU * own_scale;
+        float cj[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          cj[j] = ((own >> j) & 1u) ? cu * v32[j] : ((early >> j) & 1u) ? cN * v32[j] : 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int j = 8 * q4 + 2 * p;
-            w4[p] = sub <= quad ? pack_bf16(c * v32[j], c * v32[j + 1]) : 0u;
-          }
-          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
+          const int j = 8 * q4;
+          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), pack_bf16(cj[j], cj[j + 1]),
+                       pack_bf16(cj[j + 2], cj[j + 3]), pack_bf16(cj[j + 4], cj[j + 5]),
+                       pack_bf16(cj[j + 6], cj[j + 7]));
         }
       }
       fence_proxy_async_smem();
@@ -606,7 +647,9 @@ __global__ void __maxnreg__(96)
 }  // namespace
 
 bool prompt_tc_fits(const Shape& s, int batch, int num_slots, int64_t seq_len) {
-  return production_shape(s) && (int64_t)batch * s.H <= (1 << 30) &&
+  return s.dtype == HB_DTYPE_BF16 && s.d == kD && s.f == kFH &&
+         (s.L == 16 || s.L == 32 || s.L == 64) && seq_len % s.L == 0 &&
+         (int64_t)batch * seq_len >= kSeg && (int64_t)batch * s.H <= (1 << 30) &&
          (int64_t)batch * seq_len < ((int64_t)1 << 31) &&
          (int64_t)num_slots * s.H * kF < ((int64_t)1 << 31);
 }
@@ -614,7 +657,8 @@ bool prompt_tc_fits(const Shape& s, int batch, int num_slots, int64_t seq_len) {
 cudaError_t launch_prompt_tc(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                              const void* k, const void* v, int64_t seq_len, float* S_pool,
                              float* Z_pool, int num_slots, const void* W, const float* gate,
-                             void* o, unsigned* status, cudaStream_t st) {
+                             void* o, unsigned* status, cudaStream_t st, bool commit_all,
+                             const int32_t* commit_mask) {
   Maps maps;
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)s.H, (uint64_t)batch * seq_len};
@@ -660,9 +704,12 @@ cudaError_t launch_prompt_tc(const Shape& s, int batch, const int32_t* slot_idx,
   a.qkv[2] = static_cast<const uint8_t*>(v);
   a.status = status;
   a.wait_limit = wait_limit_cycles();
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_prompt_tc), kSmemBytes);
+  a.commit_all = commit_all ? 1 : 0;
+  a.commit_mask = commit_mask;
+  auto* kernel = s.L == 16 ? k_prompt_tc<16> : s.L == 64 ? k_prompt_tc<64> : k_prompt_tc<32>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
-  k_prompt_tc<<<dim3(batch * s.H), kThreads, kSmemBytes, st>>>(maps, a);
+  kernel<<<dim3(batch * s.H), kThreads, kSmemBytes, st>>>(maps, a);
   return cudaGetLastError();
 }
 
