@@ -342,6 +342,7 @@ class ServeResult:
             "tokens_per_s_device": self.tokens / self.device_s if self.device_s else 0.0,
             "peak_active": self.peak_active, "mean_active": self.mean_active,
             "capacity_limit": self.capacity_limit, "finished": self.finished,
+            "device_phases": getattr(self, "phases", None),
         }
 
 
@@ -365,6 +366,8 @@ def simulate(backend, cfg: ServeConfig, max_steps: int = None, trace: list = Non
         if not plan.active:
             raise RuntimeError("no request fits the memory budget")
         a = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m2 = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         if plan.admitted:
@@ -377,11 +380,13 @@ def simulate(backend, cfg: ServeConfig, max_steps: int = None, trace: list = Non
         slots_host = [r.slot for r in plan.active]
         slots = torch.tensor(slots_host, dtype=torch.int32).to(dev, non_blocking=True)
         commit = torch.tensor(plan.commit, dtype=torch.int32).to(dev, non_blocking=True)
+        m1.record(stream)
         backend.step(slots, commit)
+        m2.record(stream)
         if isinstance(backend, SoftmaxBackend):
             backend.append(plan, slots_host)
         b.record(stream)
-        events.append((a, b))
+        events.append((a, m1, m2, b))
         if trace is not None:
             for b, (r, c) in enumerate(zip(plan.active, plan.commit)):
                 if c:
@@ -393,10 +398,15 @@ def simulate(backend, cfg: ServeConfig, max_steps: int = None, trace: list = Non
         steps += 1
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
-    step_ms = [a.elapsed_time(b) for a, b in events]
-    return ServeResult(backend.name, steps, sched.tokens_done, wall, sum(step_ms) / 1e3,
-                       sched.peak_active, active_sum / max(steps, 1), sched.capacity_limit(),
-                       len(sched.finished), step_ms)
+    step_ms = [a.elapsed_time(b) for a, m1, m2, b in events]
+    phases = {"before_attend_s": sum(a.elapsed_time(m1) for a, m1, m2, b in events) / 1e3,
+              "attend_s": sum(m1.elapsed_time(m2) for a, m1, m2, b in events) / 1e3,
+              "after_attend_s": sum(m2.elapsed_time(b) for a, m1, m2, b in events) / 1e3}
+    res = ServeResult(backend.name, steps, sched.tokens_done, wall, sum(step_ms) / 1e3,
+                      sched.peak_active, active_sum / max(steps, 1), sched.capacity_limit(),
+                      len(sched.finished), step_ms)
+    res.phases = phases
+    return res
 
 
 def compare(cfg: ServeConfig, device, max_steps: int = None) -> dict:
