@@ -45,7 +45,6 @@ using namespace ptx;
 
 constexpr int kD = 128, kFH = 64, kF = 128;
 constexpr int kThreads = 96 + 512;  // k producer, MMA, v producer, 16 epilogue warps
-constexpr int kTargetCtas = 148;  // SMs of a B300; splits aim to fill them once
 
 // Shared-memory layout (bytes from a 1024-aligned base).
 constexpr int kOffK = 0;            // 2 stages x 2 boxes x [128 rows][128 B]
@@ -573,10 +572,15 @@ __global__ void __launch_bounds__(256) k_state_reduce(const __grid_constant__ Ar
   }
 }
 
+// Splits per (request, head) so that the grid fills the current device's
+// SMs about once (one CTA per SM); the workspace size query and the launch
+// both call this on the current device, so they agree.
 int splits_for(int batch, int H, int64_t max_seqlen) {
   const int64_t units = (int64_t)batch * H;
   const int64_t chunks = (max_seqlen + 127) / 128;
-  int64_t s = kTargetCtas / (units > 0 ? units : 1);
+  int sms = 0;
+  if (current_sm_count(&sms) != cudaSuccess || sms <= 0) sms = 148;
+  int64_t s = sms / (units > 0 ? units : 1);
   if (s > chunks) s = chunks;
   if (s > 64) s = 64;
   return s < 1 ? 1 : (int)s;
