@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  grid_dep_launch();  // the split reduction may be scheduled as SMs free up
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bar[kKFull0 + s]);
       }
     }
+    __syncwarp();  // the warp reaches the block barrier at the end converged
   } else if (warp == 2) {
     // ----------------------------------------------------- v producer
     // v of chunk c is loaded once phi^T V of chunk c - 2 has completed
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bar[kVFull0 + s]);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && n_my > 0) {
@@ -293,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) atomicOr(a.status, kStatusTimeout);
       umma_commit(&bar[kAccFull]);
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
     // 16 warps. Warp w (3..18) reads TMEM lane quarter q = w % 4 (tokens
@@ -540,7 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Sums the split partials of each unit in split order and writes S/Z.
+// Block (h, b, z) takes elements z * 256 + t, stepping by 256 * gridDim.z,
+// so a few units still spread over many SMs. Launched as a programmatic
+// dependent of k_state_tc: it waits for that grid before reading anything.
 __global__ void __launch_bounds__(256) k_state_reduce(const __grid_constant__ Args a) {
+  grid_dep_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   int64_t row0, cnt;
   if (!unit_range(a, b, &row0, &cnt)) return;  // flagged by k_state_tc
@@ -551,8 +559,9 @@ __global__ void __launch_bounds__(256) k_state_reduce(const __grid_constant__ Ar
   float4* S = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD);
   float4* Z = reinterpret_cast<float4*>(a.Z_pool + unit * kF);
   constexpr int n4 = kPartialFloats / 4;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+  for (int i = blockIdx.z * blockDim.x + threadIdx.x; i < n4; i += blockDim.x * gridDim.z) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int j = 0; j < a.splits; ++j) {
       const float4 p = part[(size_t)j * n4 + i];
       acc.x += p.x;
@@ -631,8 +640,11 @@ cudaError_t launch_tc(const Shape& s, int batch, const int32_t* slot_idx, const 
   k_state_tc<<<dim3(splits, s.H, batch), kThreads, kSmemBytes, st>>>(maps, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (splits > 1) {
-    k_state_reduce<<<dim3(s.H, batch), 256, 0, st>>>(a);
-    e = cudaGetLastError();
+    // enough blocks per unit that the reduction runs on every SM
+    const int64_t units = (int64_t)batch * s.H;
+    int z = (int)((4 * 148 + units - 1) / units);
+    z = z < 1 ? 1 : (z > 16 ? 16 : z);
+    e = launch_pdl(k_state_reduce, dim3(s.H, batch, z), dim3(256), 0, st, a);
   }
   return e;
 }

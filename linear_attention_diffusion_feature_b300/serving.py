@@ -409,11 +409,23 @@ def simulate(backend, cfg: ServeConfig, max_steps: int = None, trace: list = Non
     return res
 
 
-def compare(cfg: ServeConfig, device, max_steps: int = None) -> dict:
-    """The same request stream on both servers."""
+def compare(cfg: ServeConfig, device, max_steps: int = None, warmup: bool = True) -> dict:
+    """The same request stream on both servers.
+
+    With ``warmup``, each server first runs the stream's first block
+    (admission, ``steps_per_block`` steps and the commit) on a throwaway
+    backend of the same shapes, untimed: the first use of a device function
+    in a process (module loading, and a just-in-time compile where the
+    binary holds no code for the device) can stall the host for seconds,
+    and without the warm-up that stall lands in the first timed step."""
     syn = _Synthetic(cfg, device)
     out = {}
     for cls in (HybridBackend, SoftmaxBackend):
+        if warmup:
+            be = cls(cfg, device, syn)
+            simulate(be, cfg, cfg.steps_per_block + 1)
+            del be
+            torch.cuda.empty_cache()
         be = cls(cfg, device, syn)
         out[be.name] = simulate(be, cfg, max_steps).as_dict()
         del be
