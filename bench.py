@@ -1098,9 +1098,10 @@ def run_prefill_attend(args):
 
 def run_blocklen(args):
     """The continuous-batching step (64 requests, 16 committing, hb_block_attend_commit)
-    at block lengths L = 16, 32 and 64: L = 32 takes the persistent attend
-    kernel, 16 and 64 the segment kernel on a one-block prompt. Six layer
-    instances in turn, graphs of 600 steps replayed for >= 0.5 s."""
+    at block lengths L = 16, 32 and 64: L = 32 and 16 take the persistent
+    attend kernel (16-token blocks in its 32-row tiles), 64 the segment
+    kernel on a one-block prompt. Six layer instances in turn, graphs of 600
+    steps replayed for >= 0.5 s."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
@@ -1146,7 +1147,10 @@ def run_blocklen(args):
                   + N_COMMIT * H * (F * D * 4 + F * 4))
         out.append({"block_len": Lb, "ms": ms, "tokens_per_s": B * Lb / (ms / 1e3),
                     "algorithmic_bytes": nbytes, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak,
-                    "kernel": "k_attend_fast (persistent)" if Lb == 32 else "k_prompt_tc"})
+                    "achieved_gbs": nbytes / (ms / 1e3) / 1e9,
+                    "kernel": {32: "k_attend_fast (persistent)",
+                               16: "k_attend_fast (persistent, 16-token blocks in 32-row tiles)"}
+                    .get(Lb, "k_prompt_tc")})
         del layers, g
         torch.cuda.empty_cache()
     top = out[0]
@@ -1158,8 +1162,9 @@ def run_blocklen(args):
         "config": {"workload": "hb_block_attend_commit, 64 requests x 16 heads, d=128, f=64, "
                                "16 committing, prefixes 32*U{8..128}", "block_lens": args.block_lens,
                    "timing": "graphs of 600 steps over 6 layer instances, >= 0.5 s of replays"},
-        "roofline": {"kernel": top["kernel"], "bound": "hbm", "achieved": None, "peak": peak,
-                     "unit": "GB/s", "frac": top["hbm_frac"], "peak_kind": kind, "traffic": None},
+        "roofline": {"kernel": top["kernel"], "bound": "hbm", "achieved": top["achieved_gbs"],
+                     "peak": peak, "unit": "GB/s", "frac": top["hbm_frac"], "peak_kind": kind,
+                     "traffic": None},
         "sweep": out,
         "gpu_launches": None,
     }

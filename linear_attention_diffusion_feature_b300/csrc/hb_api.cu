@@ -154,13 +154,13 @@ hb_status hb_block_attend(const hb_config* cfg, int32_t batch, const int32_t* sl
   cudaError_t e = hb::status_word_ptr(&status);
   if (e != cudaSuccess) return HB_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
+  if (hb::fast_attend_step_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, nullptr, o, status,
                                                 st, s.L, 0, false));
   if (hb::prompt_tc_fits(s, batch, num_slots, s.L))
-    // blocks of 16 or 64 tokens: the segment kernel on a one-block prompt,
-    // the states only read
+    // blocks of 64 tokens: the segment kernel on a one-block prompt, the
+    // states only read
     return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, s.L,
                                               const_cast<float*>(S_pool),
                                               const_cast<float*>(Z_pool), num_slots, W,
@@ -193,7 +193,7 @@ hb_status hb_block_attend_s16(const hb_config* cfg, int32_t batch, const int32_t
   hb_status r = hb::check_config(cfg, &s);
   if (r != HB_OK) return r;
   if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
-  if (!hb::fast_attend_ok(s)) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (!hb::fast_attend_step_ok(s)) return HB_ERR_UNSUPPORTED_SHAPE;
   if (batch == 0) return HB_OK;
   if (batch > 65535 * 32 || !hb::attend_fast_fits(s, batch, num_slots, s.L))
     return HB_ERR_UNSUPPORTED_SHAPE;
@@ -223,12 +223,12 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int3
   unsigned* status = nullptr;
   if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (hb::fast_attend_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
+  if (hb::fast_attend_step_ok(s) && hb::attend_fast_fits(s, batch, num_slots, s.L))
     return hb::from_cuda(hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool,
                                                 num_slots, W, gate_logits, commit, o, status,
                                                 st, s.L, 0, false));
   if (hb::prompt_tc_fits(s, batch, num_slots, s.L))
-    // blocks of 16 or 64 tokens: the segment kernel on a one-block prompt;
+    // blocks of 64 tokens: the segment kernel on a one-block prompt;
     // committing requests write their new state back
     return hb::from_cuda(hb::launch_prompt_tc(s, batch, slot_idx, q, k, v, s.L, S_pool, Z_pool,
                                               num_slots, W, gate_logits, o, status, st, false,
@@ -252,7 +252,7 @@ hb_status hb_block_attend_commit_s16(const hb_config* cfg, int32_t batch,
   hb_status r = hb::check_config(cfg, &s);
   if (r != HB_OK) return r;
   if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
-  if (!hb::fast_attend_ok(s)) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (!hb::fast_attend_step_ok(s)) return HB_ERR_UNSUPPORTED_SHAPE;
   if (batch == 0) return HB_OK;
   if (batch > 65535 * 32 || !hb::attend_fast_fits(s, batch, num_slots, s.L))
     return HB_ERR_UNSUPPORTED_SHAPE;
@@ -329,7 +329,7 @@ cudaError_t attend_grouped(const hb::Shape& s, int Hkv, int batch, const int32_t
                            const float* Z_pool, int num_slots, const void* Wq,
                            const float* gate, void* o, unsigned* status, cudaStream_t st,
                            int64_t rows_per_req, int64_t row_base) {
-  if (hb::fast_attend_ok(s) && fast_group_ok(s.H / Hkv) &&
+  if (hb::fast_attend_step_ok(s) && fast_group_ok(s.H / Hkv) &&
       hb::attend_fast_fits(s, batch, num_slots, rows_per_req))
     return hb::launch_attend_fast(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, Wq,
                                   gate, nullptr, o, status, st, (int)rows_per_req, (int)row_base,

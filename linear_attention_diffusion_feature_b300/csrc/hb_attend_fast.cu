@@ -128,6 +128,11 @@ struct Maps {
   // SM clocks after which a wait of the unit pipeline gives up (hb_set_wait_limit);
   // the final drain of copies already issued always takes the full limit
   long long wait_limit;
+  // tokens of a block: 32, or 16 (a decoding step with 16-token blocks: the
+  // 32-row tiles hold the block and 16 rows past it, which take no part:
+  // their keys are masked out of the block softmax, their k rows out of the
+  // commit, and their outputs are not stored)
+  int valid_rows;
   const uint8_t* s16;  // dual-copy step: the bf16 copies (L2 prefetch of a unit's copy)
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16 attend only: bf16, box {64, 128}
   CUtensorMap S16;  // dual-copy step: the bf16 copies [slots*H*F rows][d], box {64, 128}
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all heads; the CTAs working on its heads at the same time each
       // prefetch a 1/H slice of it, so DRAM reads it as one long run
       // (k and v have H / G heads: their block is G times smaller)
-      const size_t slice = (size_t)kL * kD * 2;  // = q block bytes / H
+      const size_t slice = (size_t)maps.valid_rows * kD * 2;  // = q block bytes / H
       const size_t row0 = (size_t)b * maps.rows_per_req + maps.row_base;
       prefetch_l2(maps.qkv[0] + row0 * H * kD * 2 + (size_t)h * slice, (uint32_t)slice);
       const size_t kv_slice = slice / G;
@@ -777,8 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    const int vrows = maps.valid_rows;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) acc_s[r] *= scale;  // scale * log2(e): scores in base 2
+    for (int r = 0; r < 4; ++r) {
+      acc_s[r] *= scale;  // scale * log2(e): scores in base 2
+      if (8 * nq + 2 * t + (r & 1) >= vrows) acc_s[r] = -INFINITY;  // a key past the block
+    }
     {
       float mx0 = fmaxf(fmaxf(acc_u[0][0], acc_u[0][1]), fmaxf(acc_u[1][0], acc_u[1][1]));
       float mx1 = fmaxf(fmaxf(acc_u[0][2], acc_u[0][3]), fmaxf(acc_u[1][2], acc_u[1][3]));
@@ -954,6 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 c = *reinterpret_cast<const float4*>(sums + (kSumMK * 32 + R) * 4);
         ip[hr] = rcp_approx((a.x + a.y) + (a.z + a.w));  // ~1e-7 relative
         im[hr] = rcp_approx((c.x + c.y) + (c.z + c.w));
+        if (R >= vrows) ip[hr] = im[hr] = 0.f;  // a row past the block: phi(k) = 0
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -1129,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk.y = pack_bf16(ov[2], ov[3]);
         const size_t orow =
             (size_t)b * maps.rows_per_req + (kSeq ? i * kL : maps.row_base) + R;
-        *reinterpret_cast<uint2*>(o + (orow * H + h) * kD + c0 + 4 * t) = pk;
+        if (R < vrows) *reinterpret_cast<uint2*>(o + (orow * H + h) * kD + c0 + 4 * t) = pk;
       }
     }
 
@@ -1216,6 +1226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool fast_attend_ok(const Shape& s) { return production_shape(s); }
 
+bool fast_attend_step_ok(const Shape& s) {
+  Shape s32 = s;
+  s32.L = kL;
+  return production_shape(s32) && (s.L == kL || s.L == 16);
+}
+
 bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req) {
   return (int64_t)num_slots * s.H * kF < ((int64_t)1 << 31) &&
          (int64_t)batch * rows_per_req < ((int64_t)1 << 31);
@@ -1242,7 +1258,10 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
     return cudaErrorInvalidValue;
   const bool sep_wk = Wk != nullptr && Wk != W;
   if (sep_wk && !sequential) return cudaErrorInvalidValue;
+  // blocks of 16 tokens in a decoding step; prompts walk 32-token blocks
+  if (sequential ? s.L != kL : (s.L != kL && s.L != 16)) return cudaErrorInvalidValue;
   Maps maps;
+  maps.valid_rows = sequential ? kL : s.L;
   maps.kv_group = s.H / Hkv;
   maps.sep_wk = sep_wk ? 1 : 0;
   maps.s16 = static_cast<const uint8_t*>(S16_pool);
@@ -1324,7 +1343,7 @@ cudaError_t launch_attend_commit_dual(const Shape& s, int batch, const int32_t* 
                                       const float* gate, const int32_t* commit_mask, void* o,
                                       unsigned* status, cudaStream_t st) {
   return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
-                            commit_mask, o, status, st, kL, 0, false, false, false, S16_pool);
+                            commit_mask, o, status, st, s.L, 0, false, false, false, S16_pool);
 }
 
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
@@ -1344,7 +1363,7 @@ cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slo
                                    const void* W, const float* gate, void* o, unsigned* status,
                                    cudaStream_t st) {
   return launch_attend_impl(s, batch, slot_idx, q, k, v, S16_pool, Z_pool, num_slots, W, gate,
-                            nullptr, o, status, st, kL, 0, false, false, true);
+                            nullptr, o, status, st, s.L, 0, false, false, true);
 }
 
 }  // namespace hb

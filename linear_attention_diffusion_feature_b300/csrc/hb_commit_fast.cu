@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
+  __syncwarp();  // warps whose lane 0 ran a role alone reach the barrier converged
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

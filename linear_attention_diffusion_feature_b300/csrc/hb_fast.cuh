@@ -34,6 +34,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 
 bool fast_feature_map_ok(const Shape& s);
 bool fast_attend_ok(const Shape& s);
+// a decoding step (not the sequential mode): blocks of 32 or 16 tokens
+bool fast_attend_step_ok(const Shape& s);
 bool fast_state_ok(const Shape& s);
 bool fast_softmax_kv_ok(const Shape& s);
 

@@ -637,6 +637,7 @@ __global__ void __maxnreg__(96)
   }
 
   tc_fence_before();
+  __syncwarp();  // warps whose lane 0 ran a role alone reach the barrier converged
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

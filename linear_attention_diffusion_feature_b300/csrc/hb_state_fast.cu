@@ -221,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bar[kKFull0 + s]);
       }
     }
-    __syncwarp();  // the warp reaches the block barrier at the end converged
   } else if (warp == 2) {
     // ----------------------------------------------------- v producer
     // v of chunk c is loaded once phi^T V of chunk c - 2 has completed
@@ -240,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bar[kVFull0 + s]);
       }
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && n_my > 0) {
@@ -296,7 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) atomicOr(a.status, kStatusTimeout);
       umma_commit(&bar[kAccFull]);
     }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
     // 16 warps. Warp w (3..18) reads TMEM lane quarter q = w % 4 (tokens
@@ -536,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  __syncwarp();  // warps whose lane 0 ran a role alone reach the barrier converged
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
