@@ -494,15 +494,33 @@ __global__ void __maxnreg__(96)
       // scores (base 2) of own-block keys and A of earlier ones.
       const int rb = r / kBL;
       float v32[32];
-      uint32_t own = 0u, early = 0u;  // bit j: key j's class
-      if (kBL >= 32) {  // one block per 32 keys, the same class for the whole warp
-        const int kb = (32 * sub) / kBL;
-        if (kb <= rb) {
-          tmem_ld32(tbase + lane_bits + (kb == rb ? kColS : kColA) + 32 * sub, v32);
+      float m_t = -FLT_MAX, P_t = 0.f, part = 0.f;
+      // kBL >= 32: one block per 32 keys, so the class is the warp's (no
+      // per-key selection); kBL = 16: two blocks per quarter, per-key masks
+      const int kbw = (32 * sub) / kBL;
+      const bool w_own = kBL >= 32 && kbw == rb, w_early = kBL >= 32 && kbw < rb;
+      uint32_t own = 0u, early = 0u;  // kBL = 16: bit j is key j's class
+      if constexpr (kBL >= 32) {
+        if (w_own || w_early) {
+          tmem_ld32(tbase + lane_bits + (w_own ? kColS : kColA) + 32 * sub, v32);
           tmem_wait_ld();
-          if (kb == rb) own = 0xffffffffu; else early = 0xffffffffu;
         }
-      } else {  // two 16-key blocks per quarter; a warp's rows are in two blocks
+        if (w_own) {  // P = 2^{s - m} over the own block's keys held here
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v32[j] *= a.scale_log2;
+            m_t = fmaxf(m_t, v32[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v32[j] = ex2_approx(v32[j] - m_t);
+            P_t += v32[j];
+          }
+        } else if (w_early) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) part += v32[j];
+        }
+      } else {
 #pragma unroll
         for (int hk = 0; hk < 2; ++hk) {
           float sc[16], aw[16];
@@ -515,22 +533,21 @@ __global__ void __maxnreg__(96)
           if (kb == rb) own |= 0xffffu << (16 * hk);
           else if (kb < rb) early |= 0xffffu << (16 * hk);
         }
-      }
-      // own-block keys: local max and sum, merged across the quarters below
-      float m_t = -FLT_MAX, P_t = 0.f, part = 0.f;
+        // own-block keys: local max and sum, merged across the quarters below
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if ((own >> j) & 1u) {
-          v32[j] *= a.scale_log2;
-          m_t = fmaxf(m_t, v32[j]);
-        }
+        for (int j = 0; j < 32; ++j)
+          if ((own >> j) & 1u) {
+            v32[j] *= a.scale_log2;
+            m_t = fmaxf(m_t, v32[j]);
+          }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if ((own >> j) & 1u) {
-          v32[j] = ex2_approx(v32[j] - m_t);
-          P_t += v32[j];
-        } else if ((early >> j) & 1u) {
-          part += v32[j];
+        for (int j = 0; j < 32; ++j) {
+          if ((own >> j) & 1u) {
+            v32[j] = ex2_approx(v32[j] - m_t);
+            P_t += v32[j];
+          } else if ((early >> j) & 1u) {
+            part += v32[j];
+          }
         }
       }
       xm[sub * 128 + r] = m_t;
@@ -544,17 +561,25 @@ __global__ void __maxnreg__(96)
         if (s + 1 == n_seg && ok && commits) a.Z_pool[unit * kF + r] = Zs[r];
       }
       // row r's merge coefficients (its four threads compute the same): the
-      // own block's max m2 and sum P merged exactly over the quarters
+      // own block's max m2 and sum P (kBL = 32: one quarter holds the whole
+      // block; otherwise merged exactly over the quarters that hold a part)
       float dn = (xden[r] + xden[128 + r]) + (xden[256 + r] + xden[384 + r]);
       dn += (xa[r] + xa[128 + r]) + (xa[256 + r] + xa[384 + r]);
-      float m2 = -FLT_MAX;
+      float m2, P, own_scale;
+      if constexpr (kBL == 32) {
+        m2 = xm[quad * 128 + r];
+        P = xP[quad * 128 + r];
+        own_scale = 1.f;
+      } else {
+        m2 = -FLT_MAX;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) m2 = fmaxf(m2, xm[q * 128 + r]);
-      float P = 0.f;
+        for (int q = 0; q < 4; ++q) m2 = fmaxf(m2, xm[q * 128 + r]);
+        P = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (xP[q * 128 + r] > 0.f) P = fmaf(xP[q * 128 + r], ex2_approx(xm[q * 128 + r] - m2), P);
-      const float own_scale = P_t > 0.f ? ex2_approx(m_t - m2) : 0.f;
+        for (int q = 0; q < 4; ++q)
+          if (xP[q * 128 + r] > 0.f) P = fmaf(xP[q * 128 + r], ex2_approx(xm[q * 128 + r] - m2), P);
+        own_scale = P_t > 0.f ? ex2_approx(m_t - m2) : 0.f;
+      }
       float cU, cN;
       if (a.merge == HB_MERGE_SHARED_NORM) {
         const float lam2 = log_sigmoid(gl) * kLog2e + m2;
@@ -577,7 +602,20 @@ __global__ void __maxnreg__(96)
           cN = 0.f;
         }
       }
-      {
+      if constexpr (kBL >= 32) {
+        // C = cU P on the own block, cN A on earlier ones, 0 on later ones
+        const float c = w_own ? cU * own_scale : w_early ? cN : 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int j = 8 * q4 + 2 * p;
+            w4[p] = (w_own || w_early) ? pack_bf16(c * v32[j], c * v32[j + 1]) : 0u;
+          }
+          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
+        }
+      } else {
         const float cu = cU * own_scale;
         float cj[32];
 #pragma unroll
