@@ -848,8 +848,9 @@ def run_stack(args):
     """6 linearized layers, P=2,048-token prefixes, B in {1, 16, 64, 256}:
     one stack step = hb_block_attend of all 6 layers, timed against
     hb_softmax_kv_attend of the same 6 layers over the same prefixes kept as
-    a KV cache, and against hb_block_attend_s16 on bf16 copies of the same
-    states (bit-identical output, half the state bytes)."""
+    a KV cache, against hb_block_attend_s16 on bf16 copies of the same
+    states (bit-identical output, half the state bytes), and against
+    hb_block_attend_s8 on fp8 copies (a quarter of the state bytes; lossy)."""
     import linear_attention_diffusion_feature_b300 as hb
     from linear_attention_diffusion_feature_b300 import inputs
 
@@ -872,8 +873,12 @@ def run_stack(args):
                                 t["W"], S, Z)
             S16 = torch.empty((nB, H, F, D), dtype=torch.bfloat16, device=device)
             hb.hb_state_to_bf16(cfg, sl, S, S16)
+            S8 = torch.empty((nB, H, F, D), dtype=torch.uint8, device=device)
+            sc8 = torch.empty((nB, H), dtype=torch.float32, device=device)
+            hb.hb_state_to_fp8(cfg, sl, S, S8, sc8)
             need = hb.hb_softmax_kv_workspace_size(cfg, nB, P)
-            layers.append(dict(t=t, S=S, S16=S16, Z=Z, sl=sl, o=torch.empty_like(t["q"]),
+            layers.append(dict(t=t, S=S, S16=S16, S8=S8, sc8=sc8, Z=Z, sl=sl,
+                               o=torch.empty_like(t["q"]),
                                ws=torch.empty(max(need, 16), dtype=torch.uint8, device=device)))
         torch.cuda.synchronize()
 
@@ -889,6 +894,12 @@ def run_stack(args):
                 hb.hb_block_attend_s16(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S16"], ly["Z"],
                                        t["W"], t["gate"], o=ly["o"])
 
+        def hybrid_s8():
+            for ly in layers:
+                t = ly["t"]
+                hb.hb_block_attend_s8(cfg, ly["sl"], t["q"], t["k"], t["v"], ly["S8"], ly["sc8"],
+                                      ly["Z"], t["W"], t["gate"], o=ly["o"])
+
         def softmax():
             for ly in layers:
                 t = ly["t"]
@@ -898,11 +909,14 @@ def run_stack(args):
         reps = max(3, min(args.steps, 200))
         h_ms = _graph_ms(hybrid, 1, reps, args.warmup, stream)
         h16_ms = _graph_ms(hybrid_s16, 1, reps, args.warmup, stream)
+        h8_ms = _graph_ms(hybrid_s8, 1, reps, args.warmup, stream)
         s_ms = _graph_ms(softmax, 1, max(3, reps // 4), args.warmup, stream)
         assert hb.hb_get_device_status() == 0
         hb_bytes = N_LAYERS * (nB * ATTEND_BYTES_PER_REQUEST + ATTEND_BYTES_W)
         # the bf16 copy halves the state read: S is H * F * d * 2 bytes per request
         hb16_bytes = hb_bytes - N_LAYERS * nB * H * F * D * 2
+        # the fp8 copy: S is H * F * d bytes per request, plus a 4-byte scale per head
+        hb8_bytes = hb_bytes - N_LAYERS * nB * H * (F * D * 3 - 4)
         sm_bytes = N_LAYERS * nB * ((P + L) * H * D * 2 * 2 + 2 * L * H * D * 2)
         sweep.append({
             "batch": nB, "hybrid_ms": h_ms, "softmax_kv_ms": s_ms,
@@ -918,6 +932,11 @@ def run_stack(args):
             "s16_speedup": h_ms / h16_ms,
             "s16_note": "attend only, on copies written once before timing; the refresh a "
                         "commit makes necessary (hb_state_to_bf16) is not in this number",
+            "hybrid_s8_ms": h8_ms, "hybrid_s8_tokens_per_s": nB * L / (h8_ms / 1e3),
+            "hybrid_s8_frac": hb8_bytes / (h8_ms / 1e3) / 1e9 / peak,
+            "s8_speedup": h_ms / h8_ms,
+            "s8_note": "attend only, on fp8 copies written once before timing (lossy: the "
+                       "output is the attend on the dequantised state)",
         })
         del layers
         torch.cuda.empty_cache()

@@ -183,6 +183,51 @@ hb_status hb_block_attend_s16(const hb_config* cfg, int32_t batch,
                               hb_stream_t stream);
 
 /*
+ * hb_state_to_fp8 — write an fp8 (e4m3) copy of the listed slots' S with one
+ * scale per (slot, head), for hb_block_attend_s8 (gist.science technical
+ * summary, state-compression bullet: a fixed-size state read at every step;
+ * the copy is this library's layout, not the pages'). For each listed slot
+ * and head: scale = max|S| / 448 in fp32 (rounded to nearest; 448 is the
+ * largest finite e4m3 value) and code[i][j] = e4m3(S[i][j] / scale), the
+ * quotient rounded to nearest in fp32 and then to the nearest e4m3 value
+ * (ties to even, saturating at +-448); a head whose S is all zero gets
+ * scale 0 and zero codes. The same staleness rule as hb_state_to_bf16
+ * applies: every call listed there leaves the fp8 copy stale too.
+ *   slot_idx    [batch] int32, device
+ *   S_pool      [num_slots, H, F, d] fp32, read
+ *   S8_pool     [num_slots, H, F, d] uint8 codes, written for listed slots
+ *   scale_pool  [num_slots, H] fp32, written for listed slots
+ * A slot outside [0, num_slots) is skipped and flagged as HB_ERR_DEVICE_BOUNDS.
+ */
+hb_status hb_state_to_fp8(const hb_config* cfg, int32_t batch,
+                          const int32_t* slot_idx, const float* S_pool,
+                          void* S8_pool, float* scale_pool, int32_t num_slots,
+                          hb_stream_t stream);
+
+/*
+ * hb_block_attend_s8 — hb_block_attend reading the fp8 copy written by
+ * hb_state_to_fp8: each (request, head) reads 16 KiB of state instead of 64.
+ * The output is the attend on the dequantised state S' = scale * code (the
+ * codes enter the state contraction exactly, as f16, with phi(q) as f16, and
+ * the scale multiplies the linear read), so it differs from hb_block_attend's
+ * by the copy's rounding: at the pages' shapes about 2e-3 of the output's
+ * range, inside the 1e-2 bound of the bf16 outputs. Z is read from the fp32
+ * pool. Production shape only (bf16, d = 128, f = 64, L = 32 or 16); any
+ * other shape returns HB_ERR_UNSUPPORTED_SHAPE.
+ *   S8_pool     [num_slots, H, F, d] uint8 codes, read only
+ *   scale_pool  [num_slots, H] fp32, read only
+ *   Z_pool      [num_slots, H, F] fp32, read only (the master's Z)
+ *   other arguments as in hb_block_attend.
+ */
+hb_status hb_block_attend_s8(const hb_config* cfg, int32_t batch,
+                             const int32_t* slot_idx, const void* q,
+                             const void* k, const void* v, const void* S8_pool,
+                             const float* scale_pool, const float* Z_pool,
+                             int32_t num_slots, const void* W,
+                             const float* gate_logits, void* o,
+                             hb_stream_t stream);
+
+/*
  * hb_block_attend_commit — hb_block_attend followed, for the requests whose
  * block is finished, by hb_commit_block of that same block, in one pass over
  * the state (gist.science technical summary, state-compression bullet: the

@@ -30,8 +30,10 @@ from .hb import (  # noqa: F401
     hb_softmax_kv_attend_paged,
     hb_softmax_kv_workspace_size,
     hb_block_attend_s16,
+    hb_block_attend_s8,
     hb_state_copy,
     hb_state_to_bf16,
+    hb_state_to_fp8,
     hb_state_zero,
     hb_status_string,
 )

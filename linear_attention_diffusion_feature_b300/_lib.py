@@ -75,6 +75,11 @@ SIGNATURES = {
     "hb_state_zero": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
     "hb_state_to_bf16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_int32,
                                    c_void_p]),
+    "hb_state_to_fp8": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_int32, c_void_p]),
+    "hb_block_attend_s8": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                     c_void_p, c_void_p]),
     "hb_block_attend_s16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                       c_void_p]),

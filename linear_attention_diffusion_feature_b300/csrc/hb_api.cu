@@ -206,6 +206,47 @@ hb_status hb_block_attend_s16(const hb_config* cfg, int32_t batch, const int32_t
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+hb_status hb_state_to_fp8(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                          const float* S_pool, void* S8_pool, float* scale_pool,
+                          int32_t num_slots, hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, S_pool, S8_pool, scale_pool})) != HB_OK) return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  return hb::from_cuda(hb::launch_state_to_fp8(s, batch, slot_idx, S_pool, S8_pool, scale_pool,
+                                               num_slots, status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hb_status hb_block_attend_s8(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
+                             const void* q, const void* k, const void* v, const void* S8_pool,
+                             const float* scale_pool, const float* Z_pool, int32_t num_slots,
+                             const void* W, const float* gate_logits, void* o,
+                             hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (!hb::fast_attend_step_ok(s)) return HB_ERR_UNSUPPORTED_SHAPE;
+  if (batch == 0) return HB_OK;
+  if (batch > 65535 * 32 || !hb::attend_fast_fits(s, batch, num_slots, s.L))
+    return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, q, k, v, S8_pool, scale_pool, Z_pool, W, gate_logits,
+                           o})) != HB_OK)
+    return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  return hb::from_cuda(hb::launch_attend_fast_s8(s, batch, slot_idx, q, k, v, S8_pool,
+                                                 scale_pool, Z_pool, num_slots, W, gate_logits,
+                                                 o, status,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int32_t* slot_idx,
                                  const void* q, const void* k, const void* v, float* S_pool,
                                  float* Z_pool, int32_t num_slots, const void* W,

@@ -99,8 +99,8 @@ constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, 
 constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
 constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x 3 x [32]
 constexpr int kOffBar = kOffFin + 2 * 3 * 128;
-constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head
-constexpr int kOffTmemSlot = kOffMeta + 32;
+constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head, fp8 scale
+constexpr int kOffTmemSlot = kOffMeta + 48;
 // committing variant: the commit mask as one bit per request, 32 per word
 constexpr int kMaskWords = 1024;  // batches up to 32768 are scheduled commit-first
 constexpr int kOffMaskBits = kOffTmemSlot + 16;
@@ -134,6 +134,8 @@ struct Maps {
   // commit, and their outputs are not stored)
   int valid_rows;
   const uint8_t* s16;  // dual-copy step: the bf16 copies (L2 prefetch of a unit's copy)
+  // fp8 attend (kS8): the scale of each (slot, head) copy, S = scale * code
+  const float* s8_scale;
   CUtensorMap S;  // [slots*H*F rows][d] fp32, box {32, 128}; kS16 attend only: bf16, box {64, 128}
   CUtensorMap S16;  // dual-copy step: the bf16 copies [slots*H*F rows][d], box {64, 128}
   CUtensorMap q;  // [B*L][H][d] bf16, box {64, 1, 32}
@@ -159,6 +161,11 @@ __device__ __forceinline__ uint32_t s16_off(int k, int n) {
   return (uint32_t)((n >> 6) * 16384 + k * 128 + ((((n & 63) >> 3) ^ (k & 7)) << 4) +
                     (n & 7) * 2);
 }
+// Byte offset of code S[k][n] (fp8 copy of the state) in the SW128 box of
+// the stage's S region ([128 F rows][128 codes]).
+__device__ __forceinline__ uint32_t s8_off(int k, int n) {
+  return (uint32_t)(k * 128 + ((((n >> 4) ^ (k & 7))) << 4) + (n & 15));
+}
 // Byte offset of v[key][n] (bf16) in the two SW128 boxes of the v tile.
 __device__ __forceinline__ uint32_t v_off(int key, int n) {
   return (uint32_t)((n >> 6) * 4096 + key * 128 + ((((n & 63) >> 3) ^ (key & 7)) << 4) +
@@ -178,13 +185,18 @@ __device__ __forceinline__ uint32_t v_off(int key, int n) {
 // round-to-nearest of the fp32 master. The state contraction takes S as bf16
 // operands rounded to nearest either way, so the output is bit-identical to
 // the fp32 pool's, while a unit reads 32 KiB of state instead of 64.
+// kS8 (attend only): S_pool is an fp8 (e4m3) copy of the states with one
+// scale per (slot, head), S = scale * code. The codes enter the state
+// contraction as f16 (exact), with phi(q) as f16 too, and the scale folds
+// into the merge coefficients, so a unit reads 16 KiB of state instead of 64;
+// the output is that of the attend on the dequantised state.
 // kS16 with kCommit (the dual-copy step): every slot has the fp32 master in
 // S_pool and its bf16 copy behind maps.S16. A request that does not commit
 // reads the copy; a committing request reads the master, adds its block,
 // and stores the new master and its round-to-nearest copy. The output bits
 // are those of the fp32-only step whenever the copies are in step with the
 // masters.
-template <bool kCommit, bool kSeq = false, bool kS16 = false>
+template <bool kCommit, bool kSeq = false, bool kS16 = false, bool kS8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attend_fast(const __grid_constant__ Maps maps, int batch, int H, int num_slots, float scale,
                   int merge, const int32_t* __restrict__ slot_idx,
@@ -192,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float* __restrict__ Z_pool, const float* __restrict__ gate,
                   __nv_bfloat16* __restrict__ o, unsigned* status) {
   static_assert(!(kS16 && kSeq), "the sequential mode keeps the fp32 state on chip");
+  static_assert(!(kS8 && (kCommit || kSeq || kS16)), "the fp8 copy is read by the attend only");
   constexpr bool kDual = kS16 && kCommit;  // the dual-copy step
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -332,9 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             cN = 0.f;
           }
         }
+        // (fp8 copy: the contraction used the codes, S = scale * code)
+        const float sc = kS8 ? __int_as_float(meta[8 + s]) : 1.f;
         fin[R] = cU;
-        fin[32 + R] = cN * isp;
-        fin[64 + R] = cN * ism;
+        fin[32 + R] = cN * isp * sc;
+        fin[64 + R] = cN * ism * sc;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&fin_ready[s]);
@@ -534,10 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     struct Window {
       int b, h, flags;  // flags: kUnitCommit, or -1 for a request the mask lost
       int slot;
+      float scale;      // fp8 copy: the unit's scale
     };
     // fills this lane's entry of window W and issues its slot load
     auto fill_window = [&](int W) -> Window {
-      Window wd{0, 0, 0, -1};
+      Window wd{0, 0, 0, -1, 1.f};
       const int i = 32 * W + lane;
       if (i >= n_local) return wd;
       const int p = first + i * stride;
@@ -558,6 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         wd.flags = -1;
       } else {
         wd.slot = slot_idx[wd.b];
+        if (kS8 && wd.slot >= 0 && wd.slot < num_slots)
+          wd.scale = maps.s8_scale[(size_t)wd.slot * (H / maps.kv_group) + wd.h / maps.kv_group];
       }
       return wd;
     };
@@ -576,6 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto unit_slot = [&](int i) {
       return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.slot : win_next.slot,
+                         i & 31);
+    };
+    auto unit_scale = [&](int i) {
+      return __shfl_sync(0xffffffffu, (i >> 5) == win_base ? win_cur.scale : win_next.scale,
                          i & 31);
     };
     auto issue_head = [&](int i) {
@@ -602,10 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int hs = h / maps.kv_group;  // the state's head
       const int Hs = H / maps.kv_group;
       const int flags = unit_flags(i), slot = unit_slot(i);
+      const float scale = kS8 ? unit_scale(i) : 1.f;
       uint8_t* st = smem + s * kStageStride;
       if (lane == 0) {
         meta[4 + s] = b;
         meta[6 + s] = h;
+        meta[8 + s] = __float_as_int(scale);
         if (flags < 0 || slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
@@ -619,7 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     &head_full[s]);
           mbar_arrive(&head_full[s]);
           const int srow = (slot * Hs + hs) * kF;
-          if (kS16 && !(kDual && (flags & kUnitCommit))) {
+          if (kS8) {
+            // the fp8 copy: one SWIZZLE_128B box of [128 F rows][128 codes]
+            mbar_arrive_expect_tx(&s_full[s], kSBytes / 4);
+            tma_load_2d(st + kOffS, &maps.S, 0, srow, &s_full[s]);
+          } else if (kS16 && !(kDual && (flags & kUnitCommit))) {
             // the bf16 copy (a dual-copy step's committing unit reads the master)
             mbar_arrive_expect_tx(&s_full[s], kSBytes / 2);
 #pragma unroll
@@ -642,9 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t unit = (size_t)slot * (H / G) + h / G;
       if (kDual && !(flags & kUnitCommit))
         prefetch_l2(maps.s16 + unit * kF * kD * 2, kF * kD * 2);
-      else
-        prefetch_l2(reinterpret_cast<const uint8_t*>(S_pool) + unit * kF * kD * (kS16 && !kDual ? 2 : 4),
-                    kF * kD * (kS16 && !kDual ? 2 : 4));
+      else {
+        // bytes per state value in S_pool: fp8 copy 1, bf16 copy 2, fp32 4
+        constexpr int kSv = kS8 ? 1 : (kS16 && !kDual) ? 2 : 4;
+        prefetch_l2(reinterpret_cast<const uint8_t*>(S_pool) + unit * kF * kD * kSv, kF * kD * kSv);
+      }
       prefetch_l2(Z_pool + unit * kF, kF * 4);
       // the request's block of q, k, v is one contiguous range of L rows of
       // all heads; the CTAs working on its heads at the same time each
@@ -910,10 +940,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t off0 = sw128(R0, c >> 3) + (c & 7) * 2;
         const uint32_t off1 = sw128(R1, c >> 3) + (c & 7) * 2;
-        st_shared_u32(sPhi + off0, pack_bf16(ep[0], ep[1]));
-        st_shared_u32(sPhi + off1, pack_bf16(ep[2], ep[3]));
-        st_shared_u32(sPhi + 4096 + off0, pack_bf16(em[0], em[1]));
-        st_shared_u32(sPhi + 4096 + off1, pack_bf16(em[2], em[3]));
+        // (the fp8 copy's contraction runs on f16 operands)
+        auto pk = [](float lo, float hi) { return kS8 ? pack_f16(lo, hi) : pack_bf16(lo, hi); };
+        st_shared_u32(sPhi + off0, pk(ep[0], ep[1]));
+        st_shared_u32(sPhi + off1, pk(ep[2], ep[3]));
+        st_shared_u32(sPhi + 4096 + off0, pk(em[0], em[1]));
+        st_shared_u32(sPhi + 4096 + off1, pk(em[2], em[3]));
       }
       float p[4], ss[2];
 #pragma unroll
@@ -1044,7 +1076,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int k0 = 16 * kk + 2 * t;
         uint32_t b00, b01, b10, b11;
-        if (kS16 && !cm) {
+        if (kS8) {
+          // codes S[k][col], S[k][col + 1] share a 16-bit word; regroup by
+          // column ({S[k][c], S[k + 1][c]}) and widen to f16 pairs
+          const uint32_t h0 = ld_shared_u16(sS + s8_off(k0, col));
+          const uint32_t h1 = ld_shared_u16(sS + s8_off(k0 + 1, col));
+          const uint32_t h8 = ld_shared_u16(sS + s8_off(k0 + 8, col));
+          const uint32_t h9 = ld_shared_u16(sS + s8_off(k0 + 9, col));
+          const uint32_t p01 = __byte_perm(h0, h1, 0x5140), p89 = __byte_perm(h8, h9, 0x5140);
+          b00 = e4m3x2_to_f16x2(p01);
+          b10 = e4m3x2_to_f16x2(p01 >> 16);
+          b01 = e4m3x2_to_f16x2(p89);
+          b11 = e4m3x2_to_f16x2(p89 >> 16);
+        } else if (kS16 && !cm) {
           // the same operands as below: S[k][col], S[k][col + 1] share a word
           const uint32_t w0 = ld_shared_u32(sS + s16_off(k0, col));
           const uint32_t w1 = ld_shared_u32(sS + s16_off(k0 + 1, col));
@@ -1067,8 +1111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float (&acc)[2][2][4] = kk < 4 ? acc_p : acc_m;
 #pragma unroll
         for (int m2 = 0; m2 < 2; ++m2) {
-          mma_bf16(acc[m2][0], a[m2], b00, b01);
-          mma_bf16(acc[m2][1], a[m2], b10, b11);
+          if (kS8) {
+            mma_f16(acc[m2][0], a[m2], b00, b01);
+            mma_f16(acc[m2][1], a[m2], b10, b11);
+          } else {
+            mma_bf16(acc[m2][0], a[m2], b00, b01);
+            mma_bf16(acc[m2][1], a[m2], b10, b11);
+          }
         }
       }
 #pragma unroll
@@ -1249,8 +1298,12 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
                                bool commit_all, bool sequential, bool state_bf16,
                                void* S16_pool = nullptr, int Hkv = -1,
-                               const void* Wk = nullptr) {
+                               const void* Wk = nullptr, const float* s8_scale = nullptr) {
   const bool dual = S16_pool != nullptr;
+  // the fp8 copy (with its per-(slot, head) scales) is read by the attend only
+  const bool fp8 = s8_scale != nullptr;
+  if (fp8 && (commit_mask || commit_all || sequential || dual || state_bf16))
+    return cudaErrorInvalidValue;
   if (Hkv <= 0) Hkv = s.H;
   // grouped heads in the attend-only kernels; a separate key map in the
   // sequential mode
@@ -1265,6 +1318,7 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
   maps.kv_group = s.H / Hkv;
   maps.sep_wk = sep_wk ? 1 : 0;
   maps.s16 = static_cast<const uint8_t*>(S16_pool);
+  maps.s8_scale = s8_scale;
   maps.rows_per_req = rows_per_req;
   maps.wait_limit = wait_limit_cycles();
   maps.row_base = row_base;
@@ -1274,12 +1328,16 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
   maps.qkv[2] = static_cast<const uint8_t*>(v);
   maps.w = static_cast<const uint8_t*>(W);
   {
+    // bytes per value: fp32 master 4, bf16 copy 2, fp8 copy 1; a box row is
+    // 128 bytes (SWIZZLE_128B) of 128 F rows
+    const int vb = fp8 ? 1 : state_bf16 ? 2 : 4;
     const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)num_slots * Hkv * kF};
-    const uint64_t strides[1] = {(uint64_t)kD * (state_bf16 ? 2 : 4)};
-    const uint32_t box[2] = {state_bf16 ? 64u : 32u, 128};
-    if (!encode_tmap(&maps.S,
-                     state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                     2, S_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t strides[1] = {(uint64_t)kD * vb};
+    const uint32_t box[2] = {(uint32_t)(128 / vb), 128};
+    const CUtensorMapDataType dt = fp8          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : state_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!encode_tmap(&maps.S, dt, 2, S_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     maps.S16 = maps.S;  // unused unless dual
   }
@@ -1318,6 +1376,7 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
       return cudaErrorInvalidValue;
   }
   auto* kernel = dual         ? k_attend_fast<true, false, true>
+                 : fp8        ? k_attend_fast<false, false, false, true>
                  : state_bf16 ? k_attend_fast<false, false, true>
                  : sequential ? k_attend_fast<true, true>
                  : (commit_mask || commit_all) ? k_attend_fast<true> : k_attend_fast<false>;
@@ -1364,6 +1423,17 @@ cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slo
                                    cudaStream_t st) {
   return launch_attend_impl(s, batch, slot_idx, q, k, v, S16_pool, Z_pool, num_slots, W, gate,
                             nullptr, o, status, st, s.L, 0, false, false, true);
+}
+
+cudaError_t launch_attend_fast_s8(const Shape& s, int batch, const int32_t* slot_idx,
+                                  const void* q, const void* k, const void* v,
+                                  const void* S8_pool, const float* scale_pool,
+                                  const float* Z_pool, int num_slots, const void* W,
+                                  const float* gate, void* o, unsigned* status,
+                                  cudaStream_t st) {
+  return launch_attend_impl(s, batch, slot_idx, q, k, v, S8_pool, Z_pool, num_slots, W, gate,
+                            nullptr, o, status, st, s.L, 0, false, false, false, nullptr, -1,
+                            nullptr, scale_pool);
 }
 
 }  // namespace hb

@@ -1,6 +1,7 @@
-// A bf16 copy of the state pool for the attend's read (hb_state_to_bf16,
-// hb_block_attend_s16). Internal to libhb.so; the public signatures are in
-// include/hb.h.
+// Reduced-precision copies of the state pool for the attend's read: bf16
+// (hb_state_to_bf16, hb_block_attend_s16) and fp8 with a scale per (slot,
+// head) (hb_state_to_fp8, hb_block_attend_s8). Internal to libhb.so; the
+// public signatures are in include/hb.h.
 //
 // The attend's state contraction takes S as bf16 operands rounded to nearest
 // from the fp32 state, so a copy holding exactly those rounded values gives
@@ -24,6 +25,21 @@ cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slo
                                    const void* S16_pool, const float* Z_pool, int num_slots,
                                    const void* W, const float* gate, void* o, unsigned* status,
                                    cudaStream_t st);
+
+// The fp8 (e4m3) copy with one scale per (slot, head): scale = max|S| / 448,
+// code = e4m3(S / scale) for the listed slots; a slot outside
+// [0, num_slots) is skipped and flagged (hb_state_copy.cu).
+cudaError_t launch_state_to_fp8(const Shape& s, int batch, const int32_t* slot_idx,
+                                const float* S_pool, void* S8_pool, float* scale_pool,
+                                int num_slots, unsigned* status, cudaStream_t st);
+
+// hb_block_attend on the fp8 copy (production shape only; hb_attend_fast.cu).
+cudaError_t launch_attend_fast_s8(const Shape& s, int batch, const int32_t* slot_idx,
+                                  const void* q, const void* k, const void* v,
+                                  const void* S8_pool, const float* scale_pool,
+                                  const float* Z_pool, int num_slots, const void* W,
+                                  const float* gate, void* o, unsigned* status,
+                                  cudaStream_t st);
 
 // hb_block_attend_commit with the bf16 copies beside the fp32 masters:
 // requests that do not commit read their copy, committing ones read the

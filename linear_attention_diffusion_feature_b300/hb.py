@@ -184,6 +184,53 @@ def hb_block_attend_s16(cfg: Config, slot_idx, q, k, v, S16_pool, Z_pool, W, gat
     return o
 
 
+def hb_state_to_fp8(cfg: Config, slot_idx, S_pool, S8_pool, scale_pool, stream=None) -> None:
+    """Writes the fp8 (e4m3) copy of the listed slots' S, one scale per
+    (slot, head): scale = max|S| / 448, code = e4m3(S / scale)."""
+    B = slot_idx.shape[0]
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    if S_pool.dim() != 4:
+        raise ValueError("S_pool: expected [num_slots, H, F, d]")
+    num_slots = S_pool.shape[0]
+    shape = (num_slots, cfg.num_heads, cfg.F, cfg.head_dim)
+    _check(S_pool, "S_pool", torch.float32, shape)
+    _check(S8_pool, "S8_pool", torch.uint8, shape)
+    _check(scale_pool, "scale_pool", torch.float32, (num_slots, cfg.num_heads))
+    lib = _lib.load()
+    _raise(lib.hb_state_to_fp8(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(S_pool),
+                               _ptr(S8_pool), _ptr(scale_pool), num_slots, _stream(stream)),
+           "hb_state_to_fp8")
+
+
+def hb_block_attend_s8(cfg: Config, slot_idx, q, k, v, S8_pool, scale_pool, Z_pool, W,
+                       gate_logits, o=None, stream=None) -> torch.Tensor:
+    """hb_block_attend on the fp8 copy of S (a quarter of the state bytes;
+    the output is the attend on the dequantised state); Z_pool is the fp32
+    master's."""
+    B = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    _check(slot_idx, "slot_idx", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (B, L, H, d))
+    if S8_pool.dim() != 4:
+        raise ValueError("S8_pool: expected [num_slots, H, F, d]")
+    num_slots = S8_pool.shape[0]
+    _check(S8_pool, "S8_pool", torch.uint8, (num_slots, H, cfg.F, d))
+    _check(scale_pool, "scale_pool", torch.float32, (num_slots, H))
+    _check(Z_pool, "Z_pool", torch.float32, (num_slots, H, cfg.F))
+    _check(W, "W", cfg.torch_dtype, (H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (H,))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (B, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_s8(ctypes.byref(cfg.c()), B, _ptr(slot_idx), _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(S8_pool), _ptr(scale_pool), _ptr(Z_pool),
+                                  num_slots, _ptr(W), _ptr(gate_logits), _ptr(o),
+                                  _stream(stream)), "hb_block_attend_s8")
+    return o
+
+
 def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits,
                            commit, o=None, stream=None) -> torch.Tensor:
     """hb_block_attend, then hb_commit_block of the same block for the requests
