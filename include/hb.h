@@ -168,7 +168,7 @@ hb_status hb_state_to_bf16(const hb_config* cfg, int32_t batch,
  * S as bf16 operands rounded to nearest in either case, so the output is
  * bit-identical to hb_block_attend's on the fp32 states the copy was made
  * from, while each (request, head) reads 32 KiB of state instead of 64.
- * Production shape only (bf16, d = 128, f = 64, L = 32); any other shape
+ * Production shape only (bf16, d = 128, f = 64, L = 32 or 16); any other shape
  * returns HB_ERR_UNSUPPORTED_SHAPE.
  *   S16_pool  [num_slots, H, F, d] bf16, read only
  *   Z_pool    [num_slots, H, F] fp32, read only (the master's Z)
@@ -263,7 +263,7 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
  * stays in step without a separate hb_state_to_bf16 pass. While every listed
  * slot's copy is the round-to-nearest of its master on entry, o, S_pool and
  * Z_pool come out bit-identical to hb_block_attend_commit's on the masters.
- * Production shape only (bf16, d = 128, f = 64, L = 32); any other shape
+ * Production shape only (bf16, d = 128, f = 64, L = 32 or 16); any other shape
  * returns HB_ERR_UNSUPPORTED_SHAPE.
  *   S_pool    [num_slots, H, F, d] fp32 masters: read for committing
  *             requests and written for them
