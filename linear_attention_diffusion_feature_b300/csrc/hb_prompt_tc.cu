@@ -57,18 +57,19 @@ constexpr int kOffXP = kOffXm + 2048;    // [4][128]: the matching partial sums
 constexpr int kOffZ = kOffXP + 2048;     // [128]: Z
 constexpr int kOffZq = kOffZ + 512;      // [4][128]: the segment's column sums of phi(K)
 constexpr int kOffBar = kOffZq + 2048;
-constexpr int kNumBars = 11;
+constexpr int kNumBars = 12;
 constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
-enum { kBarW = 0, kBarQK, kBarV0, kBarV1, kBarU, kBarPhi, kBarL, kBarC, kBarO, kBarE, kBarDone };
+enum { kBarW = 0, kBarQK, kBarV0, kBarV1, kBarU, kBarPhi, kBarL, kBarC, kBarO, kBarE, kBarSc,
+       kBarDone };
 
 // tensor-memory columns (512 allocated; lane = row of every accumulator)
 constexpr uint32_t kColM = 0;    // the state S [F][d], fp32, for the whole prompt
-constexpr uint32_t kColU = 128;  // U_q (64) and U_k (64); later O2 (128)
+constexpr uint32_t kColU = 128;  // O2 (128)
 constexpr uint32_t kColS = 256;  // block scores; later O1
-constexpr uint32_t kColA = 384;  // phi(Q) phi(K)^T
+constexpr uint32_t kColA = 384;  // U_q (64) and U_k (64); later phi(Q) phi(K)^T
 
 struct Maps {
   CUtensorMap q, k, v;  // [B*T rows][H][d] bf16, box {64, 1, 128}
@@ -154,6 +155,7 @@ __global__ void __maxnreg__(96)
     mbar_init(&bar[kBarC], kEpiWarps);
     mbar_init(&bar[kBarO], 1);
     mbar_init(&bar[kBarE], kEpiWarps);
+    mbar_init(&bar[kBarSc], 1);
     mbar_init(&bar[kBarDone], 1);
     fence_mbar_init();
   }
@@ -246,24 +248,34 @@ __global__ void __maxnreg__(96)
       constexpr uint32_t idKM = umma_idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
       constexpr uint32_t idMM = umma_idesc_bf16(128, 128, 1, 1);  // both MN-major
       const long long lim = a.wait_limit;
+      // U_q = Q W and U_k = K W of segment s, into the A columns
+      auto issue_u = [&]() {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tbase + kColA, desc_k(sQ, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tbase + kColA + 64, desc_k(sK, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
+        umma_commit(&bar[kBarU]);
+      };
+      // Segment s's U is issued as soon as its Q, K have landed and the A
+      // columns are free (segment s - 1's C is written), so it runs while
+      // the epilogue forms s - 1's outputs; its scores Sc wait for those
+      // outputs to be read (the S columns) and run while the epilogue forms
+      // s's feature maps, which overwrite Q and K only after Sc has read them.
       bool ok = mbar_wait(&bar[kBarW], 0, lim);
+      if (ok) ok = mbar_wait(&bar[kBarQK], 0, lim);
+      if (ok) issue_u();
       for (int s = 0; ok && s < n_seg; ++s) {
         const uint32_t vb = sV + (s & 1) * 32768;
-        ok = mbar_wait(&bar[kBarQK], s & 1, lim);
-        if (ok && s > 0) ok = mbar_wait(&bar[kBarE], (s - 1) & 1, lim);  // O1, O2 of s - 1 read
-        if (!ok) break;
+        if (s > 0 && !(ok = mbar_wait(&bar[kBarE], (s - 1) & 1, lim))) break;  // O1, O2 of s - 1 read
         tc_fence_after();
-        // U_q = Q W, U_k = K W, Sc = Q K^T
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tbase + kColU, desc_k(sQ, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tbase + kColU + 64, desc_k(sK, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
+        // Sc = Q K^T
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColS, desc_k(sQ, ks), desc_k(sK, ks), idKK, ks > 0 ? 1u : 0u);
-        umma_commit(&bar[kBarU]);
+        umma_commit(&bar[kBarSc]);
         // phi(Q), phi(K) written by the epilogue; V landed
         ok = mbar_wait(&bar[kBarPhi], s & 1, lim);
         if (ok) ok = mbar_wait(&bar[kBarV0 + (s & 1)], (s >> 1) & 1, lim);
@@ -289,6 +301,11 @@ __global__ void __maxnreg__(96)
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColS, desc_k(sKlo, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarO]);
+        // the next segment's U (A has been read; its Q, K load after L)
+        if (s + 1 < n_seg) {
+          if (!(ok = mbar_wait(&bar[kBarQK], (s + 1) & 1, lim))) break;
+          issue_u();
+        }
       }
       if (!ok) atomicOr(a.status, kStatusTimeout);
       // every MMA issued has completed before tensor memory is freed
@@ -397,9 +414,12 @@ __global__ void __maxnreg__(96)
         named_bar_sync(1, 32 * kEpiWarps);
       };
       // queries: phi(Q) (bf16) over Q, and phi(q) . Z of this thread's columns
-      tmem_ld16(tbase + lane_bits + kColU + 16 * sub, u);
+      tmem_ld16(tbase + lane_bits + kColA + 16 * sub, u);
       tmem_wait_ld();
       softmaxes();
+      // Q and K are overwritten below: the scores Sc must have read them
+      if (ok) ok = mbar_wait(&bar[kBarSc], s & 1, a.wait_limit);
+      tc_fence_after();
       {
         float den = 0.f;
 #pragma unroll
@@ -419,7 +439,7 @@ __global__ void __maxnreg__(96)
       }
       // keys: phi(K) as hi + lo over K and in the lo buffer (rows past the
       // prompt are zero, so they add nothing)
-      tmem_ld16(tbase + lane_bits + kColU + 64 + 16 * sub, u);
+      tmem_ld16(tbase + lane_bits + kColA + 64 + 16 * sub, u);
       tmem_wait_ld();
       softmaxes();
       if (!live) {
