@@ -57,13 +57,13 @@ constexpr int kOffXP = kOffXm + 2048;    // [4][128]: the matching partial sums
 constexpr int kOffZ = kOffXP + 2048;     // [128]: Z
 constexpr int kOffZq = kOffZ + 512;      // [4][128]: the segment's column sums of phi(K)
 constexpr int kOffBar = kOffZq + 2048;
-constexpr int kNumBars = 12;
+constexpr int kNumBars = 13;
 constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
 enum { kBarW = 0, kBarQK, kBarV0, kBarV1, kBarU, kBarPhi, kBarL, kBarC, kBarO, kBarE, kBarSc,
-       kBarDone };
+       kBarUpd, kBarDone };
 
 // tensor-memory columns (512 allocated; lane = row of every accumulator)
 constexpr uint32_t kColM = 0;    // the state S [F][d], fp32, for the whole prompt
@@ -156,6 +156,7 @@ __global__ void __maxnreg__(96)
     mbar_init(&bar[kBarO], 1);
     mbar_init(&bar[kBarE], kEpiWarps);
     mbar_init(&bar[kBarSc], 1);
+    mbar_init(&bar[kBarUpd], 1);
     mbar_init(&bar[kBarDone], 1);
     fence_mbar_init();
   }
@@ -218,9 +219,9 @@ __global__ void __maxnreg__(96)
       }
       for (int s = 1; s < n_seg; ++s) {
         // phi(Q) and phi(K) of the segment before, over its Q and K, have
-        // been read once its A, O2 and state-update MMAs are done; its V
-        // buffer once O1 is done too
-        if (!mbar_wait(&bar[kBarL], (s - 1) & 1, a.wait_limit)) {
+        // been read once its A, O2 and state-update MMAs are done (the
+        // update is the last of them); its V buffer once O1 is done too
+        if (!mbar_wait(&bar[kBarUpd], (s - 1) & 1, a.wait_limit)) {
           atomicOr(a.status, kStatusTimeout);
           break;
         }
@@ -281,25 +282,28 @@ __global__ void __maxnreg__(96)
         if (ok) ok = mbar_wait(&bar[kBarV0 + (s & 1)], (s >> 1) & 1, lim);
         if (!ok) break;
         tc_fence_after();
-        // A = phi(Q) phi(K)^T, O2 = phi(Q) S_start, S += phi(K)^T V (hi + lo)
+        // A = phi(Q) phi(K)^T and O2 = phi(Q) S_start (the epilogue's
+        // merge needs them); then S += phi(K)^T V (hi + lo), which runs
+        // while the epilogue forms C
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColA, desc_k(sQ, ks), desc_k(sK, ks), idKK, ks > 0 ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColU, desc_k(sQ, ks), desc_mn(sS16, ks), idKM, ks > 0 ? 1u : 0u);
+        umma_commit(&bar[kBarL]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           umma_bf16(tbase + kColM, desc_mn(sK, ks), desc_mn(vb, ks), idMM, 1u);
           umma_bf16(tbase + kColM, desc_mn(sKlo, ks), desc_mn(vb, ks), idMM, 1u);
         }
-        umma_commit(&bar[kBarL]);
-        // C written by the epilogue (over phi(Q)): O1 = C V
+        umma_commit(&bar[kBarUpd]);
+        // C written by the epilogue (over the state copy O2 has read): O1 = C V
         if (!(ok = mbar_wait(&bar[kBarC], s & 1, lim))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tbase + kColS, desc_k(sKlo, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
+          umma_bf16(tbase + kColS, desc_k(sS16, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarO]);
         // the next segment's U (A has been read; its Q, K load after L)
         if (s + 1 < n_seg) {
@@ -484,29 +488,9 @@ __global__ void __maxnreg__(96)
       if (lane == 0) mbar_arrive(&bar[kBarPhi]);
 
       // ---- E3: block softmax, weights of the earlier blocks, merge
-      //      coefficients, C; the state for the next segment
+      //      coefficients, C (over the state copy, which O2 has read)
       if (ok) ok = mbar_wait(&bar[kBarL], s & 1, a.wait_limit);
       tc_fence_after();
-      // the state after this segment: its bf16 copy for the next segment's
-      // read, or, after the last segment, the fp32 state and Z to the pool
-      {
-        float st[32];
-        tmem_ld32(tbase + lane_bits + kColM + 32 * sub, st);
-        tmem_wait_ld();
-        if (s + 1 < n_seg) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), pack_bf16(st[8 * q4], st[8 * q4 + 1]),
-                         pack_bf16(st[8 * q4 + 2], st[8 * q4 + 3]),
-                         pack_bf16(st[8 * q4 + 4], st[8 * q4 + 5]),
-                         pack_bf16(st[8 * q4 + 6], st[8 * q4 + 7]));
-        } else if (ok && commits) {
-          float4* dst = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD + r * kD + 32 * sub);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
-        }
-      }
       // This thread's 32 keys (32 sub .. 32 sub + 31 of the segment): key j
       // is in block kb = (32 sub + j) / kBL; it is the row's own block
       // (block softmax) when kb == r / kBL, an earlier block (linear weight
@@ -633,7 +617,7 @@ __global__ void __maxnreg__(96)
             const int j = 8 * q4 + 2 * p;
             w4[p] = (w_own || w_early) ? pack_bf16(c * v32[j], c * v32[j + 1]) : 0u;
           }
-          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
+          st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), w4[0], w4[1], w4[2], w4[3]);
         }
       } else {
         const float cu = cU * own_scale;
@@ -644,7 +628,7 @@ __global__ void __maxnreg__(96)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = 8 * q4;
-          st_shared_v4(sKlo + tile_off(r, 4 * sub + q4), pack_bf16(cj[j], cj[j + 1]),
+          st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), pack_bf16(cj[j], cj[j + 1]),
                        pack_bf16(cj[j + 2], cj[j + 3]), pack_bf16(cj[j + 4], cj[j + 5]),
                        pack_bf16(cj[j + 6], cj[j + 7]));
         }
@@ -654,9 +638,32 @@ __global__ void __maxnreg__(96)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarC]);
 
-      // ---- E4: o = O1 + cN O2 for this thread's 32 columns of row r
+      // ---- E4: the state after this segment (its S update is done), then
+      //      o = O1 + cN O2 for this thread's 32 columns of row r
       if (ok) ok = mbar_wait(&bar[kBarO], s & 1, a.wait_limit);
+      if (ok) ok = mbar_wait(&bar[kBarUpd], s & 1, a.wait_limit);
       tc_fence_after();
+      // its bf16 copy for the next segment's O2 (over C, which O1 has
+      // read), or, after the last segment, the fp32 state to the pool
+      {
+        float st[32];
+        tmem_ld32(tbase + lane_bits + kColM + 32 * sub, st);
+        tmem_wait_ld();
+        if (s + 1 < n_seg) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), pack_bf16(st[8 * q4], st[8 * q4 + 1]),
+                         pack_bf16(st[8 * q4 + 2], st[8 * q4 + 3]),
+                         pack_bf16(st[8 * q4 + 4], st[8 * q4 + 5]),
+                         pack_bf16(st[8 * q4 + 6], st[8 * q4 + 7]));
+        } else if (ok && commits) {
+          float4* dst = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD + r * kD + 32 * sub);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
+        }
+      }
+
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float o1[16], o2[16];
