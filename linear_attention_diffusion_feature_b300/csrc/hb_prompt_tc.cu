@@ -57,13 +57,13 @@ constexpr int kOffXP = kOffXm + 2048;    // [4][128]: the matching partial sums
 constexpr int kOffZ = kOffXP + 2048;     // [128]: Z
 constexpr int kOffZq = kOffZ + 512;      // [4][128]: the segment's column sums of phi(K)
 constexpr int kOffBar = kOffZq + 2048;
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 16;
 constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory over the sm_100 per-block limit");
 
-enum { kBarW = 0, kBarQK, kBarV0, kBarV1, kBarU, kBarPhi, kBarL, kBarC, kBarO, kBarE, kBarSc,
-       kBarUpd, kBarDone };
+enum { kBarW = 0, kBarQ, kBarK, kBarV0, kBarV1, kBarUq, kBarUk, kBarPhi, kBarL, kBarC, kBarO,
+       kBarE, kBarSc, kBarUpd, kBarPhiQ, kBarDone };
 
 // tensor-memory columns (512 allocated; lane = row of every accumulator)
 constexpr uint32_t kColM = 0;    // the state S [F][d], fp32, for the whole prompt
@@ -146,10 +146,12 @@ __global__ void __maxnreg__(96)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarW], 1);
-    mbar_init(&bar[kBarQK], 1);
+    mbar_init(&bar[kBarQ], 1);
+    mbar_init(&bar[kBarK], 1);
     mbar_init(&bar[kBarV0], 1);
     mbar_init(&bar[kBarV1], 1);
-    mbar_init(&bar[kBarU], 1);
+    mbar_init(&bar[kBarUq], 1);
+    mbar_init(&bar[kBarUk], 1);
     mbar_init(&bar[kBarPhi], kEpiWarps);
     mbar_init(&bar[kBarL], 1);
     mbar_init(&bar[kBarC], kEpiWarps);
@@ -157,6 +159,7 @@ __global__ void __maxnreg__(96)
     mbar_init(&bar[kBarE], kEpiWarps);
     mbar_init(&bar[kBarSc], 1);
     mbar_init(&bar[kBarUpd], 1);
+    mbar_init(&bar[kBarPhiQ], kEpiWarps);
     mbar_init(&bar[kBarDone], 1);
     fence_mbar_init();
   }
@@ -190,16 +193,22 @@ __global__ void __maxnreg__(96)
 #pragma unroll
         for (int j = 0; j < 3; ++j) prefetch_l2(a.qkv[j] + off, (uint32_t)bytes);
       };
-      int n_qk = 0, n_v0 = 0, n_v1 = 0;  // loads issued, for the final drain
-      auto load_qk = [&](int s) {
+      int n_q = 0, n_k = 0, n_v0 = 0, n_v1 = 0;  // loads issued, for the final drain
+      auto load_q = [&](int s) {
         const int row = (int)(base_row + (int64_t)s * kSeg);
-        ++n_qk;
-        mbar_arrive_expect_tx(&bar[kBarQK], 65536);
+        ++n_q;
+        mbar_arrive_expect_tx(&bar[kBarQ], 32768);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          tma_load_3d(smem + kOffQ + j * 16384, &maps.q, 64 * j, h, row, &bar[kBarQK]);
-          tma_load_3d(smem + kOffK + j * 16384, &maps.k, 64 * j, h, row, &bar[kBarQK]);
-        }
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(smem + kOffQ + j * 16384, &maps.q, 64 * j, h, row, &bar[kBarQ]);
+      };
+      auto load_k = [&](int s) {
+        const int row = (int)(base_row + (int64_t)s * kSeg);
+        ++n_k;
+        mbar_arrive_expect_tx(&bar[kBarK], 32768);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(smem + kOffK + j * 16384, &maps.k, 64 * j, h, row, &bar[kBarK]);
       };
       auto load_v = [&](int s) {
         const int row = (int)(base_row + (int64_t)s * kSeg);
@@ -211,21 +220,27 @@ __global__ void __maxnreg__(96)
           tma_load_3d(smem + kOffV + (s & 1) * 32768 + j * 16384, &maps.v, 64 * j, h, row, vb);
       };
       if (n_seg > 0) {
-        load_qk(0);
+        load_q(0);
+        load_k(0);
         load_v(0);
         if (n_seg > 1) load_v(1);
         l2(1);
         l2(2);
       }
       for (int s = 1; s < n_seg; ++s) {
-        // phi(Q) and phi(K) of the segment before, over its Q and K, have
-        // been read once its A, O2 and state-update MMAs are done (the
-        // update is the last of them); its V buffer once O1 is done too
+        // phi(Q) of the segment before, over its Q, has been read once its
+        // A and O2 are done; phi(K) once its state update is done too; its
+        // V buffer once O1 is done
+        if (!mbar_wait(&bar[kBarL], (s - 1) & 1, a.wait_limit)) {
+          atomicOr(a.status, kStatusTimeout);
+          break;
+        }
+        load_q(s);
         if (!mbar_wait(&bar[kBarUpd], (s - 1) & 1, a.wait_limit)) {
           atomicOr(a.status, kStatusTimeout);
           break;
         }
-        load_qk(s);
+        load_k(s);
         l2(s + 2);
         if (s + 1 < n_seg) {
           if (!mbar_wait(&bar[kBarO], (s - 1) & 1, a.wait_limit)) {
@@ -237,7 +252,8 @@ __global__ void __maxnreg__(96)
       }
       // no copy may land in the shared memory of an exited CTA: wait for the
       // last one issued on each barrier (immediate when already consumed)
-      if (n_qk > 0) mbar_wait(&bar[kBarQK], (n_qk - 1) & 1);
+      if (n_q > 0) mbar_wait(&bar[kBarQ], (n_q - 1) & 1);
+      if (n_k > 0) mbar_wait(&bar[kBarK], (n_k - 1) & 1);
       if (n_v0 > 0) mbar_wait(&bar[kBarV0], (n_v0 - 1) & 1);
       if (n_v1 > 0) mbar_wait(&bar[kBarV1], (n_v1 - 1) & 1);
     }
@@ -249,25 +265,32 @@ __global__ void __maxnreg__(96)
       constexpr uint32_t idKM = umma_idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
       constexpr uint32_t idMM = umma_idesc_bf16(128, 128, 1, 1);  // both MN-major
       const long long lim = a.wait_limit;
-      // U_q = Q W and U_k = K W of segment s, into the A columns
-      auto issue_u = [&]() {
+      // U_q = Q W and U_k = K W of segment s, into the A columns, each
+      // issued once its operand has landed
+      auto issue_u = [&](int s) -> bool {
+        if (!mbar_wait(&bar[kBarQ], s & 1, lim)) return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColA, desc_k(sQ, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
+        umma_commit(&bar[kBarUq]);
+        if (!mbar_wait(&bar[kBarK], s & 1, lim)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColA + 64, desc_k(sK, ks), desc_mn(sW, ks), idU, ks > 0 ? 1u : 0u);
-        umma_commit(&bar[kBarU]);
+        umma_commit(&bar[kBarUk]);
+        return true;
       };
-      // Segment s's U is issued as soon as its Q, K have landed and the A
-      // columns are free (segment s - 1's C is written), so it runs while
-      // the epilogue forms s - 1's outputs; its scores Sc wait for those
-      // outputs to be read (the S columns) and run while the epilogue forms
-      // s's feature maps, which overwrite Q and K only after Sc has read them.
+      // Segment s's U_q is issued once the A columns are free (segment
+      // s - 1's C is written) and its Q has landed (loaded once s - 1's A and
+      // O2 have read phi(Q)); U_k once its K has landed (after s - 1's state
+      // update). Both run while the epilogue forms s - 1's outputs; the
+      // scores Sc wait for those outputs to be read (the S columns) and run
+      // while the epilogue forms s's feature maps, which overwrite Q and K
+      // only after Sc has read them.
       bool ok = mbar_wait(&bar[kBarW], 0, lim);
-      if (ok) ok = mbar_wait(&bar[kBarQK], 0, lim);
-      if (ok) issue_u();
+      if (ok) ok = issue_u(0);
       for (int s = 0; ok && s < n_seg; ++s) {
         const uint32_t vb = sV + (s & 1) * 32768;
         if (s > 0 && !(ok = mbar_wait(&bar[kBarE], (s - 1) & 1, lim))) break;  // O1, O2 of s - 1 read
@@ -277,20 +300,23 @@ __global__ void __maxnreg__(96)
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColS, desc_k(sQ, ks), desc_k(sK, ks), idKK, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarSc]);
-        // phi(Q), phi(K) written by the epilogue; V landed
+        // phi(Q) written by the epilogue: O2 = phi(Q) S_start runs while it
+        // forms phi(K)
+        if (!(ok = mbar_wait(&bar[kBarPhiQ], s & 1, lim))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tbase + kColU, desc_k(sQ, ks), desc_mn(sS16, ks), idKM, ks > 0 ? 1u : 0u);
+        // phi(K) written; V landed
         ok = mbar_wait(&bar[kBarPhi], s & 1, lim);
         if (ok) ok = mbar_wait(&bar[kBarV0 + (s & 1)], (s >> 1) & 1, lim);
         if (!ok) break;
         tc_fence_after();
-        // A = phi(Q) phi(K)^T and O2 = phi(Q) S_start (the epilogue's
-        // merge needs them); then S += phi(K)^T V (hi + lo), which runs
-        // while the epilogue forms C
+        // A = phi(Q) phi(K)^T (with O2, what the epilogue's merge needs);
+        // then S += phi(K)^T V (hi + lo), which runs while it forms C
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(tbase + kColA, desc_k(sQ, ks), desc_k(sK, ks), idKK, ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tbase + kColU, desc_k(sQ, ks), desc_mn(sS16, ks), idKM, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarL]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -306,10 +332,7 @@ __global__ void __maxnreg__(96)
           umma_bf16(tbase + kColS, desc_k(sS16, ks), desc_mn(vb, ks), idKM, ks > 0 ? 1u : 0u);
         umma_commit(&bar[kBarO]);
         // the next segment's U (A has been read; its Q, K load after L)
-        if (s + 1 < n_seg) {
-          if (!(ok = mbar_wait(&bar[kBarQK], (s + 1) & 1, lim))) break;
-          issue_u();
-        }
+        if (s + 1 < n_seg && !(ok = issue_u(s + 1))) break;
       }
       if (!ok) atomicOr(a.status, kStatusTimeout);
       // every MMA issued has completed before tensor memory is freed
@@ -366,56 +389,51 @@ __global__ void __maxnreg__(96)
       const int valid = valid64 < kSeg ? (int)valid64 : kSeg;
       const bool live = r < valid;
       // ---- E1: the feature maps of the segment's queries and keys
-      if (ok) ok = mbar_wait(&bar[kBarU], s & 1, a.wait_limit);
+      if (ok) ok = mbar_wait(&bar[kBarUq], s & 1, a.wait_limit);
       tc_fence_after();
       float u[16];
       // phi(x) = [softmax(u), softmax(-u)] over the 64 columns of u, shared
       // by the four threads of the row: row max, min and sums exchanged
       float ph[32];
       auto softmaxes = [&]() {
-        // each thread's 16 columns with its own max and min; one exchange
-        // merges the four threads' (max, sum) and (min, sum) pairs exactly
+        // the row's max and min first (its four threads' partial ones
+        // exchanged), so every exponential is taken against the row's own
+        // bound and the sums need no rescaling; then the sums are exchanged
         float mx = -FLT_MAX, mn = FLT_MAX;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          mx = fmaxf(mx, u[j]);
-          mn = fminf(mn, u[j]);
-        }
-        float sp = 0.f, sm = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          ph[j] = ex2_approx((u[j] - mx) * kLog2e);
-          ph[16 + j] = ex2_approx((mn - u[j]) * kLog2e);
-          sp += ph[j];
-          sm += ph[16 + j];
+        for (int j = 0; j < 16; j += 2) {
+          mx = fmax3(mx, u[j], u[j + 1]);
+          mn = fmin3(mn, u[j], u[j + 1]);
         }
         xa[sub * 128 + r] = mx;
         xb[sub * 128 + r] = mn;
+        named_bar_sync(1, 32 * kEpiWarps);
+        mx = fmax3(fmax3(mx, xa[r], xa[128 + r]), xa[256 + r], xa[384 + r]);
+        mn = fmin3(fmin3(mn, xb[r], xb[128 + r]), xb[256 + r], xb[384 + r]);
+        const float opx = -mx * kLog2e, omn = mn * kLog2e;
+        float sp = 0.f, sm = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          ph[j] = ex2_approx(fmaf(u[j], kLog2e, opx));
+          ph[16 + j] = ex2_approx(fmaf(u[j], -kLog2e, omn));
+          sp += ph[j];
+          sm += ph[16 + j];
+        }
         xc[sub * 128 + r] = sp;
         xd[sub * 128 + r] = sm;
         named_bar_sync(1, 32 * kEpiWarps);
-        float M = mx, N = mn;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          M = fmaxf(M, xa[q * 128 + r]);
-          N = fminf(N, xb[q * 128 + r]);
-        }
-        float tp = 0.f, tm = 0.f;  // row totals e^{u - M}, e^{N - u} (each >= 1)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tp = fmaf(xc[q * 128 + r], ex2_approx((xa[q * 128 + r] - M) * kLog2e), tp);
-          tm = fmaf(xd[q * 128 + r], ex2_approx((N - xb[q * 128 + r]) * kLog2e), tm);
-        }
-        const float cp = ex2_approx((mx - M) * kLog2e) * rcp_approx(tp);
-        const float cm = ex2_approx((N - mn) * kLog2e) * rcp_approx(tm);
+        // row totals of e^{u - max} and e^{min - u} (each >= 1), in a fixed order
+        const float tp = (xc[r] + xc[128 + r]) + (xc[256 + r] + xc[384 + r]);
+        const float tm = (xd[r] + xd[128 + r]) + (xd[256 + r] + xd[384 + r]);
+        const float cp = rcp_approx(tp), cm = rcp_approx(tm);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           ph[j] *= cp;
           ph[16 + j] *= cm;
         }
-        // the exchange slots are rewritten by the next call only after every
-        // thread has passed this barrier
-        named_bar_sync(1, 32 * kEpiWarps);
+        // slot reuse: xa and xb are written again only after the second
+        // barrier (every thread has read them before it), xc and xd only
+        // after the next call's first barrier (likewise)
       };
       // queries: phi(Q) (bf16) over Q, and phi(q) . Z of this thread's columns
       tmem_ld16(tbase + lane_bits + kColA + 16 * sub, u);
@@ -426,9 +444,17 @@ __global__ void __maxnreg__(96)
       tc_fence_after();
       {
         float den = 0.f;
+        const float4* zp = reinterpret_cast<const float4*>(Zs + 16 * sub);
+        const float4* zm = reinterpret_cast<const float4*>(Zs + kFH + 16 * sub);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          den = fmaf(ph[j], Zs[16 * sub + j], fmaf(ph[16 + j], Zs[kFH + 16 * sub + j], den));
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 a4 = zp[j4], b4 = zm[j4];
+          const int j = 4 * j4;
+          den = fmaf(ph[j], a4.x, fmaf(ph[16 + j], b4.x, den));
+          den = fmaf(ph[j + 1], a4.y, fmaf(ph[17 + j], b4.y, den));
+          den = fmaf(ph[j + 2], a4.z, fmaf(ph[18 + j], b4.z, den));
+          den = fmaf(ph[j + 3], a4.w, fmaf(ph[19 + j], b4.w, den));
+        }
         xden[sub * 128 + r] = den;
 #pragma unroll
         for (int half = 0; half < 2; ++half)
@@ -441,8 +467,17 @@ __global__ void __maxnreg__(96)
                          pack_bf16(ph[j + 6], ph[j + 7]));
           }
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarPhiQ]);
       // keys: phi(K) as hi + lo over K and in the lo buffer (rows past the
-      // prompt are zero, so they add nothing)
+      // prompt are zero, so they add nothing). The lo buffer held the
+      // previous segment's outputs: their store has read it before this
+      // thread reaches the next barrier, and every write follows that one.
+      if (threadIdx.x == 64) bulk_wait_read();
+      if (ok) ok = mbar_wait(&bar[kBarUk], s & 1, a.wait_limit);
+      tc_fence_after();
       tmem_ld16(tbase + lane_bits + kColA + 64 + 16 * sub, u);
       tmem_wait_ld();
       softmaxes();
@@ -510,14 +545,13 @@ __global__ void __maxnreg__(96)
           tmem_wait_ld();
         }
         if (w_own) {  // P = 2^{s - m} over the own block's keys held here
+          float mr = -FLT_MAX;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) mr = fmax3(mr, v32[j], v32[j + 1]);
+          m_t = mr * a.scale_log2;  // the scale is positive: max of scaled = scaled max
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            v32[j] *= a.scale_log2;
-            m_t = fmaxf(m_t, v32[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v32[j] = ex2_approx(v32[j] - m_t);
+            v32[j] = ex2_approx(fmaf(v32[j], a.scale_log2, -m_t));
             P_t += v32[j];
           }
         } else if (w_early) {
@@ -640,27 +674,34 @@ __global__ void __maxnreg__(96)
 
       // ---- E4: the state after this segment (its S update is done), then
       //      o = O1 + cN O2 for this thread's 32 columns of row r
-      if (ok) ok = mbar_wait(&bar[kBarO], s & 1, a.wait_limit);
+      // The state is read (and, after the last segment, stored) while O1
+      // runs; its bf16 copy for the next segment's O2 goes over C once O1
+      // has read C
       if (ok) ok = mbar_wait(&bar[kBarUpd], s & 1, a.wait_limit);
       tc_fence_after();
-      // its bf16 copy for the next segment's O2 (over C, which O1 has
-      // read), or, after the last segment, the fp32 state to the pool
       {
         float st[32];
         tmem_ld32(tbase + lane_bits + kColM + 32 * sub, st);
         tmem_wait_ld();
         if (s + 1 < n_seg) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(st[2 * j], st[2 * j + 1]);
+          if (ok) ok = mbar_wait(&bar[kBarO], s & 1, a.wait_limit);
+          tc_fence_after();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), pack_bf16(st[8 * q4], st[8 * q4 + 1]),
-                         pack_bf16(st[8 * q4 + 2], st[8 * q4 + 3]),
-                         pack_bf16(st[8 * q4 + 4], st[8 * q4 + 5]),
-                         pack_bf16(st[8 * q4 + 6], st[8 * q4 + 7]));
-        } else if (ok && commits) {
-          float4* dst = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD + r * kD + 32 * sub);
+            st_shared_v4(sS16 + tile_off(r, 4 * sub + q4), pk[4 * q4], pk[4 * q4 + 1],
+                         pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        } else {
+          if (ok && commits) {
+            float4* dst = reinterpret_cast<float4*>(a.S_pool + unit * kF * kD + r * kD + 32 * sub);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(st[4 * q4], st[4 * q4 + 1], st[4 * q4 + 2], st[4 * q4 + 3]);
+          }
+          if (ok) ok = mbar_wait(&bar[kBarO], s & 1, a.wait_limit);
+          tc_fence_after();
         }
       }
 
@@ -670,35 +711,40 @@ __global__ void __maxnreg__(96)
         tmem_ld16(tbase + lane_bits + kColS + 32 * sub + 16 * hf, o1);
         tmem_ld16(tbase + lane_bits + kColU + 32 * sub + 16 * hf, o2);
         tmem_wait_ld();
+        const float2 cN2 = make_float2(cN, cN);
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           const int j = 8 * q2;
+          uint32_t w4[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float2 ov = fma2(make_float2(o2[j + 2 * p], o2[j + 2 * p + 1]), cN2,
+                                   make_float2(o1[j + 2 * p], o1[j + 2 * p + 1]));
+            w4[p] = pack_bf16(ov.x, ov.y);
+          }
           // d columns 32 sub + 16 hf + 8 q2 .. + 7: chunk 4 sub + 2 hf + q2
-          st_shared_v4(sKlo + tile_off(r, 4 * sub + 2 * hf + q2),
-                       pack_bf16(fmaf(cN, o2[j], o1[j]), fmaf(cN, o2[j + 1], o1[j + 1])),
-                       pack_bf16(fmaf(cN, o2[j + 2], o1[j + 2]), fmaf(cN, o2[j + 3], o1[j + 3])),
-                       pack_bf16(fmaf(cN, o2[j + 4], o1[j + 4]), fmaf(cN, o2[j + 5], o1[j + 5])),
-                       pack_bf16(fmaf(cN, o2[j + 6], o1[j + 6]), fmaf(cN, o2[j + 7], o1[j + 7])));
+          st_shared_v4(sKlo + tile_off(r, 4 * sub + 2 * hf + q2), w4[0], w4[1], w4[2], w4[3]);
         }
       }
       // the segment's outputs: two TMA stores (rows past the prompt are
-      // clipped by the map); the lo buffer is handed on once they have read it
+      // clipped by the map), left in flight: the next segment waits for
+      // them to have read the lo buffer only before it writes phi(K) there
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 32 * kEpiWarps);
-      if (threadIdx.x == 64) {
-        if (ok) {
+      if (threadIdx.x == 64 && ok) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_store_4d(&maps.o, 64 * j, h, s * kSeg, b, smem + kOffKlo + j * 16384);
-          bulk_commit();
-          bulk_wait_read();
-        }
+        for (int j = 0; j < 2; ++j)
+          tma_store_4d(&maps.o, 64 * j, h, s * kSeg, b, smem + kOffKlo + j * 16384);
+        bulk_commit();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarE]);
     }
-    if (!ok && threadIdx.x == 64) atomicOr(a.status, kStatusTimeout);
+    if (threadIdx.x == 64) {
+      bulk_wait_read();  // the last outputs' store has read shared memory
+      if (!ok) atomicOr(a.status, kStatusTimeout);
+    }
   }
 
   tc_fence_before();
