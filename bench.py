@@ -918,8 +918,27 @@ def run_stack(args):
                 hb.hb_softmax_kv_attend(cfg, t["prefix_k"], t["prefix_v"], t["cu_prefix"], P,
                                         t["q"], t["k"], t["v"], o=ly["o"], workspace=ly["ws"])
 
+        # the same 6 layers as one launch (hb_block_attend_commit_layers,
+        # attend only): the layers' requests, states, maps and gates side by side
+        qa, ka, va = (torch.cat([ly["t"][n] for ly in layers]) for n in ("q", "k", "v"))
+        Wa = torch.stack([ly["t"]["W"] for ly in layers])
+        ga = torch.stack([ly["t"]["gate"] for ly in layers])
+        Sa = torch.cat([ly["S"] for ly in layers])
+        Za = torch.cat([ly["Z"] for ly in layers])
+        sla = torch.arange(N_LAYERS * nB, dtype=torch.int32, device=device)
+        oa = torch.empty_like(qa)
+
+        def hybrid_layers():
+            hb.hb_block_attend_commit_layers(cfg, sla, qa, ka, va, Sa, Za, Wa, ga, None, o=oa)
+
+        hybrid()
+        hybrid_layers()
+        torch.cuda.synchronize()
+        assert torch.equal(oa, torch.cat([ly["o"] for ly in layers]))
+
         reps = max(3, min(args.steps, 200))
         h_ms = _graph_ms(hybrid, 1, reps, args.warmup, stream)
+        hl_ms = _graph_ms(hybrid_layers, 1, reps, args.warmup, stream)
         h16_ms = _graph_ms(hybrid_s16, 1, reps, args.warmup, stream)
         h8_ms = _graph_ms(hybrid_s8, 1, reps, args.warmup, stream)
         s_ms = _graph_ms(softmax, 1, max(3, reps // 4), args.warmup, stream)
@@ -939,6 +958,11 @@ def run_stack(args):
             "softmax_kv_gbs": sm_bytes / (s_ms / 1e3) / 1e9,
             "hybrid_frac": hb_bytes / (h_ms / 1e3) / 1e9 / peak,
             "softmax_kv_frac": sm_bytes / (s_ms / 1e3) / 1e9 / peak,
+            "hybrid_layers_ms": hl_ms, "hybrid_layers_tokens_per_s": nB * L / (hl_ms / 1e3),
+            "hybrid_layers_frac": hb_bytes / (hl_ms / 1e3) / 1e9 / peak,
+            "layers_speedup": h_ms / hl_ms,
+            "layers_note": "the 6 layers' attends as one launch (hb_block_attend_commit_layers), "
+                           "output bit-identical to the 6 launches",
             "hybrid_s16_ms": h16_ms, "hybrid_s16_tokens_per_s": nB * L / (h16_ms / 1e3),
             "hybrid_s16_frac": hb16_bytes / (h16_ms / 1e3) / 1e9 / peak,
             "s16_speedup": h_ms / h16_ms,
@@ -950,7 +974,7 @@ def run_stack(args):
             "s8_note": "attend only, on fp8 copies written once before timing (lossy: the "
                        "output is the attend on the dequantised state)",
         })
-        del layers
+        del layers, qa, ka, va, Wa, ga, Sa, Za, oa
         torch.cuda.empty_cache()
     top = sweep[-1]
     return {

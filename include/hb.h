@@ -252,6 +252,42 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch,
                                  hb_stream_t stream);
 
 /*
+ * hb_block_attend_commit_layers — the fused step (hb_block_attend_commit) of
+ * n_layers independent linearized layers in one launch. The pages' model
+ * linearizes several attention layers (gist.science, "How They Did It: The
+ * Two-Stage Upgrade", Stage 1: six of its twenty attention layers are
+ * replaced; pith.science, "Extended reading notes", Core claim), each with
+ * its own feature map, gate and states. In a forward pass the layers run one
+ * after another; their steps are independent only when their inputs are
+ * ready together (micro-batches at different layers, or a stack of
+ * synthetic layers), and then one launch spreads all of them over the GPU
+ * instead of one launch per layer.
+ *   n_layers     >= 1; the call holds n_layers x batch requests, request
+ *                r = l * batch + b being layer l's request b
+ *   slot_idx     [n_layers * batch] int32: each request's slot in the one
+ *                pool shared by the layers (the caller keeps them apart)
+ *   q, k, v, o   [n_layers * batch, L, H, d] activation dtype
+ *   S_pool, Z_pool  as in hb_block_attend_commit
+ *   W            [n_layers, H, d, f]: layer l's feature maps
+ *   gate_logits  [n_layers, H] fp32: layer l's gates
+ *   commit       [n_layers * batch] int32, or NULL: attend only (the pools
+ *                are then only read)
+ * Equal, request by request, to n_layers calls of hb_block_attend_commit
+ * (hb_block_attend when commit is NULL) on each layer's slice; a committing
+ * request's slot must not be read by any other request of the call. The
+ * production shape (bf16, d = 128, f = 64, L = 32 or 16) runs as one
+ * launch; other shapes run as one call per layer, in layer order.
+ */
+hb_status hb_block_attend_commit_layers(const hb_config* cfg, int32_t n_layers,
+                                        int32_t batch, const int32_t* slot_idx,
+                                        const void* q, const void* k, const void* v,
+                                        float* S_pool, float* Z_pool,
+                                        int32_t num_slots, const void* W,
+                                        const float* gate_logits,
+                                        const int32_t* commit, void* o,
+                                        hb_stream_t stream);
+
+/*
  * hb_block_attend_commit_s16 — hb_block_attend_commit for a pool that keeps,
  * beside every slot's fp32 master S, the bf16 copy hb_state_to_bf16 writes
  * (gist.science technical summary, state-compression bullet: the state is

@@ -15,6 +15,7 @@ from .hb import (  # noqa: F401
     HBError,
     hb_block_attend,
     hb_block_attend_commit,
+    hb_block_attend_commit_layers,
     hb_block_attend_commit_s16,
     hb_block_attend_ex,
     hb_commit_block,

@@ -50,6 +50,10 @@ SIGNATURES = {
     "hb_block_attend_commit": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p]),
+    "hb_block_attend_commit_layers": (c_int32, [_P, c_int32, c_int32, c_void_p, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p,
+                                                c_int32, c_void_p, c_void_p, c_void_p,
+                                                c_void_p, c_void_p]),
     "hb_block_attend_commit_s16": (c_int32, [_P, c_int32, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),

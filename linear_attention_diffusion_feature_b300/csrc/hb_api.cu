@@ -283,6 +283,49 @@ hb_status hb_block_attend_commit(const hb_config* cfg, int32_t batch, const int3
                                                         S_pool, Z_pool, num_slots, status, st));
 }
 
+hb_status hb_block_attend_commit_layers(const hb_config* cfg, int32_t n_layers, int32_t batch,
+                                        const int32_t* slot_idx, const void* q, const void* k,
+                                        const void* v, float* S_pool, float* Z_pool,
+                                        int32_t num_slots, const void* W,
+                                        const float* gate_logits, const int32_t* commit, void* o,
+                                        hb_stream_t stream) {
+  Shape s;
+  hb_status r = hb::check_config(cfg, &s);
+  if (r != HB_OK) return r;
+  if (n_layers < 1 || batch < 0 || num_slots < 0) return HB_ERR_INVALID_ARG;
+  if (batch == 0) return HB_OK;
+  const int64_t total = (int64_t)n_layers * batch;
+  if (total > 65535 * 32) return HB_ERR_UNSUPPORTED_SHAPE;
+  if ((r = hb::check_ptrs({slot_idx, q, k, v, S_pool, Z_pool, W, gate_logits, o})) != HB_OK)
+    return r;
+  unsigned* status = nullptr;
+  if (hb::status_word_ptr(&status) != cudaSuccess) return HB_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (hb::fast_attend_step_ok(s) && hb::attend_fast_fits(s, (int)total, num_slots, s.L))
+    return hb::from_cuda(hb::launch_attend_layers(s, n_layers, (int)total, slot_idx, q, k, v,
+                                                  S_pool, Z_pool, num_slots, W, gate_logits,
+                                                  commit, o, status, st));
+  // other shapes: one call per layer, in layer order
+  const size_t es = cfg->dtype == HB_DTYPE_BF16 ? 2 : 4;
+  const size_t act = (size_t)batch * s.L * s.H * s.d * es;
+  const size_t wl = (size_t)s.H * s.d * s.f * es;
+  for (int l = 0; l < n_layers; ++l) {
+    const size_t b0 = (size_t)l * batch;
+    const char* ql = static_cast<const char*>(q) + l * act;
+    const char* kl = static_cast<const char*>(k) + l * act;
+    const char* vl = static_cast<const char*>(v) + l * act;
+    char* ol = static_cast<char*>(o) + l * act;
+    const char* Wl = static_cast<const char*>(W) + l * wl;
+    const float* gl = gate_logits + (size_t)l * s.H;
+    r = commit ? hb_block_attend_commit(cfg, batch, slot_idx + b0, ql, kl, vl, S_pool, Z_pool,
+                                        num_slots, Wl, gl, commit + b0, ol, stream)
+               : hb_block_attend(cfg, batch, slot_idx + b0, ql, kl, vl, S_pool, Z_pool,
+                                 num_slots, Wl, gl, ol, stream);
+    if (r != HB_OK) return r;
+  }
+  return HB_OK;
+}
+
 hb_status hb_block_attend_commit_s16(const hb_config* cfg, int32_t batch,
                                      const int32_t* slot_idx, const void* q, const void* k,
                                      const void* v, float* S_pool, void* S16_pool,

@@ -99,7 +99,8 @@ constexpr int kOffPart = kOffZ + 1024;      // max, min of u(q); max of s; max, 
 constexpr int kOffZPart = kOffPart + 5 * 512;  // column sums of phi(k) per row tile: [2][128]
 constexpr int kOffFin = kOffZPart + 1024;   // merge coefficients per stage: 2 x 3 x [32]
 constexpr int kOffBar = kOffFin + 2 * 3 * 128;
-constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head, fp8 scale
+constexpr int kOffMeta = kOffBar + 13 * 8;  // per stage: flags, slot, request, head, fp8 scale,
+                                             // the head's row of W / gate (layer * H + head)
 constexpr int kOffTmemSlot = kOffMeta + 48;
 // committing variant: the commit mask as one bit per request, 32 per word
 constexpr int kMaskWords = 1024;  // batches up to 32768 are scheduled commit-first
@@ -119,6 +120,10 @@ struct Maps {
   // the prompt length and the block's offset for chunkwise prompt
   // processing); commit_all: every request commits (commit_mask unused).
   int rows_per_req, row_base, commit_all;
+  // several independent layers in one call: request b belongs to layer
+  // b / reqs_per_layer, whose head h takes row layer * H + h of W and gate
+  // (one layer: reqs_per_layer = batch)
+  int reqs_per_layer, n_layers;
   // grouped-query heads (attend only): query head h reads k, v, S and Z of
   // head h / kv_group (1: one key/value head per query head)
   int kv_group;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     const size_t q_bytes = (size_t)batch * maps.rows_per_req * H * kD * 2;
     const size_t kv_bytes = q_bytes / maps.kv_group;  // k, v have H / kv_group heads
-    const size_t w_bytes = (size_t)H * kD * kFH * 2;
+    const size_t w_bytes = (size_t)maps.n_layers * H * kD * kFH * 2;
     if (q_bytes + 2 * kv_bytes + w_bytes <= kPrefetchBudget) {
       const uint8_t* base[4] = {maps.qkv[0], maps.qkv[1], maps.qkv[2], maps.w};
 #pragma unroll
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int h = meta[6 + s];
-      const float gl = gate[h];
+      const float gl = gate[meta[10 + s]];
       if (meta[s] & kUnitValid) {
         const float* sums = reinterpret_cast<const float*>(smem + s * kStageStride + kOffSums);
         float* fin = fin_all + s * 96;
@@ -451,9 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, h, row, &head_full[s]);
             tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, h, row, &head_full[s]);
           }
-          tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
+          const int wh = (b / maps.reqs_per_layer) * H + h;
+          tma_load_2d(st + kOffW, &maps.W, 0, wh * kD, &head_full[s]);
           meta[4 + s] = b;
           meta[6 + s] = h;
+          meta[10 + s] = wh;
           if (bad) {
             meta[s] = 0;
             mbar_arrive(&head_full[s]);
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i == 0) {
               if (maps.sep_wk) {  // the key map, kept for the whole walk
                 mbar_expect_tx(&head_full[s], 16384);
-                tma_load_2d(smem + kStageStride + kOffS, &maps.Wk, 0, h * kD, &head_full[s]);
+                tma_load_2d(smem + kStageStride + kOffS, &maps.Wk, 0, wh * kD, &head_full[s]);
               }
               mbar_expect_tx(&head_full[s], 512);
               bulk_load(smem + kOffZ, Z_pool + (size_t)(slot * H + h) * kF, 512, &head_full[s]);
@@ -615,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + kOffK + j * 4096, &maps.k, 64 * j, g, row, &head_full[s]);
           tma_load_3d(st + kOffV + j * 4096, &maps.v, 64 * j, g, row, &head_full[s]);
         }
-        tma_load_2d(st + kOffW, &maps.W, 0, h * kD, &head_full[s]);
+        tma_load_2d(st + kOffW, &maps.W, 0, ((b / maps.reqs_per_layer) * H + h) * kD,
+                    &head_full[s]);
       }
     };
     auto issue_state = [&](int i) {
@@ -630,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[4 + s] = b;
         meta[6 + s] = h;
         meta[8 + s] = __float_as_int(scale);
+        meta[10 + s] = (b / maps.reqs_per_layer) * H + h;
         if (flags < 0 || slot < 0 || slot >= num_slots) {
           atomicOr(status, kStatusBounds);
           meta[s] = 0;
@@ -1298,7 +1307,8 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
                                unsigned* status, cudaStream_t st, int rows_per_req, int row_base,
                                bool commit_all, bool sequential, bool state_bf16,
                                void* S16_pool = nullptr, int Hkv = -1,
-                               const void* Wk = nullptr, const float* s8_scale = nullptr) {
+                               const void* Wk = nullptr, const float* s8_scale = nullptr,
+                               int n_layers = 1) {
   const bool dual = S16_pool != nullptr;
   // the fp8 copy (with its per-(slot, head) scales) is read by the attend only
   const bool fp8 = s8_scale != nullptr;
@@ -1313,7 +1323,12 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
   if (sep_wk && !sequential) return cudaErrorInvalidValue;
   // blocks of 16 tokens in a decoding step; prompts walk 32-token blocks
   if (sequential ? s.L != kL : (s.L != kL && s.L != 16)) return cudaErrorInvalidValue;
+  // independent layers: batch = n_layers x the requests of one layer
+  if (n_layers < 1 || batch % n_layers != 0 || (n_layers > 1 && sequential))
+    return cudaErrorInvalidValue;
   Maps maps;
+  maps.n_layers = n_layers;
+  maps.reqs_per_layer = batch > 0 ? batch / n_layers : 1;
   maps.valid_rows = sequential ? kL : s.L;
   maps.kv_group = s.H / Hkv;
   maps.sep_wk = sep_wk ? 1 : 0;
@@ -1364,7 +1379,7 @@ cudaError_t launch_attend_impl(const Shape& s, int batch, const int32_t* slot_id
     }
   }
   {
-    const uint64_t dims[2] = {(uint64_t)kFH, (uint64_t)s.H * kD};
+    const uint64_t dims[2] = {(uint64_t)kFH, (uint64_t)n_layers * s.H * kD};
     const uint64_t strides[1] = {kFH * 2};
     const uint32_t box[2] = {64, 128};
     if (!encode_tmap(&maps.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dims, strides, box,
@@ -1414,6 +1429,16 @@ cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_id
   return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
                             commit_mask, o, status, st, rows_per_req, row_base, commit_all,
                             sequential, false, nullptr, Hkv, Wk);
+}
+
+cudaError_t launch_attend_layers(const Shape& s, int n_layers, int batch, const int32_t* slot_idx,
+                                 const void* q, const void* k, const void* v, float* S_pool,
+                                 float* Z_pool, int num_slots, const void* W, const float* gate,
+                                 const int32_t* commit_mask, void* o, unsigned* status,
+                                 cudaStream_t st) {
+  return launch_attend_impl(s, batch, slot_idx, q, k, v, S_pool, Z_pool, num_slots, W, gate,
+                            commit_mask, o, status, st, s.L, 0, false, false, false, nullptr, -1,
+                            nullptr, nullptr, n_layers);
 }
 
 cudaError_t launch_attend_fast_s16(const Shape& s, int batch, const int32_t* slot_idx,

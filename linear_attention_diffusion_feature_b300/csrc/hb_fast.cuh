@@ -53,6 +53,14 @@ cudaError_t launch_feature_map_fast(const Shape& s, int64_t n, const void* x, co
 // and query head h reads head h / (H / Hkv); W is the query map [H, d, f].
 // Wk (sequential mode only): a separate key map [H, d, f] for the commits.
 bool attend_fast_fits(const Shape& s, int batch, int num_slots, int64_t rows_per_req);
+// Several independent layers in one launch (n_layers x the requests of one
+// layer; request b takes row (b / (batch / n_layers)) * H + h of W and gate).
+// commit_mask null: attend only.
+cudaError_t launch_attend_layers(const Shape& s, int n_layers, int batch, const int32_t* slot_idx,
+                                 const void* q, const void* k, const void* v, float* S_pool,
+                                 float* Z_pool, int num_slots, const void* W, const float* gate,
+                                 const int32_t* commit_mask, void* o, unsigned* status,
+                                 cudaStream_t st);
 cudaError_t launch_attend_fast(const Shape& s, int batch, const int32_t* slot_idx, const void* q,
                                const void* k, const void* v, const float* S_pool,
                                const float* Z_pool, int num_slots, const void* W,

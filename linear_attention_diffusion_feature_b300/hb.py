@@ -255,6 +255,38 @@ def hb_block_attend_commit(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W, ga
     return o
 
 
+def hb_block_attend_commit_layers(cfg: Config, slot_idx, q, k, v, S_pool, Z_pool, W,
+                                  gate_logits, commit=None, o=None, stream=None) -> torch.Tensor:
+    """The fused step of several independent layers in one call: W is
+    [n_layers, H, d, f], gate_logits [n_layers, H]; q, k, v, o, slot_idx and
+    commit (None: attend only) hold n_layers x batch requests, layer by
+    layer."""
+    Lyr = W.shape[0] if W.dim() == 4 else 0
+    R = slot_idx.shape[0]
+    H, d, f, L = cfg.num_heads, cfg.head_dim, cfg.feat_half, cfg.block_len
+    if Lyr < 1 or R % Lyr != 0:
+        raise ValueError("W must be [n_layers, H, d, f] with n_layers dividing the requests")
+    B = R // Lyr
+    _check(slot_idx, "slot_idx", torch.int32, (R,))
+    if commit is not None:
+        _check(commit, "commit", torch.int32, (R,))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, cfg.torch_dtype, (R, L, H, d))
+    num_slots = _check_state(cfg, S_pool, Z_pool)
+    _check(W, "W", cfg.torch_dtype, (Lyr, H, d, f))
+    _check(gate_logits, "gate_logits", torch.float32, (Lyr, H))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", cfg.torch_dtype, (R, L, H, d))
+    lib = _lib.load()
+    _raise(lib.hb_block_attend_commit_layers(
+        ctypes.byref(cfg.c()), Lyr, B, _ptr(slot_idx), _ptr(q), _ptr(k), _ptr(v), _ptr(S_pool),
+        _ptr(Z_pool), num_slots, _ptr(W), _ptr(gate_logits),
+        _ptr(commit), _ptr(o), _stream(stream)),
+        "hb_block_attend_commit_layers")
+    return o
+
+
 def hb_block_attend_commit_s16(cfg: Config, slot_idx, q, k, v, S_pool, S16_pool, Z_pool, W,
                                gate_logits, commit, o=None, stream=None) -> torch.Tensor:
     """hb_block_attend_commit on a pool with bf16 copies beside the fp32
