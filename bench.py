@@ -354,6 +354,7 @@ def run_ours(args, world, rank, local):
     nvtx.range_pop()
     nvtx.range_push("dual_copy")
     dual = component_dual_copy(args, cfg, layers, stream)
+    step_layers = component_step_layers(args, cfg, layers, stream) if world == 1 else None
     nvtx.range_pop()
     del layers
     torch.cuda.empty_cache()
@@ -367,6 +368,7 @@ def run_ours(args, world, rank, local):
         "attend_only_clocks": attend_clocks,
         "commit_cost_ms": step_launch_ms - attend_only_ms,
         "step_dual_copy": dual,
+        "step_6_layers_one_launch": step_layers,
     }
     if world == 1 and not args.no_components:
         nvtx.range_push("components")
@@ -464,6 +466,62 @@ def component_dual_copy(args, cfg, layers, stream):
         "timing": "graphs of 600 steps (layers in turn), replayed for >= 0.5 s each",
     })
     return out
+
+
+def component_step_layers(args, cfg, layers, stream):
+    """The 6 layer instances' continuous-batching steps (64 requests each, 16
+    committing) as one launch of hb_block_attend_commit_layers: the layers'
+    requests, pools, maps, gates and commit masks side by side (copies, so the
+    per-layer instances are untouched). For layers whose steps are ready
+    together; in a forward pass the layers run in turn. Graphs of 100
+    launches, replayed for >= 0.5 s."""
+    import linear_attention_diffusion_feature_b300 as hb
+
+    peak, _ = _peaks()
+    qa, ka, va = (torch.cat([ly[n] for ly in layers]) for n in ("q", "k", "v"))
+    Wa = torch.stack([ly["W"] for ly in layers])
+    ga = torch.stack([ly["gate"] for ly in layers])
+    Sa = torch.cat([ly["S"] for ly in layers])
+    Za = torch.cat([ly["Z"] for ly in layers])
+    n_sl = layers[0]["S"].shape[0]
+    sla = torch.cat([ly["slots"] + i * n_sl for i, ly in enumerate(layers)]).to(torch.int32)
+    ma = torch.cat([ly["mask"] for ly in layers])
+    oa = torch.empty_like(qa)
+
+    def step():
+        hb.hb_block_attend_commit_layers(cfg, sla, qa, ka, va, Sa, Za, Wa, ga, ma, o=oa)
+
+    for _ in range(args.warmup):
+        step()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(100):
+            step()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n_rep = max(1, int(500.0 / a.elapsed_time(b)) + 1)
+    a.record(stream)
+    for _ in range(n_rep):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (n_rep * 100)
+    assert hb.hb_get_device_status() == 0
+    nbytes = N_LAYERS * STEP_BYTES  # each layer's W is read once, as in one layer's step
+    del g, qa, ka, va, Wa, ga, Sa, Za, sla, ma, oa
+    torch.cuda.empty_cache()
+    return {"workload": "6 layers x (64 requests, 16 committing) in one launch",
+            "ms": ms, "per_layer_ms": ms / N_LAYERS,
+            "tokens_per_s": N_LAYERS * B * L / (ms / 1e3),
+            "algorithmic_bytes_per_launch": nbytes,
+            "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peak,
+            "timing": "graphs of 100 launches, replayed for >= 0.5 s"}
 
 
 def component_stack(args, device, nB: int = 256, P: int = 2048):
