@@ -17,7 +17,8 @@
 //            its chunk is done;
 //   warp 1   owns TMEM (512 columns) and issues tcgen05.mma from one thread:
 //              U    [128 tok x 64]  = K W_h            (A K-major, B MN-major)
-//              Sacc [128 F x 128 d] += phi^T V          (A, B MN-major)
+//              Sacc^T [128 d x 256] += V^T [phi_hi | phi_lo]  (A, B MN-major;
+//                   V is read once for both halves of the split)
 //            U is double-buffered, so the next chunk's K W_h overlaps the
 //            epilogue of the current one, and phi^T V runs per half-chunk
 //            (tokens 0-63, then 64-127) as soon as that half of phi is
@@ -30,9 +31,10 @@
 //            tensor cores take bf16 operands; v is exact in bf16. Z is summed
 //            from the same fp32 phi values in registers and reduced across
 //            threads once at the end.
-// At the end the epilogue reads Sacc/Zacc (thread = row of S), stages the
-// tile through swizzled shared memory and writes S/Z (or a partial sum for
-// the fixed-order split reduction) with coalesced 16-byte stores.
+// At the end the epilogue reads Sacc^T (thread = column d of S, adding the
+// hi and lo halves) and the Z sums, stages the tile through swizzled shared
+// memory as [F][d] and writes S/Z (or a partial sum for the fixed-order split
+// reduction) with coalesced 16-byte stores.
 #include <float.h>
 
 #include "hb_fast.cuh"
@@ -66,6 +68,9 @@ enum { kKFull0 = 0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVE
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
+// S^T (lane = d) as two accumulators side by side: columns 0-127 take the
+// phi hi products, 128-255 the phi lo ones (summed when read out); U is
+// double-buffered in 256-383
 constexpr uint32_t kColS = 0, kColU = 256;
 
 constexpr int kPartialFloats = kF * kD + kF;  // one partial state: S then Z
@@ -249,10 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && n_my > 0) {
       constexpr uint32_t idU = umma_idesc_bf16(128, kFH, 0, 1);
-      constexpr uint32_t idS = umma_idesc_bf16(128, kD, 1, 1);
+      // S^T [d x (F hi | F lo)] += V^T [phi_hi | phi_lo]: V is read once per
+      // step for both halves of the split (M = d = 128, N = 2F = 256)
+      constexpr uint32_t idS = umma_idesc_bf16(128, 2 * kF, 1, 1);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sW = smem_u32(smem + kOffW);
-      const uint32_t sHi = smem_u32(smem + kOffPhiHi), sLo = smem_u32(smem + kOffPhiLo);
+      const uint32_t sHi = smem_u32(smem + kOffPhiHi);
+      static_assert(kOffPhiLo == kOffPhiHi + 32768, "phi lo follows phi hi: one N = 256 operand");
       bool ok = mbar_wait(&bar[kWFull], 0);
       // Sacc += phi^T V for chunk cc, tokens 0-63 (half 0, k16 steps 0-3) as
       // soon as their phi rows are written, then tokens 64-127, so the next
@@ -269,11 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int ks_end = ksteps < 4 * (half + 1) ? ksteps : 4 * (half + 1);
           for (int ks = 4 * half; ks < ks_end; ++ks) {
-            const uint64_t aHi = umma_desc_sw128(sHi + ks * 2048, 16384, 1024);
-            const uint64_t aLo = umma_desc_sw128(sLo + ks * 2048, 16384, 1024);
-            const uint64_t bV = umma_desc_sw128(vb + ks * 2048, 16384, 1024);
-            umma_bf16(tbase + kColS, aHi, bV, idS, (cc == 0 && ks == 0) ? 0u : 1u);
-            umma_bf16(tbase + kColS, aLo, bV, idS, 1u);
+            // A = V^T (MN-major, two 64-column boxes 16 KiB apart); B = phi
+            // hi then lo (MN-major, four 64-column atoms 16 KiB apart: the lo
+            // buffer follows the hi buffer)
+            const uint64_t aV = umma_desc_sw128(vb + ks * 2048, 16384, 1024);
+            const uint64_t bP = umma_desc_sw128(sHi + ks * 2048, 16384, 1024);
+            umma_bf16(tbase + kColS, aV, bP, idS, (cc == 0 && ks == 0) ? 0u : 1u);
           }
           umma_commit(&bar[kPhiEmptyA + half]);
         }
@@ -466,20 +475,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t stage = smem_u32(smem + kOffPhiHi);  // 64 KiB, free once the MMAs are done
     {
-      float r[32];
-      if (have && n_my > 0) {
-        tmem_ld32(tbase + lane_bits + kColS + 32 * sub, r);
-        tmem_wait_ld();
-      } else {
+      // The accumulator is S^T: lane = d (= tok here), columns F of the hi
+      // half then of the lo half. This thread holds S[f][d] for its d and
+      // f = 32 sub .. 32 sub + 31, the sum of the two halves, and writes it
+      // into row f of the staged [F][d] tile (a warp's 32 d of one row are
+      // 8 distinct 16-byte chunks: no bank conflict).
+      const int dcol = tok;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = 0.f;
-      }
+      for (int hh = 0; hh < 2; ++hh) {
+        float rh[16], rl[16];
+        if (have && n_my > 0) {
+          tmem_ld16(tbase + lane_bits + kColS + 32 * sub + 16 * hh, rh);
+          tmem_ld16(tbase + lane_bits + kColS + kF + 32 * sub + 16 * hh, rl);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        const int chunk = 8 * sub + q4;
-        st_shared_v4(stage + tok * 512 + ((chunk ^ (tok & 31)) << 4), __float_as_uint(r[4 * q4]),
-                     __float_as_uint(r[4 * q4 + 1]), __float_as_uint(r[4 * q4 + 2]),
-                     __float_as_uint(r[4 * q4 + 3]));
+          for (int j = 0; j < 16; ++j) rh[j] = rl[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int f = 32 * sub + 16 * hh + j;
+          st_shared_u32(stage + f * 512 + ((((dcol >> 2) ^ (f & 31)) << 4) | ((dcol & 3) << 2)),
+                        __float_as_uint(rh[j] + rl[j]));
+        }
       }
     }
     // Z: reduce-scatter the 32 column sums across the warp's lanes (lane j
