@@ -99,6 +99,34 @@ def test_attend_pointer_checks(lib):
                                None, None, None) == 0
 
 
+def test_attend_layers_checks(lib):
+    c = _cfg()
+    f = lib.hb_block_attend_commit_layers
+    # n_layers must be >= 1
+    assert f(ctypes.byref(c), 0, 2, A, A, A, A, A, A, 4, A, A, A, A, None) == 1
+    assert f(ctypes.byref(c), -3, 2, A, A, A, A, A, A, 4, A, A, A, A, None) == 1
+    # a null or misaligned operand; the commit mask may be null (attend only)
+    assert f(ctypes.byref(c), 6, 2, A, A, None, A, A, A, 4, A, A, A, A, None) == 1
+    assert f(ctypes.byref(c), 6, 2, A, A, A, A, M, A, 4, A, A, A, A, None) == 3
+    assert f(ctypes.byref(c), 6, -1, A, A, A, A, A, A, 4, A, A, A, A, None) == 1
+    # more requests in one call than the kernels index
+    assert f(ctypes.byref(c), 64, 65535, A, A, A, A, A, A, 4, A, A, A, A, None) == 2
+    # batch 0 is a no-op
+    assert f(ctypes.byref(c), 6, 0, None, None, None, None, None, None, 0, None, None, None,
+             None, None) == 0
+
+
+def test_attend_layers_binding_rejects_a_ragged_split():
+    import torch
+
+    import linear_attention_diffusion_feature_b300 as hb
+    cfg = hb.Config(16, 128, 64, 32)
+    W = torch.zeros((3, 16, 128, 64), dtype=torch.bfloat16)
+    sl = torch.zeros((8,), dtype=torch.int32)  # 8 requests do not split into 3 layers
+    with pytest.raises(ValueError):
+        hb.hb_block_attend_commit_layers(cfg, sl, None, None, None, None, None, W, None)
+
+
 def test_commit_and_zero_checks(lib):
     c = _cfg()
     assert lib.hb_commit_block(ctypes.byref(c), 2, A, A, None, A, A, A, 4, None) == 1
