@@ -122,6 +122,35 @@ def test_layers_equal_one_call_per_layer(cuda_device, with_commit, dt, d):
         assert torch.equal(S, S0) and torch.equal(Z, Z0)
 
 
+@pytest.mark.parametrize("n_layers,L,mask", [(1, 32, "some"), (3, 16, "all"), (4, 32, "none")])
+def test_layers_edge_cases(cuda_device, n_layers, L, mask):
+    """One layer (the plain fused step), 16-token blocks with every request
+    committing, and a commit mask of zeros: bit for bit what per-layer calls
+    give."""
+    B = 20
+    c = _case(torch.bfloat16, n_layers=n_layers, B=B, L=L, seed=970 + n_layers, max_prefix=48)
+    if mask == "all":
+        c["commit"] = torch.ones(c["R"], dtype=torch.int32)
+    elif mask == "none":
+        c["commit"] = torch.zeros(c["R"], dtype=torch.int32)
+    cfg = _cfg(c, torch.bfloat16, "convex")
+    S, Z = _pool(c, cfg, cuda_device)
+    S2, Z2 = S.clone(), Z.clone()
+    dev = lambda x: x.to(cuda_device)  # noqa: E731
+    sl = dev(c["slot_of"].to(torch.int32))
+    q, k, v, W, gate = dev(c["q"]), dev(c["k"]), dev(c["v"]), dev(c["W"]), dev(c["gate"])
+    cm = dev(c["commit"])
+    o = hb.hb_block_attend_commit_layers(cfg, sl, q, k, v, S, Z, W, gate, cm)
+    o2 = torch.empty_like(o)
+    for lyr in range(n_layers):
+        r = slice(lyr * B, (lyr + 1) * B)
+        hb.hb_block_attend_commit(cfg, sl[r], q[r], k[r], v[r], S2, Z2, W[lyr], gate[lyr], cm[r],
+                                  o=o2[r])
+    assert_status_ok()
+    assert torch.equal(o, o2)
+    assert torch.equal(S, S2) and torch.equal(Z, Z2)
+
+
 def test_layers_reject_bad_shapes(cuda_device):
     c = _case(torch.bfloat16, n_layers=2, B=4, L=32, seed=960, max_prefix=8)
     cfg = _cfg(c, torch.bfloat16, "shared_norm")
